@@ -1,0 +1,166 @@
+"""fp64 CPU oracle for Longformer-style attention -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its Python binding) never loads it, and it loads nothing of theirs.
+
+The arithmetic lives in ``lf_oracle.c`` (plain C, double precision, one loop
+per output row); this module only builds it with gcc and marshals arrays.
+See that file's header for the pattern definitions and the readings taken
+where the pages (velog.io/@lainshower/Longformer, sections 3-1 and 4.1) are
+silent.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "lf_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liblf_oracle.so")
+_lib = None
+
+_F64, _F32, _BF16 = 0, 1, 2
+
+
+def build(force: bool = False) -> str:
+    """Compile lf_oracle.c into liblf_oracle.so next to it (gcc, OpenMP)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        P = ctypes.c_void_p
+        i32 = ctypes.c_int32
+        lib.lf_oracle_fwd.argtypes = [ctypes.c_int, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
+                                      P, i32, P, P, ctypes.c_int64, P, i32]
+        lib.lf_oracle_fwd.restype = ctypes.c_int
+        lib.lf_oracle_attended.argtypes = [P, i32, i32, i32, i32, i32, P, i32, P, i32, i32, i32, P, P]
+        lib.lf_oracle_attended.restype = i32
+        lib.lf_oracle_max_threads.restype = i32
+        _lib = lib
+    return _lib
+
+
+def _as_array(x):
+    """-> (contiguous numpy array, dtype code).  bf16 torch tensors keep their bits."""
+    if x is None:
+        return None, None
+    try:
+        import torch
+
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu().contiguous()
+            if x.dtype == torch.bfloat16:
+                return x.view(torch.int16).numpy().view(np.uint16), _BF16
+            x = x.numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float64:
+        return x, _F64
+    if x.dtype == np.float32:
+        return x, _F32
+    if x.dtype == np.uint16:
+        return x, _BF16
+    raise TypeError("oracle inputs must be float64, float32 or bf16, got %s" % x.dtype)
+
+
+def _i32(seq) -> Optional[np.ndarray]:
+    if seq is None:
+        return None
+    return np.ascontiguousarray(np.asarray(list(seq), dtype=np.int32))
+
+
+def _ptr(a) -> Optional[int]:
+    return None if a is None else a.ctypes.data
+
+
+def max_threads() -> int:
+    return int(_load().lf_oracle_max_threads())
+
+
+def fwd(q, k, v, *, w: int, dilation: Optional[Sequence[int]] = None, causal: bool = False,
+        pad_len: Optional[Sequence[int]] = None, qg=None, kg=None, vg=None,
+        global_idx: Sequence[int] = (), rows: Optional[Sequence[int]] = None,
+        threads: int = 0) -> np.ndarray:
+    """Attention output in float64.
+
+    q, k, v, kg, vg: [B, H, n, d]; qg: [B, H, G, d] (row r belongs to
+    global_idx[r]).  All inputs share one dtype (float64, float32 or bf16).
+    rows: optional flat row ids ((b*H + h)*n + i); then the result is
+    [len(rows), d] instead of [B, H, n, d].
+    """
+    lib = _load()
+    qa, code = _as_array(q)
+    ka, kc = _as_array(k)
+    va, vc = _as_array(v)
+    if not (code == kc == vc):
+        raise TypeError("q, k, v must share a dtype")
+    B, H, n, d = qa.shape
+    G = len(global_idx)
+    qga = kga = vga = None
+    if G:
+        qga, c1 = _as_array(qg)
+        kga, c2 = _as_array(kg)
+        vga, c3 = _as_array(vg)
+        if not (c1 == c2 == c3 == code):
+            raise TypeError("qg, kg, vg must share q's dtype")
+        if qga.shape != (B, H, G, d) or kga.shape != qa.shape or vga.shape != qa.shape:
+            raise ValueError("global tensor shapes do not match")
+    if ka.shape != qa.shape or va.shape != qa.shape:
+        raise ValueError("q, k, v shapes differ")
+    dil = _i32(dilation if dilation is not None else [1] * H)
+    if len(dil) != H:
+        raise ValueError("dilation needs one entry per head")
+    gidx = _i32(global_idx) if G else None
+    pads = _i32(pad_len)
+    rws = None
+    if rows is not None:
+        rws = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        out = np.zeros((len(rws), d), dtype=np.float64)
+    else:
+        out = np.zeros((B, H, n, d), dtype=np.float64)
+    rc = lib.lf_oracle_fwd(code, _ptr(qa), _ptr(ka), _ptr(va), _ptr(qga), _ptr(kga), _ptr(vga),
+                           _ptr(gidx), G, B, H, n, d, int(w), _ptr(dil), int(bool(causal)),
+                           _ptr(pads), _ptr(rws), 0 if rws is None else len(rws), _ptr(out),
+                           int(threads))
+    if rc != 0:
+        raise ValueError("oracle rejected the problem (code %d)" % rc)
+    return out
+
+
+def attended(*, n: int, w: int, dilation: Sequence[int], causal: bool = False,
+             global_idx: Sequence[int] = (), pad_len: Optional[Sequence[int]] = None,
+             b: int = 0, h: int = 0, i: int = 0, B: int = 1):
+    """(sorted list of attended keys, is_global_row) for one row."""
+    lib = _load()
+    H = len(dilation)
+    dil = _i32(dilation)
+    gidx = _i32(global_idx) if len(global_idx) else None
+    pads = _i32(pad_len)
+    keys = np.zeros(max(n, 1), dtype=np.int32)
+    isg = np.zeros(1, dtype=np.int32)
+    cnt = lib.lf_oracle_attended(_ptr(gidx), len(global_idx), B, H, n, int(w), _ptr(dil),
+                                 int(bool(causal)), _ptr(pads), b, h, i, _ptr(keys), _ptr(isg))
+    if cnt < 0:
+        raise ValueError("oracle rejected the pattern")
+    return sorted(int(x) for x in keys[:cnt]), bool(isg[0])
+
+
+def wl_fwd(wl, inputs, rows=None, threads: int = 0) -> np.ndarray:
+    """fwd() for a workloads.Workload and its Inputs."""
+    return fwd(inputs.q, inputs.k, inputs.v, w=wl.w, dilation=wl.dilation, causal=wl.causal,
+               pad_len=wl.pad_len, qg=inputs.qg, kg=inputs.kg, vg=inputs.vg,
+               global_idx=wl.global_idx, rows=rows, threads=threads)

@@ -1,0 +1,242 @@
+/*
+ * lf_oracle.c -- plain, slow fp64 CPU oracle for Longformer-style attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link or call
+ * this file; only the tests, the package's smoke check and the CPU-baseline
+ * leg of the benchmark use it.  It shares no code, header or constant with
+ * the CUDA library.
+ *
+ * What it computes (velog.io/@lainshower/Longformer, section 3-1 "Attention
+ * Pattern"):
+ *   - Sliding window: a token attends w/2 neighbours on each side of itself.
+ *     Read here as |i - j| <= w/2 with the token itself included, so an
+ *     interior row attends w + 1 keys.
+ *   - Dilated sliding window: the window keeps its number of cells and
+ *     leaves gaps between them.  Read here as offsets that are multiples of
+ *     the head's dilation delta, up to delta * w/2 on each side.
+ *   - Global attention: the chosen tokens attend to every token and every
+ *     token attends to them; a global key that already lies in a row's band
+ *     is counted once (the attended set is a set union).
+ *   - Linear projections for global attention: the global computation uses
+ *     its own Q/K/V projections.  Read here as: rows of global tokens score
+ *     qg against kg of all valid keys and average vg; every other row uses
+ *     q, k and v for both its band and the global columns.
+ * The autoregressive variant (section 4.1) is read as the same window with
+ * its forward half removed: keys i - delta*t for t = 0..w/2.  Causality also
+ * restricts global rows (keys j <= g) and global columns (g <= i).
+ * Padding: pad_len[b] trailing tokens of batch row b are padding; they are
+ * never attended and their output rows are exact zeros.
+ * Scale 1/sqrt(d); no dropout or bias.
+ *
+ * Everything is evaluated in double: for each row the attended set is
+ * enumerated, scores are computed with a plain dot product, the row maximum
+ * is subtracted, exp() from libm is applied and the weighted values are
+ * summed and divided by the weight total.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* element type of the input tensors */
+enum { ORC_F64 = 0, ORC_F32 = 1, ORC_BF16 = 2 };
+
+static double load_elem(int dtype, const void* base, int64_t idx) {
+  if (dtype == ORC_F64) return ((const double*)base)[idx];
+  if (dtype == ORC_F32) return (double)((const float*)base)[idx];
+  /* bf16: the upper 16 bits of an IEEE binary32 */
+  uint32_t bits = ((uint32_t)((const uint16_t*)base)[idx]) << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+typedef struct {
+  int dtype;
+  const void *q, *k, *v, *qg, *kg, *vg;
+  const int32_t* global_idx;
+  int32_t G, B, H, n, d, w, causal;
+  const int32_t* dilation;
+  const int32_t* pad_len;
+} problem;
+
+/* rank of position i in the sorted global list, or -1 if i is not global */
+static int global_rank(const problem* p, int32_t i) {
+  for (int32_t r = 0; r < p->G; ++r)
+    if (p->global_idx[r] == i) return r;
+  return -1;
+}
+
+/* Is key j inside row i's (dilated, possibly causal) window? */
+static int in_window(const problem* p, int32_t h, int32_t i, int32_t j) {
+  int64_t delta = p->dilation[h];
+  int64_t half = p->w / 2;
+  int64_t off = (int64_t)j - (int64_t)i;           /* key offset from the row */
+  if (off % delta != 0) return 0;                  /* dilation gaps */
+  int64_t steps = off / delta;
+  int64_t left = half;                             /* look-back reach in steps */
+  int64_t right = p->causal ? 0 : half;            /* look-ahead reach in steps */
+  return steps >= -left && steps <= right;
+}
+
+/*
+ * Enumerate the attended key set of row (b, h, i).  Writes the key indices
+ * to keys[] (capacity n) and returns their count.  *is_global_row is set when
+ * the row belongs to a global token (its keys then index kg/vg).
+ * Returns 0 for padding rows.
+ */
+static int32_t attended_set(const problem* p, int32_t b, int32_t h, int32_t i,
+                            int32_t* keys, int* is_global_row) {
+  int32_t L = p->n - (p->pad_len ? p->pad_len[b] : 0);
+  int32_t cnt = 0;
+  *is_global_row = 0;
+  if (i >= L) return 0;
+  if (global_rank(p, i) >= 0) {
+    /* a global token attends every valid token (only earlier ones if causal) */
+    *is_global_row = 1;
+    for (int32_t j = 0; j < L; ++j)
+      if (!p->causal || j <= i) keys[cnt++] = j;
+    return cnt;
+  }
+  /* the window: offsets delta*t for t in [-half, +half] (t <= 0 if causal) */
+  int64_t delta = p->dilation[h];
+  int64_t half = p->w / 2;
+  if (half > p->n) half = p->n;                  /* wider reaches nothing new */
+  int64_t right = p->causal ? 0 : half;
+  for (int64_t t = -half; t <= right; ++t) {
+    int64_t j = (int64_t)i + delta * t;
+    if (j >= 0 && j < L) keys[cnt++] = (int32_t)j;
+  }
+  /* the global columns, each counted once */
+  for (int32_t r = 0; r < p->G; ++r) {
+    int32_t g = p->global_idx[r];
+    if (g >= L || (p->causal && g > i)) continue;
+    if (in_window(p, h, i, g)) continue;         /* already in the band */
+    keys[cnt++] = g;
+  }
+  return cnt;
+}
+
+/* one output row: softmax(scale * <q_row, k_j>) weighted sum of v_j over keys */
+static void one_row(const problem* p, int32_t b, int32_t h, int32_t i,
+                    int32_t* keys, double* scores, double* out_row) {
+  const int32_t n = p->n, d = p->d;
+  const int64_t bh = (int64_t)b * p->H + h;
+  int is_g = 0;
+  int32_t cnt = attended_set(p, b, h, i, keys, &is_g);
+  for (int32_t c = 0; c < d; ++c) out_row[c] = 0.0;
+  if (cnt == 0) return;
+
+  const void *qs, *ks, *vs;
+  int64_t qrow;
+  if (is_g) {
+    qs = p->qg; ks = p->kg; vs = p->vg;
+    qrow = bh * p->G + global_rank(p, i);
+  } else {
+    qs = p->q; ks = p->k; vs = p->v;
+    qrow = bh * n + i;
+  }
+  const double scale = 1.0 / sqrt((double)d);
+  double mx = -INFINITY;
+  for (int32_t t = 0; t < cnt; ++t) {
+    int64_t krow = bh * n + keys[t];
+    double s = 0.0;
+    for (int32_t c = 0; c < d; ++c)
+      s += load_elem(p->dtype, qs, qrow * d + c) * load_elem(p->dtype, ks, krow * d + c);
+    s *= scale;
+    scores[t] = s;
+    if (s > mx) mx = s;
+  }
+  double total = 0.0;
+  for (int32_t t = 0; t < cnt; ++t) {
+    double e = exp(scores[t] - mx);
+    total += e;
+    int64_t vrow = bh * n + keys[t];
+    for (int32_t c = 0; c < d; ++c) out_row[c] += e * load_elem(p->dtype, vs, vrow * d + c);
+  }
+  for (int32_t c = 0; c < d; ++c) out_row[c] /= total;
+}
+
+static int check_problem(const problem* p) {
+  if (p->B < 0 || p->H < 0 || p->n < 0 || p->d <= 0 || p->w < 0 || (p->w & 1)) return 1;
+  if (p->G < 0 || (p->G > 0 && !p->global_idx)) return 1;
+  for (int32_t h = 0; h < p->H; ++h)
+    if (p->dilation[h] < 1) return 1;
+  for (int32_t r = 0; r < p->G; ++r) {
+    if (p->global_idx[r] < 0 || p->global_idx[r] >= p->n) return 1;
+    if (r > 0 && p->global_idx[r] <= p->global_idx[r - 1]) return 1;
+  }
+  if (p->pad_len)
+    for (int32_t b = 0; b < p->B; ++b)
+      if (p->pad_len[b] < 0 || p->pad_len[b] > p->n) return 1;
+  return 0;
+}
+
+/*
+ * Full or sampled forward.  rows == NULL: every row, out is [B, H, n, d].
+ * Otherwise rows[0..nrows) are flat row ids ((b*H + h)*n + i) and out is
+ * [nrows, d].  Returns 0 on success, 1 on an invalid problem.
+ */
+int lf_oracle_fwd(int dtype, const void* q, const void* k, const void* v,
+                  const void* qg, const void* kg, const void* vg,
+                  const int32_t* global_idx, int32_t G,
+                  int32_t B, int32_t H, int32_t n, int32_t d, int32_t w,
+                  const int32_t* dilation, int32_t causal, const int32_t* pad_len,
+                  const int64_t* rows, int64_t nrows, double* out, int32_t nthreads) {
+  problem p = {dtype, q, k, v, qg, kg, vg, global_idx, G, B, H, n, d, w, causal, dilation, pad_len};
+  if (check_problem(&p)) return 1;
+  int64_t total = rows ? nrows : (int64_t)B * H * n;
+  if (total == 0) return 0;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+  int err = 0;
+#pragma omp parallel
+  {
+    int32_t* keys = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
+    double* scores = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    if (!keys || !scores) {
+#pragma omp atomic write
+      err = 2;
+    } else {
+#pragma omp for schedule(dynamic, 16)
+      for (int64_t t = 0; t < total; ++t) {
+        int64_t flat = rows ? rows[t] : t;
+        int32_t i = (int32_t)(flat % n);
+        int64_t bh = flat / n;
+        int32_t h = (int32_t)(bh % H), b = (int32_t)(bh / H);
+        one_row(&p, b, h, i, keys, scores, out + t * d);
+      }
+    }
+    free(keys);
+    free(scores);
+  }
+  return err;
+}
+
+/* The attended key set of one row (for pattern tests).  keys must hold n ints. */
+int32_t lf_oracle_attended(const int32_t* global_idx, int32_t G, int32_t B, int32_t H,
+                           int32_t n, int32_t w, const int32_t* dilation, int32_t causal,
+                           const int32_t* pad_len, int32_t b, int32_t h, int32_t i,
+                           int32_t* keys, int32_t* is_global_row) {
+  problem p = {ORC_F64, 0, 0, 0, 0, 0, 0, global_idx, G, B, H, n, 1, w, causal, dilation, pad_len};
+  if (check_problem(&p)) return -1;
+  int g = 0;
+  int32_t cnt = attended_set(&p, b, h, i, keys, &g);
+  *is_global_row = g;
+  return cnt;
+}
+
+/* Number of threads an OpenMP region of this library would use. */
+int32_t lf_oracle_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
