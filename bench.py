@@ -1,0 +1,374 @@
+#!/usr/bin/env python3
+"""Benchmark of the band-attention forward on B300.
+
+One step = one forward call (band kernel + global-row kernels) over one batch
+of seeded synthetic inputs that are already resident in HBM.  Default
+workload: bf16 encoder pattern B2 H12 n4096 d64, w=512, one global token.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own copy of
+the workload (weak scaling; the path needs no collective) and the reported
+time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "band-attn fwd useful TFLOP/s & % bf16 tensor peak; tokens/s vs n"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        j = json.load(open(path))
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "long_sequence_sliding_longformer_b300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload: str):
+    """DRAM bytes per band-kernel launch from a committed ncu summary, if it was
+    taken on the current kernel sources for this workload; else None."""
+    path = os.path.join(ROOT, "profiles", "band_traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        j = json.load(open(path))
+        e = j.get(workload)
+        if e and e.get("source_hash") == kernel_source_hash():
+            return e.get("bytes_per_launch_full")
+    except (ValueError, OSError):
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, 0
+    import torch.distributed as dist
+    rank = int(os.environ["RANK"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend)
+    return rank, ws, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int, device) -> float:
+    if ws <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def useful_work(wl):
+    import long_sequence_sliding_longformer_b300 as lf
+    pairs, flops = lf.count_pairs(B=wl.B, H=wl.H, n=wl.n, d=wl.d, w=wl.w, dilation=wl.dilation,
+                                  causal=wl.causal, pad_len=wl.pad_len, global_idx=wl.global_idx)
+    # split: pairs on the global tokens' own rows (global-row kernels) vs the rest (band kernel)
+    gpairs = 0
+    for b in range(wl.B):
+        L = wl.valid_len(b)
+        for g in wl.global_idx:
+            if g < L:
+                gpairs += (g + 1 if wl.causal else L) * wl.H
+    return pairs, flops, gpairs * 4 * wl.d
+
+
+def band_bytes(wl) -> int:
+    """Algorithmic HBM bytes of the band kernel: q, k, v read once, out written
+    once, over all rows (8*d bytes per token-head in bf16)."""
+    return 4 * wl.B * wl.H * wl.n * wl.d * wl.elem_bytes
+
+
+def cpu_sample(wl, inp, target_s: float = 12.0):
+    """Time the oracle on whole (batch, head) slices of the workload until about
+    target_s seconds of work; returns (seconds, useful flops, threads, description)."""
+    import long_sequence_sliding_longformer_b300 as lf
+    import numpy as np
+    import oracle
+    host = workloads.Inputs(*[None if t is None else t.cpu() for t in
+                              (inp.q, inp.k, inp.v, inp.qg, inp.kg, inp.vg)])
+    n = wl.n
+    slices = [(b, h) for b in range(wl.B) for h in range(wl.H)]
+    done, secs, flops = 0, 0.0, 0.0
+    while done < len(slices):
+        take = 1 if done == 0 else max(1, min(len(slices) - done,
+                                              int(done * (target_s - secs) / max(secs, 1e-3))))
+        if done > 0 and secs >= target_s:
+            break
+        chunk = slices[done:done + take]
+        rows = np.concatenate([np.arange(n, dtype=np.int64) + (b * wl.H + h) * n for b, h in chunk])
+        t0 = time.perf_counter()
+        oracle.wl_fwd(wl, host, rows=rows)
+        secs += time.perf_counter() - t0
+        for b, h in chunk:
+            pad = None if wl.pad_len is None else [wl.pad_len[b]]
+            _, f = lf.count_pairs(B=1, H=1, n=n, d=wl.d, w=wl.w, dilation=[wl.dilation[h]],
+                                  causal=wl.causal, pad_len=pad, global_idx=wl.global_idx)
+            flops += f
+        done += take
+    desc = "%d of %d (batch, head) slices, all %d rows each (every row of the sample)" % (
+        done, len(slices), n)
+    return secs, flops, oracle.max_threads(), desc
+
+
+def run_reference(args, wl):
+    rank, ws, _ = dist_setup()
+    if rank != 0:
+        return
+    inp = workloads.make_inputs(wl, "cpu")
+    times, flops_tot = [], 0.0
+    threads, desc = 0, ""
+    per_step_target = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    for it in range(args.warmup + args.steps):
+        secs, flops, threads, desc = cpu_sample(wl, inp, target_s=per_step_target)
+        if it >= args.warmup:
+            times.append(secs)
+            flops_tot += flops
+    value = flops_tot / sum(times) / 1e12
+    tok = wl.tokens()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), CPU generator)",
+        "config": dict(wl.describe(), sample="bounded per step"),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "tokens_per_s": value * 1e12 * tok / useful_work(wl)[1],
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu(args, wl):
+    import long_sequence_sliding_longformer_b300 as lf
+    rank, ws, local = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lf.load()
+    inp = workloads.make_inputs(wl, str(dev), seed=wl.seed + rank)
+    out = torch.empty_like(inp.q)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(o=out):
+        lf.attn(inp.q, inp.k, inp.v, w=wl.w, dilation=wl.dilation, causal=wl.causal,
+                pad_len=wl.pad_len, qg=inp.qg, kg=inp.kg, vg=inp.vg, global_idx=wl.global_idx, out=o)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    bev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    launches0 = lf.launch_count()
+    with ClockSampler(dev.index) as clocks:
+        barrier(ws)
+        torch.cuda.synchronize(dev)
+        wall0 = time.perf_counter()
+        for i in range(K):
+            flush.zero_()  # evict L2 so every step reads its inputs from HBM
+            lf.set_band_events(*bev[i])
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        lf.set_band_events(None, None)
+        torch.cuda.synchronize(dev)
+        barrier(ws)
+        wall = time.perf_counter() - wall0
+    launches = lf.launch_count() - launches0
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    band_ms = [a.elapsed_time(b) for a, b in bev]
+    total_ms = max_over_ranks(sum(step_ms), ws, dev)
+    ms_per_step = total_ms / K
+
+    # ---- end to end through the public API: pinned host in, host out
+    host_in = [t.cpu().pin_memory() for t in inp.tensors()]
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    dev_in = [torch.empty_like(t) for t in inp.tensors()]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_k = max(3, min(K, 50))
+
+    def e2e_step():
+        for d_, h_ in zip(dev_in, host_in):
+            d_.copy_(h_, non_blocking=True)
+        names = ["q", "k", "v", "qg", "kg", "vg"]
+        t = dict(zip(names, dev_in))
+        lf.attn(t["q"], t["k"], t["v"], w=wl.w, dilation=wl.dilation, causal=wl.causal,
+                pad_len=wl.pad_len, qg=t.get("qg"), kg=t.get("kg"), vg=t.get("vg"),
+                global_idx=wl.global_idx, out=out)
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    e0.record(stream)
+    for _ in range(e2e_k):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_k, ws, dev)
+
+    pairs, flops, gflops_part = useful_work(wl)
+    band_flops = flops - gflops_part
+    pk = peaks()
+    value = ws * flops / (ms_per_step * 1e-3) / 1e12
+    band_avg_ms = statistics.mean(band_ms)
+    band_achieved = band_flops / (band_avg_ms * 1e-3) / 1e12
+    hbm_achieved = band_bytes(wl) / (band_avg_ms * 1e-3) / 1e9
+    traffic = committed_traffic(wl.name)
+    line = None
+    if rank == 0:
+        cs = clocks.summary()
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+            "data": "synthetic (seeded N(0,1) on the device)",
+            "config": dict(wl.describe(), parallelism="replicas: one workload per GPU" if ws > 1 else "1 GPU",
+                           l2="flushed before every step (256 MiB write)"),
+            "tokens_per_s": ws * wl.tokens() / (ms_per_step * 1e-3),
+            "frac_of_bf16_peak": value / pk["bf16_tflops"],
+            "roofline": {"bound": "tensor", "achieved": band_achieved, "peak": pk["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": band_achieved / pk["bf16_tflops"],
+                         "traffic": traffic, "kernel": "band_tc_kernel",
+                         "peak_source": pk["source"] + " (burst)",
+                         "hbm_achieved_gbs": hbm_achieved, "hbm_frac": hbm_achieved / pk["hbm_gbs"],
+                         "band_ms": band_avg_ms, "band_share_of_step": band_avg_ms / statistics.mean(step_ms)},
+            "e2e": {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": launches,
+            "clocks": {"sm_mhz": cs["sm_mhz"], "sm_max_mhz": cs["sm_max_mhz"], "reasons": cs["reasons"],
+                       "samples": cs["samples"]},
+            "wall_s_timed_region": wall,
+            "useful_flops_per_step": flops,
+        }
+    if rank == 0 and not args.no_cpu_baseline and ws == 1:
+        secs, sflops, threads, desc = cpu_sample(wl, inp, target_s=args.cpu_seconds)
+        v = sflops / secs / 1e12
+        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                "sample": desc, "seconds": secs}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="lf", choices=["lf", "reference"])
+    ap.add_argument("--workload", default=workloads.bf16_encoder().name,
+                    help="one of: " + ", ".join(w.name for w in workloads.all_workloads()))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    wl = workloads.by_name(args.workload)
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_gpu(args, wl)
+
+
+if __name__ == "__main__":
+    main()

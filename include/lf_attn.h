@@ -1,0 +1,127 @@
+/*
+ * lf_attn.h -- C ABI of the B300 (sm_103a) Longformer-style attention library.
+ *
+ * The operation (velog.io/@lainshower/Longformer, section 3-1 "Attention
+ * Pattern" and section 4.1 for the autoregressive pattern):
+ *
+ *   Each token i of a sequence of n tokens attends to the keys of its window:
+ *   offsets delta*t for integer t in [-w/2, +w/2] (the token itself included,
+ *   so an interior row attends w + 1 keys), where delta = dilation[h] is the
+ *   per-head dilation ("Dilated Sliding Window").  With causal != 0 the window
+ *   keeps only t in [-w/2, 0] (look-back only, w/2 + 1 keys).
+ *   A few global tokens ("Global Attention") attend to every token and every
+ *   token attends to them.  Global attention has its own projections
+ *   ("Linear Projections for Global Attention"): the row of a global token g
+ *   is softmax(qg[g] . kg[j] / sqrt(d)) averaged over vg[j] for all valid j
+ *   (j <= g when causal); every other row scores q against k over its window
+ *   plus the global tokens' columns (each key counted once) and averages v.
+ *   Scores are scaled by 1/sqrt(d); there is no dropout or bias.
+ *   Padding: pad_len[b] trailing tokens of batch row b are never attended and
+ *   their output rows are written as zeros.
+ *
+ * Layouts: every [B, H, n, d] tensor is row-major and contiguous (d fastest);
+ * qg is [B, H, G, d] with row r belonging to position global_idx[r].
+ * All device pointers must be 16-byte aligned and `out` must not overlap any
+ * input.  Index arrays (global_idx, dilation, pad_len) are HOST memory, read
+ * during the call and not retained.  The caller owns every buffer; the
+ * library keeps no pointer after returning.
+ *
+ * Calls are asynchronous on `stream` (0 = legacy default stream): they
+ * enqueue kernels and return without synchronising.  Arguments are validated
+ * on the host before anything is enqueued; on any error the call returns a
+ * non-zero status, enqueues nothing and leaves `out` untouched.  A call that
+ * fails after validation (a CUDA launch error) returns LF_ERR_CUDA.
+ * lf_last_error_message() then describes the failure (per host thread).
+ */
+#ifndef LF_ATTN_H
+#define LF_ATTN_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LF_OK = 0,
+  LF_ERR_INVALID_ARG = 1, /* a null/misaligned pointer, bad size, unsorted global list, ... */
+  LF_ERR_UNSUPPORTED = 2, /* valid but outside this build's limits (e.g. bf16 d not 64/128) */
+  LF_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+  LF_ERR_NO_MEMORY = 4,   /* scratch space for the global rows could not be allocated */
+  LF_ERR_TIMEOUT = 5      /* a kernel gave up waiting (reported by lf_device_error) */
+} lf_status;
+
+/* Largest number of global tokens per call. */
+#define LF_MAX_GLOBAL 4096
+
+/*
+ * bf16 forward.  q, k, v, kg, vg, out: [B, H, n, d] bf16 device memory;
+ * qg: [B, H, G, d] bf16 device memory.  G = n_global (0 <= G <= LF_MAX_GLOBAL);
+ * global_idx: host array of G strictly increasing positions in [0, n), NULL
+ * iff G == 0 (qg, kg, vg may then be NULL).  w: total window, even, >= 0.
+ * dilation: host array of H values >= 1.  causal: 0 or 1.  pad_len: host
+ * array of B trailing-pad counts in [0, n], or NULL for none.
+ * Supported d: 64 and 128.  Computes in fp32 on the tensor cores (bf16
+ * operands, fp32 accumulation, fp32 online softmax) and rounds the output
+ * to bf16 (round to nearest even).
+ */
+lf_status lf_attn_fwd(const void* q, const void* k, const void* v,
+                      const void* qg, const void* kg, const void* vg,
+                      const int32_t* global_idx, int32_t n_global,
+                      void* out,
+                      int32_t B, int32_t H, int32_t n, int32_t d,
+                      int32_t w, const int32_t* dilation, int32_t causal,
+                      const int32_t* pad_len, cudaStream_t stream);
+
+/*
+ * fp32 forward: same arguments and semantics as lf_attn_fwd with every
+ * tensor in fp32; any d in [1, 128].  CUDA-core arithmetic in fp32.
+ */
+lf_status lf_attn_fwd_f32(const void* q, const void* k, const void* v,
+                          const void* qg, const void* kg, const void* vg,
+                          const int32_t* global_idx, int32_t n_global,
+                          void* out,
+                          int32_t B, int32_t H, int32_t n, int32_t d,
+                          int32_t w, const int32_t* dilation, int32_t causal,
+                          const int32_t* pad_len, cudaStream_t stream);
+
+/*
+ * Host-only: the useful work of a problem, counted exactly from the pattern.
+ * *pairs = number of attended (query, key) pairs over all valid rows and
+ * heads; *flops = 4 * d * pairs (one multiply-add each for QK^T and PV).
+ * Takes the same pattern arguments as lf_attn_fwd; touches no GPU.
+ */
+lf_status lf_attn_count_pairs(int32_t B, int32_t H, int32_t n, int32_t d, int32_t w,
+                              const int32_t* dilation, int32_t causal, const int32_t* pad_len,
+                              const int32_t* global_idx, int32_t n_global,
+                              int64_t* pairs, double* flops);
+
+/* Name of a status code (static storage). */
+const char* lf_status_string(lf_status s);
+
+/* Detail of the last failure on the calling host thread ("" if none). */
+const char* lf_last_error_message(void);
+
+/*
+ * Profiling hook.  While set (non-NULL), every forward call records `start`
+ * just before and `stop` just after its band kernel, on the call's stream.
+ * Pass NULL, NULL to clear.  Per host thread.
+ */
+lf_status lf_attn_set_band_events(cudaEvent_t start, cudaEvent_t stop);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t lf_attn_launch_count(void);
+
+/*
+ * Synchronises the current device and reads the library's device error word
+ * (0 = none; otherwise LF_ERR_TIMEOUT in the low byte and the kernel role
+ * that gave up in the next byte).  clear != 0 resets it to 0.
+ */
+lf_status lf_device_error(uint32_t* code, int32_t clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LF_ATTN_H */

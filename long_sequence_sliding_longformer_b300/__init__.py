@@ -1,0 +1,156 @@
+"""Longformer-style band attention on one B300 -- Python binding of liblf_attn.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library's kernels (see include/lf_attn.h for the operation and its ABI).
+There is no fallback: if the library is missing or a call fails, an error is
+raised.
+
+    out = attn(q, k, v, w=512, dilation=[1]*H, causal=False,
+               qg=qg, kg=kg, vg=vg, global_idx=[0], pad_len=None)
+
+q, k, v, kg, vg: [B, H, n, d] CUDA tensors (bf16 with d in {64, 128}, or
+fp32 with d <= 128); qg: [B, H, G, d].  The call is asynchronous on the
+current CUDA stream (or `stream`).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+__all__ = ["attn", "count_pairs", "set_band_events", "launch_count", "device_error", "LfError",
+           "load", "LIB_PATH"]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblf_attn.so")
+_lib = None
+
+_STATUS = {0: "LF_OK", 1: "LF_ERR_INVALID_ARG", 2: "LF_ERR_UNSUPPORTED", 3: "LF_ERR_CUDA",
+           4: "LF_ERR_NO_MEMORY", 5: "LF_ERR_TIMEOUT"}
+
+
+class LfError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("%s: %s" % (_STATUS.get(status, status), message))
+        self.status = status
+
+
+def load():
+    """Load liblf_attn.so (built by _build.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("liblf_attn.so is not built; run long_sequence_sliding_longformer_b300._build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, i32 = ctypes.c_void_p, ctypes.c_int32
+    fwd_args = [P, P, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, P, i32, P, P]
+    for name in ("lf_attn_fwd", "lf_attn_fwd_f32"):
+        fn = getattr(lib, name)
+        fn.argtypes = fwd_args
+        fn.restype = ctypes.c_int
+    lib.lf_attn_count_pairs.argtypes = [i32, i32, i32, i32, i32, P, i32, P, P, i32,
+                                        ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double)]
+    lib.lf_attn_count_pairs.restype = ctypes.c_int
+    lib.lf_status_string.argtypes = [ctypes.c_int]
+    lib.lf_status_string.restype = ctypes.c_char_p
+    lib.lf_last_error_message.restype = ctypes.c_char_p
+    lib.lf_attn_set_band_events.argtypes = [P, P]
+    lib.lf_attn_set_band_events.restype = ctypes.c_int
+    lib.lf_attn_launch_count.restype = ctypes.c_uint64
+    lib.lf_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+    lib.lf_device_error.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise LfError(status, load().lf_last_error_message().decode())
+
+
+def _i32_array(seq) -> Optional[ctypes.Array]:
+    if seq is None:
+        return None
+    seq = [int(x) for x in seq]
+    return (ctypes.c_int32 * max(len(seq), 1))(*seq)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, w: int,
+         dilation: Optional[Sequence[int]] = None, causal: bool = False,
+         pad_len: Optional[Sequence[int]] = None, qg: Optional[torch.Tensor] = None,
+         kg: Optional[torch.Tensor] = None, vg: Optional[torch.Tensor] = None,
+         global_idx: Sequence[int] = (), out: Optional[torch.Tensor] = None,
+         stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Sliding / dilated / causal window attention with global tokens."""
+    lib = load()
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, n, d]")
+    B, H, n, d = q.shape
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("q must be bf16 or fp32, got %s" % q.dtype)
+    tensors = [("q", q), ("k", k), ("v", v)]
+    G = len(global_idx)
+    if G:
+        tensors += [("qg", qg), ("kg", kg), ("vg", vg)]
+    for name, t in tensors:
+        if t is None:
+            raise ValueError("%s is required" % name)
+        if not t.is_cuda or t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA tensor of dtype %s" % (name, q.dtype))
+        want = (B, H, G, d) if name == "qg" else (B, H, n, d)
+        if tuple(t.shape) != want:
+            raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), want))
+    if out is None:
+        out = torch.empty_like(q)
+    elif tuple(out.shape) != (B, H, n, d) or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [B, H, n, d] tensor of q's dtype")
+    dil = _i32_array(dilation if dilation is not None else [1] * H)
+    if len(dilation if dilation is not None else [1] * H) != H:
+        raise ValueError("dilation needs one entry per head")
+    gidx = _i32_array(global_idx) if G else None
+    pads = _i32_array(pad_len)
+    if pad_len is not None and len(pad_len) != B:
+        raise ValueError("pad_len needs one entry per batch row")
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    fn = lib.lf_attn_fwd if q.dtype == torch.bfloat16 else lib.lf_attn_fwd_f32
+    with torch.cuda.device(q.device):
+        _check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr(qg) if G else None,
+                  _ptr(kg) if G else None, _ptr(vg) if G else None, gidx, G, out.data_ptr(),
+                  B, H, n, d, int(w), dil, int(bool(causal)), pads, s.cuda_stream))
+    return out
+
+
+def count_pairs(*, B: int, H: int, n: int, d: int, w: int, dilation: Sequence[int],
+                causal: bool = False, pad_len: Optional[Sequence[int]] = None,
+                global_idx: Sequence[int] = ()):
+    """(attended pairs, useful FLOPs = 4*d*pairs) of a pattern; host only."""
+    lib = load()
+    pairs = ctypes.c_int64(0)
+    flops = ctypes.c_double(0.0)
+    _check(lib.lf_attn_count_pairs(B, H, n, d, int(w), _i32_array(dilation), int(bool(causal)),
+                                   _i32_array(pad_len), _i32_array(global_idx) if len(global_idx) else None,
+                                   len(global_idx), ctypes.byref(pairs), ctypes.byref(flops)))
+    return int(pairs.value), float(flops.value)
+
+
+def set_band_events(start: Optional[torch.cuda.Event], stop: Optional[torch.cuda.Event]):
+    """Record `start`/`stop` around the band kernel of every later call (None, None clears)."""
+    sp = None if start is None else ctypes.c_void_p(start.cuda_event)
+    ep = None if stop is None else ctypes.c_void_p(stop.cuda_event)
+    _check(load().lf_attn_set_band_events(sp, ep))
+
+
+def launch_count() -> int:
+    return int(load().lf_attn_launch_count())
+
+
+def device_error(clear: bool = False) -> int:
+    code = ctypes.c_uint32(0)
+    _check(load().lf_device_error(ctypes.byref(code), int(bool(clear))))
+    return int(code.value)

@@ -1,0 +1,539 @@
+// lf_attn.cu -- the C ABI of include/lf_attn.h: argument validation, planning
+// of the band-kernel work (residue classes, tiles, TMA tensor maps), the
+// global-row scratch space, and the launches.  Single translation unit: the
+// kernels are included below.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "lf_internal.cuh"
+#include "band_tc.cuh"
+#include "band_simt.cuh"
+#include "global_rows.cuh"
+
+namespace lf {
+
+static thread_local char t_msg[512] = "";
+static thread_local cudaEvent_t t_band_start = nullptr, t_band_stop = nullptr;
+static std::atomic<uint64_t> g_launches{0};
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_msg, sizeof t_msg, fmt, ap);
+  va_end(ap);
+}
+
+void count_launch(int k) { g_launches.fetch_add((uint64_t)k, std::memory_order_relaxed); }
+
+// ------------------------------------------------------------------ driver entry point for TMA maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// [d, rows, planes] bf16 view with row stride `row_stride` elements, plane
+// stride `plane_stride` elements; boxes of [64, 128, 1] with 128-byte swizzle.
+static lf_status make_map(CUtensorMap* m, const void* base, int d, int64_t rows, int64_t planes,
+                          int64_t row_stride, int64_t plane_stride) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) {
+    set_error("cuTensorMapEncodeTiled is not available from the driver");
+    return LF_ERR_CUDA;
+  }
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)planes};
+  cuuint64_t strides[2] = {(cuuint64_t)row_stride * 2, (cuuint64_t)plane_stride * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled failed (%d) for rows=%lld planes=%lld stride=%lld", (int)r,
+              (long long)rows, (long long)planes, (long long)row_stride);
+    return LF_ERR_CUDA;
+  }
+  return LF_OK;
+}
+
+static int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+
+// ------------------------------------------------------------------ problem + validation
+struct Problem {
+  const void *q, *k, *v, *qg, *kg, *vg;
+  const int32_t* gidx;
+  int32_t G;
+  void* out;
+  int32_t B, H, n, d, w;
+  const int32_t* dil;
+  int32_t causal;
+  const int32_t* pad;
+  cudaStream_t stream;
+  int elem;  // bytes per element
+};
+
+static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+  return x < y + nb && y < x + na;
+}
+
+// Checks that need no pointers: sizes, window, dilation, padding, global list.
+static lf_status validate_pattern(const Problem& P) {
+  if (P.B < 0 || P.H < 0 || P.n < 0) {
+    set_error("B, H and n must be >= 0 (got %d, %d, %d)", P.B, P.H, P.n);
+    return LF_ERR_INVALID_ARG;
+  }
+  if (P.d < 1) {
+    set_error("d must be >= 1 (got %d)", P.d);
+    return LF_ERR_INVALID_ARG;
+  }
+  if (P.w < 0 || (P.w & 1)) {
+    set_error("w must be even and >= 0 (got %d)", P.w);
+    return LF_ERR_INVALID_ARG;
+  }
+  if (P.causal != 0 && P.causal != 1) {
+    set_error("causal must be 0 or 1 (got %d)", P.causal);
+    return LF_ERR_INVALID_ARG;
+  }
+  if (P.G < 0) {
+    set_error("n_global must be >= 0 (got %d)", P.G);
+    return LF_ERR_INVALID_ARG;
+  }
+  if (P.G > LF_MAX_GLOBAL) {
+    set_error("n_global must be <= %d (got %d)", LF_MAX_GLOBAL, P.G);
+    return LF_ERR_UNSUPPORTED;
+  }
+  if (P.H > 0 && !P.dil) {
+    set_error("dilation must not be NULL");
+    return LF_ERR_INVALID_ARG;
+  }
+  for (int h = 0; h < P.H; ++h)
+    if (P.dil[h] < 1) {
+      set_error("dilation[%d] = %d must be >= 1", h, P.dil[h]);
+      return LF_ERR_INVALID_ARG;
+    }
+  if (P.pad)
+    for (int b = 0; b < P.B; ++b)
+      if (P.pad[b] < 0 || P.pad[b] > P.n) {
+        set_error("pad_len[%d] = %d must be in [0, n=%d]", b, P.pad[b], P.n);
+        return LF_ERR_INVALID_ARG;
+      }
+  if (P.G > 0) {
+    if (!P.gidx) {
+      set_error("global_idx must not be NULL when n_global > 0");
+      return LF_ERR_INVALID_ARG;
+    }
+    for (int r = 0; r < P.G; ++r) {
+      if (P.gidx[r] < 0 || P.gidx[r] >= P.n) {
+        set_error("global_idx[%d] = %d is outside [0, n=%d)", r, P.gidx[r], P.n);
+        return LF_ERR_INVALID_ARG;
+      }
+      if (r > 0 && P.gidx[r] <= P.gidx[r - 1]) {
+        set_error("global_idx must be strictly increasing (entry %d)", r);
+        return LF_ERR_INVALID_ARG;
+      }
+    }
+  }
+  return LF_OK;
+}
+
+static lf_status validate(const Problem& P, bool bf16) {
+  lf_status st = validate_pattern(P);
+  if (st != LF_OK) return st;
+  if (bf16 && P.d != 64 && P.d != 128) {
+    set_error("bf16 path supports d = 64 or 128 (got %d)", P.d);
+    return LF_ERR_UNSUPPORTED;
+  }
+  if (!bf16 && P.d > 128) {
+    set_error("fp32 path supports d <= 128 (got %d)", P.d);
+    return LF_ERR_UNSUPPORTED;
+  }
+  if (!bf16 && P.H > kMaxHeadsSimt) {
+    set_error("fp32 path supports H <= %d (got %d)", kMaxHeadsSimt, P.H);
+    return LF_ERR_UNSUPPORTED;
+  }
+  if (P.n >= (1 << 28)) {
+    set_error("n must be < 2^28 (got %d)", P.n);
+    return LF_ERR_UNSUPPORTED;
+  }
+  const int64_t elems = (int64_t)P.B * P.H * P.n * P.d;
+  if (elems == 0) return LF_OK;
+  const void* ptrs[7] = {P.q, P.k, P.v, P.out, P.qg, P.kg, P.vg};
+  const char* names[7] = {"q", "k", "v", "out", "qg", "kg", "vg"};
+  const int need = P.G > 0 ? 7 : 4;
+  for (int t = 0; t < need; ++t) {
+    if (!ptrs[t]) {
+      set_error("%s must not be NULL", names[t]);
+      return LF_ERR_INVALID_ARG;
+    }
+    if (((uintptr_t)ptrs[t]) & 15) {
+      set_error("%s must be 16-byte aligned", names[t]);
+      return LF_ERR_INVALID_ARG;
+    }
+  }
+  const size_t bytes = (size_t)elems * P.elem;
+  const size_t gbytes = (size_t)P.B * P.H * P.G * P.d * P.elem;
+  for (int t = 0; t < need; ++t) {
+    if (t == 3) continue;
+    if (overlaps(P.out, bytes, ptrs[t], t == 4 ? gbytes : bytes)) {
+      set_error("out overlaps %s", names[t]);
+      return LF_ERR_INVALID_ARG;
+    }
+  }
+  return LF_OK;
+}
+
+static void fill_pattern(PatternParams& pp, const Problem& P, int b0, int nb) {
+  memset(&pp, 0, sizeof pp);
+  pp.B = nb;
+  pp.H = P.H;
+  pp.n = P.n;
+  pp.d = P.d;
+  const int64_t half = std::min<int64_t>(P.w / 2, P.n);
+  pp.half = (int32_t)half;
+  pp.right = P.causal ? 0 : (int32_t)half;
+  pp.causal = P.causal;
+  pp.G = P.G;
+  pp.scale = (float)(1.0 / std::sqrt((double)P.d));
+  for (int b = 0; b < nb; ++b) pp.pad[b] = P.pad ? P.pad[b0 + b] : 0;
+  for (int r = 0; r < P.G; ++r) pp.gidx[r] = P.gidx[r];
+}
+
+// ------------------------------------------------------------------ global rows
+template <typename T>
+static lf_status run_global_rows(const Problem& P, int b0, int nbat) {
+  if (P.G == 0 || nbat == 0) return LF_OK;
+  PatternParams pp;
+  fill_pattern(pp, P, b0, nbat);
+  const size_t off = (size_t)b0 * P.H * P.n * P.d;
+  const size_t goff = (size_t)b0 * P.H * P.G * P.d;
+  // chunk: a multiple of the sub-chunk; grow it until the scratch stays <= 64 MiB
+  const int64_t bh = (int64_t)nbat * P.H;
+  const int64_t qblocks = (P.G + kGQ - 1) / kGQ;
+  // enough CTAs to fill the GPU about four times over, in chunks of 128 keys
+  int64_t chunk = 128;
+  while (chunk * 2 <= P.n && bh * qblocks * ((P.n + chunk * 2 - 1) / (chunk * 2)) >= 4 * sm_count())
+    chunk *= 2;
+  auto ws_bytes = [&](int64_t c) {
+    const int64_t nch = (P.n + c - 1) / c;
+    return (size_t)(bh * nch * P.G * (P.d + 2)) * sizeof(float);
+  };
+  while (ws_bytes(chunk) > ((size_t)64 << 20) && chunk < P.n) chunk *= 2;
+  const int nchunks = (int)((P.n + chunk - 1) / chunk);
+  const size_t wsb = ws_bytes(chunk);
+  float* ws = nullptr;
+  cudaError_t e = cudaMallocAsync((void**)&ws, wsb, P.stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    set_error("scratch allocation of %zu bytes failed: %s", wsb, cudaGetErrorString(e));
+    return LF_ERR_NO_MEMORY;
+  }
+  lf_status st = launch_global_rows<T>(pp, reinterpret_cast<const T*>(P.qg) + goff,
+                                       reinterpret_cast<const T*>(P.kg) + off,
+                                       reinterpret_cast<const T*>(P.vg) + off,
+                                       reinterpret_cast<T*>(P.out) + off, ws, nchunks, (int)chunk, P.stream);
+  cudaError_t fe = cudaFreeAsync(ws, P.stream);
+  if (st == LF_OK && fe != cudaSuccess) {
+    set_error("scratch free failed: %s", cudaGetErrorString(fe));
+    return LF_ERR_CUDA;
+  }
+  return st;
+}
+
+// ------------------------------------------------------------------ bf16 band planning
+struct SegPlan {
+  int h, r, delta, n_r, tiles;
+};
+
+static lf_status run_band_bf16(const Problem& P, int b0, int nbat) {
+  // every (head, residue) class with at least one row
+  std::vector<SegPlan> segs;
+  for (int h = 0; h < P.H; ++h) {
+    const int delta = P.dil[h];
+    for (int r = 0; r < delta && r < P.n; ++r) {
+      const int n_r = (P.n - r + delta - 1) / delta;
+      segs.push_back({h, r, delta, n_r, (n_r + 127) / 128});
+    }
+  }
+  const int grid_cap = sm_count();
+  const size_t off = (size_t)b0 * P.H * P.n * P.d;
+  const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(P.q) + off;
+  const __nv_bfloat16* k = reinterpret_cast<const __nv_bfloat16*>(P.k) + off;
+  const __nv_bfloat16* v = reinterpret_cast<const __nv_bfloat16*>(P.v) + off;
+  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(P.out) + off;
+  const int64_t planes = (int64_t)nbat * P.H;
+
+  static thread_local BandParams* bp = nullptr;  // ~25 KB: keep it off the stack
+  if (!bp) bp = new (std::nothrow) BandParams;
+  if (!bp) {
+    set_error("host allocation of the band parameter block failed");
+    return LF_ERR_NO_MEMORY;
+  }
+  size_t s0 = 0;
+  while (s0 < segs.size()) {
+    BandParams& p = *bp;
+    memset(&p, 0, sizeof p);
+    int nsets = 0;
+    int set_delta[kMaxSets], set_r[kMaxSets];
+    size_t s1 = s0;
+    int items_per_b = 0;
+    for (; s1 < segs.size() && (int)(s1 - s0) < kMaxSeg; ++s1) {
+      const SegPlan& sg = segs[s1];
+      int set = -1;
+      for (int t = 0; t < nsets; ++t)
+        if (set_delta[t] == sg.delta && set_r[t] == sg.r) set = t;
+      if (set < 0) {
+        if (nsets == kMaxSets) break;
+        set = nsets++;
+        set_delta[set] = sg.delta;
+        set_r[set] = sg.r;
+      }
+      BandSeg& bs = p.seg[s1 - s0];
+      bs.h = sg.h;
+      bs.r = sg.r;
+      bs.delta = sg.delta;
+      bs.n_r = sg.n_r;
+      bs.tiles = sg.tiles;
+      bs.set = set;
+      bs.begin = items_per_b;
+      items_per_b += sg.tiles;
+    }
+    for (int t = 0; t < nsets; ++t) {
+      const int delta = set_delta[t], r = set_r[t];
+      const int64_t n_r = (P.n - r + delta - 1) / delta;
+      const int64_t rs = (int64_t)delta * P.d, ps = (int64_t)P.n * P.d;
+      const size_t ro = (size_t)r * P.d;
+      lf_status st;
+      if ((st = make_map(&p.tq[t], q + ro, P.d, n_r, planes, rs, ps)) != LF_OK) return st;
+      if ((st = make_map(&p.tk[t], k + ro, P.d, n_r, planes, rs, ps)) != LF_OK) return st;
+      if ((st = make_map(&p.tv[t], v + ro, P.d, n_r, planes, rs, ps)) != LF_OK) return st;
+    }
+    p.k = k;
+    p.v = v;
+    p.out = out;
+    p.B = nbat;
+    p.H = P.H;
+    p.n = P.n;
+    const int64_t half = std::min<int64_t>(P.w / 2, P.n);
+    p.half = (int32_t)half;
+    p.right = P.causal ? 0 : (int32_t)half;
+    p.causal = P.causal;
+    p.G = P.G;
+    p.nseg = (int32_t)(s1 - s0);
+    p.items_per_b = items_per_b;
+    const int64_t total = (int64_t)items_per_b * nbat;
+    if (total > 0x7fffffff) {
+      set_error("too many band tiles (%lld)", (long long)total);
+      return LF_ERR_UNSUPPORTED;
+    }
+    p.total_items = (int32_t)total;
+    p.sl2 = (float)(1.4426950408889634 / std::sqrt((double)P.d));
+    for (int b = 0; b < nbat; ++b) p.pad[b] = P.pad ? P.pad[b0 + b] : 0;
+    for (int r = 0; r < P.G; ++r) p.gidx[r] = P.gidx[r];
+    const int grid = (int)std::min<int64_t>(total, grid_cap);
+    if (grid > 0) {
+      lf_status st = launch_band_tc(p, P.d, grid, P.stream);
+      if (st != LF_OK) return st;
+    }
+    s0 = s1;
+  }
+  return LF_OK;
+}
+
+static lf_status run_band_f32(const Problem& P, int b0, int nbat) {
+  static thread_local SimtParams* sp = nullptr;  // ~18 KB: keep it off the stack
+  if (!sp) sp = new (std::nothrow) SimtParams;
+  if (!sp) {
+    set_error("host allocation of the fp32 parameter block failed");
+    return LF_ERR_NO_MEMORY;
+  }
+  const size_t off = (size_t)b0 * P.H * P.n * P.d;
+  fill_pattern(sp->pat, P, b0, nbat);
+  for (int h = 0; h < P.H; ++h) sp->dil[h] = P.dil[h];
+  return launch_band_simt_f32(*sp, reinterpret_cast<const float*>(P.q) + off,
+                              reinterpret_cast<const float*>(P.k) + off,
+                              reinterpret_cast<const float*>(P.v) + off,
+                              reinterpret_cast<float*>(P.out) + off, P.stream);
+}
+
+static lf_status forward(const Problem& P, bool bf16) {
+  t_msg[0] = 0;
+  lf_status st = validate(P, bf16);
+  if (st != LF_OK) return st;
+  if ((int64_t)P.B * P.H * P.n == 0) return LF_OK;
+  if (bf16 && !encode_fn()) {
+    set_error("cuTensorMapEncodeTiled is not available from the driver");
+    return LF_ERR_CUDA;
+  }
+  cudaGetLastError();  // a stale error from someone else must not be reported as ours
+  if (t_band_start) {
+    cudaError_t e = cudaEventRecord(t_band_start, P.stream);
+    if (e != cudaSuccess) {
+      set_error("cudaEventRecord: %s", cudaGetErrorString(e));
+      return LF_ERR_CUDA;
+    }
+  }
+  for (int b0 = 0; b0 < P.B; b0 += kMaxBatch) {
+    const int nb = std::min(kMaxBatch, P.B - b0);
+    st = bf16 ? run_band_bf16(P, b0, nb) : run_band_f32(P, b0, nb);
+    if (st != LF_OK) return st;
+  }
+  if (t_band_stop) {
+    cudaError_t e = cudaEventRecord(t_band_stop, P.stream);
+    if (e != cudaSuccess) {
+      set_error("cudaEventRecord: %s", cudaGetErrorString(e));
+      return LF_ERR_CUDA;
+    }
+  }
+  for (int b0 = 0; b0 < P.B; b0 += kMaxBatch) {
+    const int nb = std::min(kMaxBatch, P.B - b0);
+    st = bf16 ? run_global_rows<__nv_bfloat16>(P, b0, nb) : run_global_rows<float>(P, b0, nb);
+    if (st != LF_OK) return st;
+  }
+  return LF_OK;
+}
+
+}  // namespace lf
+
+// ====================================================================== C ABI
+extern "C" {
+
+lf_status lf_attn_fwd(const void* q, const void* k, const void* v, const void* qg, const void* kg,
+                      const void* vg, const int32_t* global_idx, int32_t n_global, void* out,
+                      int32_t B, int32_t H, int32_t n, int32_t d, int32_t w,
+                      const int32_t* dilation, int32_t causal, const int32_t* pad_len,
+                      cudaStream_t stream) {
+  lf::Problem P{q, k, v, qg, kg, vg, global_idx, n_global, out, B, H, n, d, w, dilation, causal,
+                pad_len, stream, 2};
+  return lf::forward(P, true);
+}
+
+lf_status lf_attn_fwd_f32(const void* q, const void* k, const void* v, const void* qg,
+                          const void* kg, const void* vg, const int32_t* global_idx,
+                          int32_t n_global, void* out, int32_t B, int32_t H, int32_t n, int32_t d,
+                          int32_t w, const int32_t* dilation, int32_t causal,
+                          const int32_t* pad_len, cudaStream_t stream) {
+  lf::Problem P{q, k, v, qg, kg, vg, global_idx, n_global, out, B, H, n, d, w, dilation, causal,
+                pad_len, stream, 4};
+  return lf::forward(P, false);
+}
+
+lf_status lf_attn_count_pairs(int32_t B, int32_t H, int32_t n, int32_t d, int32_t w,
+                              const int32_t* dilation, int32_t causal, const int32_t* pad_len,
+                              const int32_t* global_idx, int32_t n_global, int64_t* pairs,
+                              double* flops) {
+  lf::t_msg[0] = 0;
+  lf::Problem P{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, global_idx, n_global, nullptr,
+                B, H, n, d, w, dilation, causal, pad_len, nullptr, 1};
+  lf_status st = lf::validate_pattern(P);
+  if (st != LF_OK) return st;
+  if (!pairs && !flops) return LF_OK;
+  const int64_t half = std::min<int64_t>(w / 2, n);
+  const int64_t right = causal ? 0 : half;
+  int64_t total = 0;
+  for (int b = 0; b < B; ++b) {
+    const int64_t L = n - (pad_len ? pad_len[b] : 0);
+    for (int h = 0; h < H; ++h) {
+      const int64_t delta = dilation[h];
+      for (int64_t i = 0; i < L; ++i) {
+        // global row?
+        int lo = 0, hi = n_global - 1, is_g = 0;
+        while (lo <= hi) {
+          const int mid = (lo + hi) / 2;
+          if (global_idx[mid] == i) { is_g = 1; break; }
+          if (global_idx[mid] < i) lo = mid + 1; else hi = mid - 1;
+        }
+        if (is_g) {
+          total += causal ? (i + 1) : L;
+          continue;
+        }
+        // window steps t in [-half, right] with 0 <= i + delta*t < L
+        const int64_t tlo = std::max<int64_t>(-half, -(i / delta));
+        const int64_t thi = std::min<int64_t>(right, (L - 1 - i) / delta);
+        int64_t cnt = thi >= tlo ? thi - tlo + 1 : 0;
+        for (int r = 0; r < n_global; ++r) {
+          const int64_t g = global_idx[r];
+          if (g >= L || (causal && g > i)) continue;
+          const int64_t o = g - i;
+          if (o % delta == 0 && o / delta >= -half && o / delta <= right) continue;
+          ++cnt;
+        }
+        total += cnt;
+      }
+    }
+  }
+  if (pairs) *pairs = total;
+  if (flops) *flops = 4.0 * (double)d * (double)total;
+  return LF_OK;
+}
+
+const char* lf_status_string(lf_status s) {
+  switch (s) {
+    case LF_OK: return "LF_OK";
+    case LF_ERR_INVALID_ARG: return "LF_ERR_INVALID_ARG";
+    case LF_ERR_UNSUPPORTED: return "LF_ERR_UNSUPPORTED";
+    case LF_ERR_CUDA: return "LF_ERR_CUDA";
+    case LF_ERR_NO_MEMORY: return "LF_ERR_NO_MEMORY";
+    case LF_ERR_TIMEOUT: return "LF_ERR_TIMEOUT";
+  }
+  return "LF_ERR_UNKNOWN";
+}
+
+const char* lf_last_error_message(void) { return lf::t_msg; }
+
+lf_status lf_attn_set_band_events(cudaEvent_t start, cudaEvent_t stop) {
+  if ((start == nullptr) != (stop == nullptr)) {
+    lf::set_error("set both band events or neither");
+    return LF_ERR_INVALID_ARG;
+  }
+  lf::t_band_start = start;
+  lf::t_band_stop = stop;
+  return LF_OK;
+}
+
+uint64_t lf_attn_launch_count(void) { return lf::g_launches.load(std::memory_order_relaxed); }
+
+lf_status lf_device_error(uint32_t* code, int32_t clear) {
+  if (!code) {
+    lf::set_error("code must not be NULL");
+    return LF_ERR_INVALID_ARG;
+  }
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(code, lf::g_device_error, sizeof(uint32_t));
+  if (e == cudaSuccess && clear) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(lf::g_device_error, &zero, sizeof zero);
+  }
+  if (e != cudaSuccess) {
+    lf::set_error("reading the device error word: %s", cudaGetErrorString(e));
+    return LF_ERR_CUDA;
+  }
+  return LF_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,271 @@
+// lf_internal.cuh -- shared definitions of the CUDA library (not part of the ABI).
+//
+// Parameter blocks passed by value to the kernels, limits, the device error
+// word, and thin inline-PTX wrappers for the sm_100-family features the band
+// kernel uses: mbarriers, TMA tensor loads, and tcgen05 (TMEM allocation,
+// MMA, commit, TMEM loads/stores).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/lf_attn.h"
+
+namespace lf {
+
+// ----------------------------------------------------------------- limits
+constexpr int kMaxSets = 8;      // (dilation, residue) tensor-map sets per band launch
+constexpr int kMaxSeg = 128;     // (head, residue) segments per band launch
+constexpr int kMaxBatch = 256;   // batch rows per launch (larger B is split on the host)
+constexpr int kMaxGlobal = LF_MAX_GLOBAL;
+
+// ----------------------------------------------------------------- error word
+// Bits 0-7: lf_status of the failure; bits 8-15: role that gave up.
+enum Role : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleDrain = 4 };
+// Defined once here: the library is built as a single translation unit.
+__device__ uint32_t g_device_error = 0;
+
+// ----------------------------------------------------------------- band kernel params
+// A segment is one (head, residue class) of the dilated window: rows
+// i = r + delta*m for m in [0, n_r).  Tiles of 128 such rows are work items.
+struct BandSeg {
+  int32_t h, r, delta, n_r, tiles, set, begin, pad_;
+};
+
+struct BandParams {
+  CUtensorMap tq[kMaxSets];  // per (delta, r): dims {d, n_r, B*H}, row stride delta*d
+  CUtensorMap tk[kMaxSets];
+  CUtensorMap tv[kMaxSets];
+  const __nv_bfloat16* k;  // row gathers of the global tokens' keys/values
+  const __nv_bfloat16* v;
+  __nv_bfloat16* out;
+  int32_t B, H, n;
+  int32_t half, right;     // window reach in steps: look-back half, look-ahead right
+  int32_t causal, G, nseg, items_per_b, total_items;
+  float sl2;               // log2(e) / sqrt(d)
+  int32_t pad[kMaxBatch];
+  BandSeg seg[kMaxSeg];
+  int32_t gidx[kMaxGlobal];
+};
+
+// ----------------------------------------------------------------- simt / global-row params
+struct PatternParams {
+  int32_t B, H, n, d, half, right, causal, G;
+  float scale;
+  int32_t dil_max;               // unused by kernels; kept for host checks
+  int32_t pad[kMaxBatch];
+  int32_t gidx[kMaxGlobal];
+};
+
+// dilation per head for the SIMT kernel (heads beyond are split on the host)
+constexpr int kMaxHeadsSimt = 256;
+struct SimtParams {
+  PatternParams pat;
+  int32_t dil[kMaxHeadsSimt];
+};
+
+// ----------------------------------------------------------------- host-side launchers
+struct LaunchCtx {
+  cudaStream_t stream;
+  cudaEvent_t band_start, band_stop;  // optional
+};
+
+// All return LF_OK or an error status and set the thread's message.
+lf_status launch_band_tc(const BandParams& p, int d, int grid, cudaStream_t s);
+lf_status launch_band_simt_f32(const SimtParams& p, const float* q, const float* k, const float* v,
+                               float* out, cudaStream_t s);
+template <typename T>
+lf_status launch_global_rows(const PatternParams& p, const T* qg, const T* kg, const T* vg, T* out,
+                             float* ws, int nchunks, int chunk, cudaStream_t s);
+
+void set_error(const char* fmt, ...);
+void count_launch(int k = 1);
+
+// ----------------------------------------------------------------- device helpers
+#ifdef __CUDACC__
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: gives up after `limit_ns` or when *abort becomes non-zero.
+// On giving up it records the role in the device error word, raises *abort
+// and returns false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint32_t role, uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > limit_ns) {
+        atomicCAS(&g_device_error, 0u, (uint32_t)LF_ERR_TIMEOUT | (role << 8));
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait by a whole warp; the lanes agree on the outcome.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint32_t role) {
+  const bool ok = mbar_wait(bar, parity, abort, role);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---- tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, bf16 in, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation issued so far by this thread completes.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: 128-byte swizzle, version 1 (sm_100 family).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.
+// b_mn_major: B operand stored with N contiguous (as V is).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn_major << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// 32 lanes x 32 consecutive fp32 columns: thread t of the warp receives lane
+// (32*(warp%4) + t) of TMEM, columns [col, col+32).  Waits for completion.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&f)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&f)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(__float_as_uint(f[0])), "r"(__float_as_uint(f[1])), "r"(__float_as_uint(f[2])),
+      "r"(__float_as_uint(f[3])), "r"(__float_as_uint(f[4])), "r"(__float_as_uint(f[5])),
+      "r"(__float_as_uint(f[6])), "r"(__float_as_uint(f[7])), "r"(__float_as_uint(f[8])),
+      "r"(__float_as_uint(f[9])), "r"(__float_as_uint(f[10])), "r"(__float_as_uint(f[11])),
+      "r"(__float_as_uint(f[12])), "r"(__float_as_uint(f[13])), "r"(__float_as_uint(f[14])),
+      "r"(__float_as_uint(f[15])), "r"(__float_as_uint(f[16])), "r"(__float_as_uint(f[17])),
+      "r"(__float_as_uint(f[18])), "r"(__float_as_uint(f[19])), "r"(__float_as_uint(f[20])),
+      "r"(__float_as_uint(f[21])), "r"(__float_as_uint(f[22])), "r"(__float_as_uint(f[23])),
+      "r"(__float_as_uint(f[24])), "r"(__float_as_uint(f[25])), "r"(__float_as_uint(f[26])),
+      "r"(__float_as_uint(f[27])), "r"(__float_as_uint(f[28])), "r"(__float_as_uint(f[29])),
+      "r"(__float_as_uint(f[30])), "r"(__float_as_uint(f[31]))
+      : "memory");
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+#endif  // __CUDACC__
+
+}  // namespace lf

@@ -1,0 +1,164 @@
+"""The C-ABI library on the host (no GPU): it builds, loads, exports every
+symbol include/lf_attn.h declares, rejects invalid arguments before touching
+the device, and counts the pattern's useful work exactly."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import long_sequence_sliding_longformer_b300 as lf
+from long_sequence_sliding_longformer_b300 import _build
+import oracle
+import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lf_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return lf.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lf_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for want in ("lf_attn_fwd", "lf_attn_fwd_f32", "lf_status_string", "lf_last_error_message"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(["LF_OK", "LF_ERR_INVALID_ARG", "LF_ERR_UNSUPPORTED", "LF_ERR_CUDA",
+                                 "LF_ERR_NO_MEMORY", "LF_ERR_TIMEOUT"]):
+        assert lib.lf_status_string(code).decode() == name
+    assert lib.lf_status_string(99).decode() == "LF_ERR_UNKNOWN"
+
+
+def _arr(xs):
+    return (ctypes.c_int32 * max(len(xs), 1))(*xs)
+
+
+FAKE = 0x10000  # an aligned address that is never dereferenced: validation rejects first
+
+
+def _call(lib, fn="lf_attn_fwd", *, q=FAKE, k=FAKE + 0x100000, v=FAKE + 0x200000, qg=None, kg=None,
+          vg=None, gidx=None, G=0, out=FAKE + 0x300000, B=1, H=1, n=64, d=64, w=8, dil=(1,),
+          causal=0, pad=None):
+    f = getattr(lib, fn)
+    return f(q, k, v, qg, kg, vg, _arr(gidx) if gidx is not None else None, G, out, B, H, n, d, w,
+             _arr(dil) if dil is not None else None, causal, _arr(pad) if pad is not None else None, None)
+
+
+INVALID = [
+    dict(w=7),                       # odd window
+    dict(w=-2),
+    dict(B=-1),
+    dict(n=-5),
+    dict(d=0),
+    dict(causal=2),
+    dict(dil=(0,)),
+    dict(dil=None),
+    dict(q=None),
+    dict(out=None),
+    dict(q=FAKE + 8),                # misaligned
+    dict(out=FAKE),                  # aliases q
+    dict(pad=(65,)),                 # pad > n
+    dict(pad=(-1,)),
+    dict(G=2, gidx=None, qg=FAKE + 0x400000, kg=FAKE + 0x500000, vg=FAKE + 0x600000),
+    dict(G=2, gidx=(3, 3), qg=FAKE + 0x400000, kg=FAKE + 0x500000, vg=FAKE + 0x600000),
+    dict(G=2, gidx=(5, 2), qg=FAKE + 0x400000, kg=FAKE + 0x500000, vg=FAKE + 0x600000),
+    dict(G=1, gidx=(64,), qg=FAKE + 0x400000, kg=FAKE + 0x500000, vg=FAKE + 0x600000),
+    dict(G=1, gidx=(0,), qg=None, kg=FAKE + 0x500000, vg=FAKE + 0x600000),
+    dict(G=-1),
+]
+
+
+@pytest.mark.parametrize("kw", INVALID, ids=[str(k) for k in INVALID])
+@pytest.mark.parametrize("fn", ["lf_attn_fwd", "lf_attn_fwd_f32"])
+def test_invalid_arguments_are_rejected_on_the_host(lib, fn, kw):
+    assert _call(lib, fn, **kw) == 1
+    assert lib.lf_last_error_message().decode() != ""
+
+
+@pytest.mark.parametrize("kw", [dict(d=32), dict(d=96), dict(d=256)])
+def test_bf16_head_dims_outside_64_128_are_unsupported(lib, kw):
+    assert _call(lib, "lf_attn_fwd", **kw) == 2
+
+
+def test_fp32_head_dim_limit(lib):
+    assert _call(lib, "lf_attn_fwd_f32", d=129) == 2
+
+
+def test_too_many_globals_unsupported(lib):
+    g = list(range(4097))
+    assert _call(lib, n=5000, G=4097, gidx=g, qg=FAKE + 0x4000000, kg=FAKE + 0x8000000,
+                 vg=FAKE + 0xC000000, q=FAKE, k=FAKE + 0x1000000, v=FAKE + 0x2000000,
+                 out=FAKE + 0x3000000) == 2
+
+
+def test_empty_problems_are_no_ops(lib):
+    for kw in (dict(B=0), dict(H=0, dil=()), dict(n=0)):
+        assert _call(lib, **kw) == 0
+
+
+def _oracle_pairs(B, H, n, w, dil, causal, pad, gidx):
+    tot = 0
+    for b in range(B):
+        for h in range(H):
+            for i in range(n):
+                keys, _ = oracle.attended(n=n, w=w, dilation=dil, causal=causal, global_idx=gidx,
+                                          pad_len=pad, b=b, h=h, i=i, B=B)
+                tot += len(keys)
+    return tot
+
+
+@pytest.mark.parametrize("B,H,n,w,dil,causal,pad,gidx", [
+    (1, 1, 64, 8, [1], False, None, []),
+    (2, 2, 100, 10, [1, 3], True, [0, 17], [0, 50]),
+    (1, 3, 37, 0, [1, 2, 5], False, [4], [1, 2, 36]),
+    (2, 1, 50, 200, [2], False, [0, 49], [7]),
+    (1, 2, 90, 12, [4, 1], True, None, list(range(0, 90, 9))),
+])
+def test_pair_count_matches_oracle_sets(lib, B, H, n, w, dil, causal, pad, gidx):
+    pairs, flops = lf.count_pairs(B=B, H=H, n=n, d=8, w=w, dilation=dil, causal=causal, pad_len=pad,
+                                  global_idx=gidx)
+    assert pairs == _oracle_pairs(B, H, n, w, dil, causal, pad, gidx)
+    assert flops == 4 * 8 * pairs
+
+
+def test_pair_count_of_named_workloads(lib):
+    # the fp32 window-64 workload: 512 rows, interior rows attend 65 keys
+    wl = workloads.fp32_window64()
+    pairs, _ = lf.count_pairs(B=wl.B, H=wl.H, n=wl.n, d=wl.d, w=wl.w, dilation=wl.dilation)
+    assert pairs == 512 * 65 - 2 * sum(32 - t for t in range(32))
+    # the causal char-LM workload: look-back 256 on every residue class
+    wl = workloads.bf16_charlm()
+    pairs, _ = lf.count_pairs(B=wl.B, H=wl.H, n=wl.n, d=wl.d, w=wl.w, dilation=wl.dilation,
+                              causal=True)
+    want = 0
+    for delta in wl.dilation:
+        for r in range(delta):
+            n_r = len(range(r, wl.n, delta))
+            want += sum(min(m, 256) + 1 for m in range(n_r))
+    assert pairs == want
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    import importlib
+    monkeypatch.setattr(lf, "LIB_PATH", str(tmp_path / "nope.so"))
+    monkeypatch.setattr(lf, "_lib", None)
+    with pytest.raises(RuntimeError):
+        lf.load()
