@@ -48,7 +48,8 @@ struct BandCfg {
 };
 
 struct ItemInfo {
-  int b, h, r, delta, n_r, set, m0, Lb, Lm, kstart, nb, ngt;
+  int b, h, r, delta, n_r, set, m0, Lb, Lm, kstart, kend, nb, ngt;
+  int i_last;  // position of the tile's last valid query row
   bool zero;
 };
 
@@ -73,8 +74,9 @@ __device__ __forceinline__ ItemInfo decode_item(const BandParams& p, int item) {
   it.zero = it.m0 >= it.Lm;
   it.kstart = max(0, it.m0 - p.half);
   const int lastq = min(it.m0 + 127, it.Lm - 1);
-  const int kend = min(it.Lm - 1, lastq + p.right);
-  it.nb = it.zero ? 0 : (kend - it.kstart) / 128 + 1;
+  it.kend = min(it.Lm - 1, lastq + p.right);  // last key any row of the tile attends
+  it.i_last = it.r + it.delta * lastq;
+  it.nb = it.zero ? 0 : (it.kend - it.kstart) / 128 + 1;
   it.ngt = it.zero ? 0 : (p.G + 127) / 128;
   return it;
 }
@@ -172,9 +174,12 @@ __device__ void band_producer(const BandParams& p, const BandSmem<D>& sm, int la
       const int ng = (cnt + 15) & ~15;
       int* gpos = sm.gpos(s);
       int* gm = sm.gm(s);
+      // a global key no row of this tile may attend (padding, or after the
+      // tile's last row when causal) is stored as zeros
+      const int g_lim = p.causal ? min(it.Lb - 1, it.i_last) : it.Lb - 1;
       for (int c = lane; c < 128; c += 32) {
         const int g = (c < cnt) ? p.gidx[g0 + c] : -1;
-        const bool valid = (c < cnt) && g < it.Lb;
+        const bool valid = (c < cnt) && g <= g_lim;
         gpos[c] = valid ? g : -1;
         int mg = -(1 << 29);  // "not in this residue class": never inside the band
         if (valid && (g - it.r) % it.delta == 0) mg = (g - it.r) / it.delta;
@@ -190,7 +195,7 @@ __device__ void band_producer(const BandParams& p, const BandSmem<D>& sm, int la
         uint4 kx = make_uint4(0, 0, 0, 0), vx = make_uint4(0, 0, 0, 0);
         if (row < cnt) {
           const int g = p.gidx[g0 + row];
-          if (g < it.Lb) {
+          if (g <= g_lim) {
             kx = __ldg(reinterpret_cast<const uint4*>(kb + (size_t)g * D) + ch);
             vx = __ldg(reinterpret_cast<const uint4*>(vb + (size_t)g * D) + ch);
           }
@@ -410,12 +415,14 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
           }
         }
       }
-      // ---- value rows past the valid length may hold anything: zero them
+      // ---- value rows after the last key any row of the tile attends (the
+      // padding, and keys outside every window of the tile) are zeroed, so
+      // whatever they hold cannot reach the output through 0 * value
       if (is_band) {
         const int kb = it.kstart + 128 * j;
-        if (kb + 127 >= it.Lm) {
+        if (kb + 127 > it.kend) {
           if (!warp_wait(sm.kv_full(s), (kvj / C::kStages) & 1, abort, kRoleSoftmax)) { ok = false; break; }
-          if (kb + row >= it.Lm) {
+          if (kb + row > it.kend) {
             uint8_t* vs = sm.v_ptr(s);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c)

@@ -222,6 +222,24 @@ def test_causal_rows_ignore_later_tiles(dtype):
     assert torch.equal(out[:, :, :P0], base[:, :, :P0])
 
 
+def test_keys_outside_every_window_of_a_tile_cannot_reach_it():
+    """The band kernel computes 128 query rows at a time; a key outside the
+    union of that tile's windows (and not global) must not affect those rows,
+    whatever it holds."""
+    n, w, t = 2048, 128, 6
+    wl = workloads.custom("oow", "bf16", 1, 2, n, 64, w, (1, 1), False, (5,), None, seed=11)
+    inp = workloads.make_inputs(wl, "cuda")
+    base = run(wl, inp).clone()
+    lo, hi = 128 * t - w // 2, 128 * t + 127 + w // 2
+    outside = torch.ones(n, dtype=torch.bool, device="cuda")
+    outside[lo:hi + 1] = False
+    outside[5] = False
+    for x in (inp.q, inp.k, inp.v):
+        x[:, :, outside] = float("nan")
+    out = run(wl, inp)
+    assert torch.equal(out[:, :, 128 * t:128 * t + 128], base[:, :, 128 * t:128 * t + 128])
+
+
 def test_full_window_equals_dense_attention():
     """w >= 2n, one head, no globals: ordinary attention (checked against
     torch's fp32 SDPA on the same bf16 values)."""
