@@ -253,6 +253,10 @@ def run_gpu(args, wl):
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     bev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in bev:  # torch creates the underlying CUDA events on first record
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
     launches0 = lf.launch_count()
     with ClockSampler(dev.index) as clocks:
         barrier(ws)

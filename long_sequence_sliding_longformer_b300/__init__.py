@@ -141,6 +141,9 @@ def count_pairs(*, B: int, H: int, n: int, d: int, w: int, dilation: Sequence[in
 
 def set_band_events(start: Optional[torch.cuda.Event], stop: Optional[torch.cuda.Event]):
     """Record `start`/`stop` around the band kernel of every later call (None, None clears)."""
+    for e in (start, stop):
+        if e is not None and not e.cuda_event:
+            raise ValueError("record the event once before passing it (torch creates it lazily)")
     sp = None if start is None else ctypes.c_void_p(start.cuda_event)
     ep = None if stop is None else ctypes.c_void_p(stop.cuda_event)
     _check(load().lf_attn_set_band_events(sp, ep))
