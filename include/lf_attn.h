@@ -87,6 +87,36 @@ lf_status lf_attn_fwd_f32(const void* q, const void* k, const void* v,
                           const int32_t* pad_len, cudaStream_t stream);
 
 /*
+ * lf_attn_fwd without any device memory allocation.  The pages have no
+ * counterpart to this: it is an interface choice, not part of the method.
+ *
+ * lf_attn_fwd allocates the scratch of its global-row pass (stream-ordered,
+ * on every call with n_global > 0).  This variant is for callers that cannot
+ * allocate device memory while they run: an engine that reserves its whole
+ * memory budget at start-up, code that must not meet an out-of-memory error
+ * or allocator latency in the middle of a step, or a host application that
+ * owns the CUDA allocator and does not let plug-ins call it.
+ *
+ * Same arguments, semantics and results as lf_attn_fwd (bf16; results agree
+ * within rounding, since the global rows may be split into longer key
+ * chunks).  The scratch is a 16 MiB array inside the library that every GPU
+ * loading the library holds until the process exits.  The first call on each
+ * device looks up that array's device address, so make the first call on a
+ * device before any stream capture.  Returns LF_ERR_UNSUPPORTED when
+ * B*H*n_global*(d+2) fp32 values (per block of 256 batch rows) exceed the
+ * array.  All calls share the array and it keeps the last call's contents
+ * (every value a call reads is written earlier in that call): calls whose
+ * kernels overlap on the GPU, e.g. on two streams at once, race on it.
+ */
+lf_status lf_attn_fwd_noalloc(const void* q, const void* k, const void* v,
+                              const void* qg, const void* kg, const void* vg,
+                              const int32_t* global_idx, int32_t n_global,
+                              void* out,
+                              int32_t B, int32_t H, int32_t n, int32_t d,
+                              int32_t w, const int32_t* dilation, int32_t causal,
+                              const int32_t* pad_len, cudaStream_t stream);
+
+/*
  * Host-only: the useful work of a problem, counted exactly from the pattern.
  * *pairs = number of attended (query, key) pairs over all valid rows and
  * heads; *flops = 4 * d * pairs (one multiply-add each for QK^T and PV).

@@ -537,3 +537,6 @@ lf_status lf_device_error(uint32_t* code, int32_t clear) {
 }
 
 }  // extern "C"
+
+// The allocation-free variant of lf_attn_fwd (same translation unit).
+#include "lf_noalloc.cuh"
