@@ -189,10 +189,176 @@ global_partial_kernel(const __grid_constant__ PatternParams p, const T* __restri
   }
 }
 
+// bf16 streaming variant for a few global queries (NQ <= 8 per CTA).  Each
+// key row is split into 16-byte chunks across CH = D/8 lanes, so a warp reads
+// 32/CH whole rows per step with coalesced 16-byte loads; a lane keeps the
+// running (max, sum, weighted values) of its key slot for its 8 columns, and
+// the slots and warps are merged in a fixed order at the end.
+constexpr int kGsWarps = 4;
+
+template <int D, int NQ>
+__global__ void __launch_bounds__(kGsWarps * 32)
+global_partial_stream_kernel(const __grid_constant__ PatternParams p,
+                             const __nv_bfloat16* __restrict__ qg,
+                             const __nv_bfloat16* __restrict__ kg,
+                             const __nv_bfloat16* __restrict__ vg, float* __restrict__ ws,
+                             int nchunks, int chunk) {
+  constexpr int CH = D / 8;       // 16-byte chunks per row
+  constexpr int KPW = 32 / CH;    // key rows per warp step
+  __shared__ float red[kGsWarps][NQ][D + 2];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ks = lane / CH, c = lane % CH;
+  const int g0 = blockIdx.x * NQ;
+  const int c_idx = blockIdx.y;
+  const int64_t bh = blockIdx.z;
+  const int gq = min(NQ, p.G - g0);
+  const int b = (int)(bh / p.H);
+  const int L = p.n - p.pad[b];
+  const float sl2 = p.scale * 1.4426950408889634f;
+  const float NEG_INF = -__int_as_float(0x7f800000);
+
+  float qv[NQ][8];
+  int gpos[NQ];
+#pragma unroll
+  for (int g = 0; g < NQ; ++g) {
+    gpos[g] = (g < gq) ? p.gidx[g0 + g] : -1;
+    uint4 x = make_uint4(0, 0, 0, 0);
+    if (g < gq) x = __ldg(reinterpret_cast<const uint4*>(qg + ((bh * p.G) + g0 + g) * D) + c);
+    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(h2[e]);
+      qv[g][2 * e] = f.x * sl2;
+      qv[g][2 * e + 1] = f.y * sl2;
+    }
+  }
+  float m[NQ], l[NQ], acc[NQ][8];
+#pragma unroll
+  for (int g = 0; g < NQ; ++g) {
+    m[g] = NEG_INF;
+    l[g] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
+  }
+
+  const int k_begin = c_idx * chunk;
+  const int k_end = min(k_begin + chunk, L);
+  const uint4* kb = reinterpret_cast<const uint4*>(kg + bh * (int64_t)p.n * D);
+  const uint4* vb = reinterpret_cast<const uint4*>(vg + bh * (int64_t)p.n * D);
+  constexpr int U = 4;  // key steps in flight per warp
+  constexpr int STEP = kGsWarps * KPW;
+  for (int j00 = k_begin + warp * KPW; j00 < k_end; j00 += U * STEP) {
+   uint4 kxs[U], vxs[U];
+#pragma unroll
+   for (int u = 0; u < U; ++u) {
+    const int j = j00 + u * STEP + ks;
+    kxs[u] = make_uint4(0, 0, 0, 0);
+    vxs[u] = make_uint4(0, 0, 0, 0);
+    if (j < k_end) {
+      kxs[u] = __ldg(kb + (int64_t)j * CH + c);
+      vxs[u] = __ldg(vb + (int64_t)j * CH + c);
+    }
+   }
+#pragma unroll
+   for (int u = 0; u < U; ++u) {
+    const int j = j00 + u * STEP + ks;
+    const bool valid = j < k_end;
+    float kf[8], vf[8];
+    {
+      const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kxs[u]);
+      const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&vxs[u]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 a = __bfloat1622float2(k2[e]);
+        const float2 bb = __bfloat1622float2(v2[e]);
+        kf[2 * e] = a.x;
+        kf[2 * e + 1] = a.y;
+        vf[2 * e] = bb.x;
+        vf[2 * e + 1] = bb.y;
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < NQ; ++g) {
+      float s = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) s = fmaf(qv[g][e], kf[e], s);
+#pragma unroll
+      for (int off = CH / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      const bool ok = valid && g < gq && (!p.causal || j <= gpos[g]);
+      if (ok) {
+        if (s > m[g]) {
+          const float alpha = ex2_approx(m[g] - s);  // 0 when m was -inf
+          l[g] *= alpha;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[g][e] *= alpha;
+          m[g] = s;
+        }
+        const float pw = ex2_approx(s - m[g]);
+        l[g] += pw;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[g][e] = fmaf(pw, vf[e], acc[g][e]);
+      }
+    }
+   }
+  }
+  // merge the key slots of this warp (lanes c, c+CH, ...), in a fixed order
+#pragma unroll
+  for (int off = CH; off < 32; off <<= 1) {
+#pragma unroll
+    for (int g = 0; g < NQ; ++g) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m[g], off);
+      const float l2 = __shfl_xor_sync(0xffffffffu, l[g], off);
+      const float mn = fmaxf(m[g], m2);
+      const float fa = (m[g] == NEG_INF) ? 0.f : ex2_approx(m[g] - mn);
+      const float fb = (m2 == NEG_INF) ? 0.f : ex2_approx(m2 - mn);
+      l[g] = l[g] * fa + l2 * fb;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float a2 = __shfl_xor_sync(0xffffffffu, acc[g][e], off);
+        acc[g][e] = acc[g][e] * fa + a2 * fb;
+      }
+      m[g] = mn;
+    }
+  }
+  if (ks == 0) {
+#pragma unroll
+    for (int g = 0; g < NQ; ++g) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) red[warp][g][2 + c * 8 + e] = acc[g][e];
+      if (c == 0) {
+        red[warp][g][0] = m[g];
+        red[warp][g][1] = l[g];
+      }
+    }
+  }
+  __syncthreads();
+  // merge the warps in order and write the chunk's partial state
+  for (int idx = tid; idx < gq * (D + 2); idx += kGsWarps * 32) {
+    const int g = idx / (D + 2), col = idx - (idx / (D + 2)) * (D + 2);
+    float mm = NEG_INF;
+#pragma unroll
+    for (int w = 0; w < kGsWarps; ++w) mm = fmaxf(mm, red[w][g][0]);
+    float val = 0.f;
+    if (col == 0) {
+      val = mm;
+    } else {
+#pragma unroll
+      for (int w = 0; w < kGsWarps; ++w) {
+        const float mw = red[w][g][0];
+        const float f = (mw == NEG_INF) ? 0.f : ex2_approx(mw - mm);
+        val = fmaf(red[w][g][col], f, val);
+      }
+    }
+    ws[((bh * nchunks + c_idx) * p.G + g0 + g) * (D + 2) + col] = val;
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(128)
 global_merge_kernel(const __grid_constant__ PatternParams p, const float* __restrict__ ws,
                     T* __restrict__ out, int nchunks) {
+  __shared__ float red_m[4];
   const int g = blockIdx.x;
   const int64_t bh = blockIdx.y;
   const int b = (int)(bh / p.H);
@@ -202,19 +368,28 @@ global_merge_kernel(const __grid_constant__ PatternParams p, const float* __rest
   const float NEG_INF = -__int_as_float(0x7f800000);
   T* orow = out + (bh * p.n + pos) * D;
   const int c = threadIdx.x;
+  const float* base = ws + ((bh * nchunks) * p.G + g) * (D + 2);
+  const int64_t cstride = (int64_t)p.G * (D + 2);
+  // maximum over the chunks, all threads at once
+  float M = NEG_INF;
+  for (int ch = c; ch < nchunks; ch += 128) M = fmaxf(M, base[ch * cstride]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if ((c & 31) == 0) red_m[c >> 5] = M;
+  __syncthreads();
+  M = fmaxf(fmaxf(red_m[0], red_m[1]), fmaxf(red_m[2], red_m[3]));
   if (c >= D) return;
   if (pos >= L) {
     from_f<T>(orow + c, 0.f);
     return;
   }
-  float M = NEG_INF;
-  for (int ch = 0; ch < nchunks; ++ch) M = fmaxf(M, ws[((bh * nchunks + ch) * p.G + g) * (D + 2)]);
   float l = 0.f, a = 0.f;
   if (M != NEG_INF) {
+#pragma unroll 4
     for (int ch = 0; ch < nchunks; ++ch) {
-      const float* e = ws + ((bh * nchunks + ch) * p.G + g) * (D + 2);
-      if (e[0] == NEG_INF) continue;
-      const float f = ex2_approx(e[0] - M);
+      const float* e = base + ch * cstride;
+      const float me = e[0];
+      const float f = (me == NEG_INF) ? 0.f : ex2_approx(me - M);
       l = fmaf(e[1], f, l);
       a = fmaf(e[2 + c], f, a);
     }
@@ -222,31 +397,80 @@ global_merge_kernel(const __grid_constant__ PatternParams p, const float* __rest
   from_f<T>(orow + c, l > 0.f ? a / l : 0.f);
 }
 
+// Query-block size of the streaming kernel for a given number of global tokens.
+inline int stream_nq(int G) { return G >= 8 ? 8 : (G >= 4 ? 4 : (G >= 2 ? 2 : 1)); }
+
 template <typename T>
-lf_status launch_global_rows(const PatternParams& p, const T* qg, const T* kg, const T* vg, T* out,
-                             float* ws, int nchunks, int chunk, cudaStream_t s) {
+inline bool launch_partial_stream(const PatternParams&, const T*, const T*, const T*, float*, int,
+                                  int, cudaStream_t) {
+  return false;  // fp32 inputs use the generic kernel
+}
+
+template <int D>
+inline void launch_stream_d(const PatternParams& p, const __nv_bfloat16* qg, const __nv_bfloat16* kg,
+                            const __nv_bfloat16* vg, float* ws, int nchunks, int chunk,
+                            cudaStream_t s) {
+  const int nq = stream_nq(p.G);
+  dim3 grid((p.G + nq - 1) / nq, nchunks, (unsigned)((int64_t)p.B * p.H));
+  switch (nq) {
+    case 1: global_partial_stream_kernel<D, 1><<<grid, kGsWarps * 32, 0, s>>>(p, qg, kg, vg, ws, nchunks, chunk); break;
+    case 2: global_partial_stream_kernel<D, 2><<<grid, kGsWarps * 32, 0, s>>>(p, qg, kg, vg, ws, nchunks, chunk); break;
+    case 4: global_partial_stream_kernel<D, 4><<<grid, kGsWarps * 32, 0, s>>>(p, qg, kg, vg, ws, nchunks, chunk); break;
+    default: global_partial_stream_kernel<D, 8><<<grid, kGsWarps * 32, 0, s>>>(p, qg, kg, vg, ws, nchunks, chunk); break;
+  }
+}
+
+template <>
+inline bool launch_partial_stream<__nv_bfloat16>(const PatternParams& p, const __nv_bfloat16* qg,
+                                                 const __nv_bfloat16* kg, const __nv_bfloat16* vg,
+                                                 float* ws, int nchunks, int chunk, cudaStream_t s) {
+  if (p.d == 64) launch_stream_d<64>(p, qg, kg, vg, ws, nchunks, chunk, s);
+  else if (p.d == 128) launch_stream_d<128>(p, qg, kg, vg, ws, nchunks, chunk, s);
+  else return false;
+  return true;
+}
+
+template <typename T>
+lf_status launch_global_partial(const PatternParams& p, const T* qg, const T* kg, const T* vg,
+                                float* ws, int nchunks, int chunk, cudaStream_t s) {
   const int64_t bhs = (int64_t)p.B * p.H;
-  if (bhs > 65535 || nchunks > 0x7fffffff) {
-    set_error("global-row kernels: B*H = %lld exceeds the grid limit", (long long)bhs);
+  if (bhs > 65535 || nchunks > 65535) {
+    set_error("global-row kernels: B*H = %lld or %d key chunks exceed the grid limit", (long long)bhs, nchunks);
     return LF_ERR_UNSUPPORTED;
   }
-  dim3 g1(nchunks, (p.G + kGQ - 1) / kGQ, (unsigned)bhs);
-  global_partial_kernel<T><<<g1, kGThreads, 0, s>>>(p, qg, kg, vg, ws, nchunks, chunk);
+  if (!launch_partial_stream(p, qg, kg, vg, ws, nchunks, chunk, s)) {
+    dim3 g1(nchunks, (p.G + kGQ - 1) / kGQ, (unsigned)bhs);
+    global_partial_kernel<T><<<g1, kGThreads, 0, s>>>(p, qg, kg, vg, ws, nchunks, chunk);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("global partial kernel launch: %s", cudaGetErrorString(e));
     return LF_ERR_CUDA;
   }
   count_launch();
-  dim3 g2(p.G, (unsigned)bhs);
+  return LF_OK;
+}
+
+template <typename T>
+lf_status launch_global_merge(const PatternParams& p, const float* ws, T* out, int nchunks,
+                              cudaStream_t s) {
+  dim3 g2(p.G, (unsigned)((int64_t)p.B * p.H));
   global_merge_kernel<T><<<g2, 128, 0, s>>>(p, ws, out, nchunks);
-  e = cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("global merge kernel launch: %s", cudaGetErrorString(e));
     return LF_ERR_CUDA;
   }
   count_launch();
   return LF_OK;
+}
+
+template <typename T>
+lf_status launch_global_rows(const PatternParams& p, const T* qg, const T* kg, const T* vg, T* out,
+                             float* ws, int nchunks, int chunk, cudaStream_t s) {
+  lf_status st = launch_global_partial<T>(p, qg, kg, vg, ws, nchunks, chunk, s);
+  if (st != LF_OK) return st;
+  return launch_global_merge<T>(p, ws, out, nchunks, s);
 }
 
 template lf_status launch_global_rows<float>(const PatternParams&, const float*, const float*,

@@ -225,44 +225,95 @@ static void fill_pattern(PatternParams& pp, const Problem& P, int b0, int nb) {
 }
 
 // ------------------------------------------------------------------ global rows
-template <typename T>
-static lf_status run_global_rows(const Problem& P, int b0, int nbat) {
-  if (P.G == 0 || nbat == 0) return LF_OK;
-  PatternParams pp;
-  fill_pattern(pp, P, b0, nbat);
-  const size_t off = (size_t)b0 * P.H * P.n * P.d;
-  const size_t goff = (size_t)b0 * P.H * P.G * P.d;
-  // chunk: a multiple of the sub-chunk; grow it until the scratch stays <= 64 MiB
+// Key-chunk length of the global-row pass for batch rows [b0, b0 + nbat):
+// enough CTAs to fill the GPU about four times over, then longer chunks
+// until the partial states stay within 64 MiB.
+static int64_t global_chunk(const Problem& P, int nbat, size_t* ws_floats) {
   const int64_t bh = (int64_t)nbat * P.H;
   const int64_t qblocks = (P.G + kGQ - 1) / kGQ;
-  // enough CTAs to fill the GPU about four times over, in chunks of 128 keys
   int64_t chunk = 128;
   while (chunk * 2 <= P.n && bh * qblocks * ((P.n + chunk * 2 - 1) / (chunk * 2)) >= 4 * sm_count())
     chunk *= 2;
-  auto ws_bytes = [&](int64_t c) {
-    const int64_t nch = (P.n + c - 1) / c;
-    return (size_t)(bh * nch * P.G * (P.d + 2)) * sizeof(float);
-  };
-  while (ws_bytes(chunk) > ((size_t)64 << 20) && chunk < P.n) chunk *= 2;
-  const int nchunks = (int)((P.n + chunk - 1) / chunk);
-  const size_t wsb = ws_bytes(chunk);
+  auto floats = [&](int64_t c) { return (size_t)(bh * ((P.n + c - 1) / c) * P.G * (P.d + 2)); };
+  while (floats(chunk) * sizeof(float) > ((size_t)64 << 20) && chunk < P.n) chunk *= 2;
+  *ws_floats = floats(chunk);
+  return chunk;
+}
+
+// A second stream (and fork/join events) per host thread and device, so the
+// global-row partial pass can run beside the band kernel.
+struct AuxStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kMaxAuxDevices = 16;
+static thread_local AuxStream t_aux[kMaxAuxDevices];
+
+static AuxStream* aux_stream() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxAuxDevices) return nullptr;
+  AuxStream& a = t_aux[dev];
+  if (!a.s) {
+    if (cudaStreamCreateWithFlags(&a.s, cudaStreamNonBlocking) != cudaSuccess) {
+      cudaGetLastError();
+      a.s = nullptr;
+      return nullptr;
+    }
+    if (cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+  }
+  return &a;
+}
+
+// Enqueues the global rows' partial pass on `ps` (after `fork` if set) and
+// records how to merge; the merge runs later on the caller's stream.
+struct GlobalPass {
   float* ws = nullptr;
-  cudaError_t e = cudaMallocAsync((void**)&ws, wsb, P.stream);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    set_error("scratch allocation of %zu bytes failed: %s", wsb, cudaGetErrorString(e));
-    return LF_ERR_NO_MEMORY;
+  size_t floats = 0;
+};
+
+template <typename T>
+static lf_status global_partials(const Problem& P, float* ws, cudaStream_t ps) {
+  size_t off_ws = 0;
+  for (int b0 = 0; b0 < P.B; b0 += kMaxBatch) {
+    const int nb = std::min(kMaxBatch, P.B - b0);
+    size_t nf = 0;
+    const int64_t chunk = global_chunk(P, nb, &nf);
+    const int nchunks = (int)((P.n + chunk - 1) / chunk);
+    PatternParams pp;
+    fill_pattern(pp, P, b0, nb);
+    const size_t off = (size_t)b0 * P.H * P.n * P.d;
+    const size_t goff = (size_t)b0 * P.H * P.G * P.d;
+    lf_status st = launch_global_partial<T>(pp, reinterpret_cast<const T*>(P.qg) + goff,
+                                            reinterpret_cast<const T*>(P.kg) + off,
+                                            reinterpret_cast<const T*>(P.vg) + off, ws + off_ws,
+                                            nchunks, (int)chunk, ps);
+    if (st != LF_OK) return st;
+    off_ws += nf;
   }
-  lf_status st = launch_global_rows<T>(pp, reinterpret_cast<const T*>(P.qg) + goff,
-                                       reinterpret_cast<const T*>(P.kg) + off,
-                                       reinterpret_cast<const T*>(P.vg) + off,
-                                       reinterpret_cast<T*>(P.out) + off, ws, nchunks, (int)chunk, P.stream);
-  cudaError_t fe = cudaFreeAsync(ws, P.stream);
-  if (st == LF_OK && fe != cudaSuccess) {
-    set_error("scratch free failed: %s", cudaGetErrorString(fe));
-    return LF_ERR_CUDA;
+  return LF_OK;
+}
+
+template <typename T>
+static lf_status global_merges(const Problem& P, const float* ws) {
+  size_t off_ws = 0;
+  for (int b0 = 0; b0 < P.B; b0 += kMaxBatch) {
+    const int nb = std::min(kMaxBatch, P.B - b0);
+    size_t nf = 0;
+    const int64_t chunk = global_chunk(P, nb, &nf);
+    const int nchunks = (int)((P.n + chunk - 1) / chunk);
+    PatternParams pp;
+    fill_pattern(pp, P, b0, nb);
+    const size_t off = (size_t)b0 * P.H * P.n * P.d;
+    lf_status st = launch_global_merge<T>(pp, ws + off_ws, reinterpret_cast<T*>(P.out) + off, nchunks,
+                                          P.stream);
+    if (st != LF_OK) return st;
+    off_ws += nf;
   }
-  return st;
+  return LF_OK;
 }
 
 // ------------------------------------------------------------------ bf16 band planning
@@ -381,6 +432,79 @@ static lf_status run_band_f32(const Problem& P, int b0, int nbat) {
                               reinterpret_cast<float*>(P.out) + off, P.stream);
 }
 
+static lf_status record(cudaEvent_t e, cudaStream_t s) {
+  cudaError_t r = cudaEventRecord(e, s);
+  if (r != cudaSuccess) {
+    set_error("cudaEventRecord: %s", cudaGetErrorString(r));
+    return LF_ERR_CUDA;
+  }
+  return LF_OK;
+}
+
+static lf_status wait_event(cudaStream_t s, cudaEvent_t e) {
+  cudaError_t r = cudaStreamWaitEvent(s, e, 0);
+  if (r != cudaSuccess) {
+    set_error("cudaStreamWaitEvent: %s", cudaGetErrorString(r));
+    return LF_ERR_CUDA;
+  }
+  return LF_OK;
+}
+
+template <typename T>
+static lf_status forward_t(const Problem& P, bool bf16) {
+  lf_status st;
+  // ---- global rows: scratch, then the partial pass on a second stream
+  float* ws = nullptr;
+  AuxStream* aux = nullptr;
+  if (P.G > 0) {
+    size_t total = 0;
+    for (int b0 = 0; b0 < P.B; b0 += kMaxBatch) {
+      size_t nf = 0;
+      global_chunk(P, std::min(kMaxBatch, P.B - b0), &nf);
+      total += nf;
+    }
+    cudaError_t e = cudaMallocAsync((void**)&ws, total * sizeof(float), P.stream);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      set_error("scratch allocation of %zu bytes failed: %s", total * sizeof(float), cudaGetErrorString(e));
+      return LF_ERR_NO_MEMORY;
+    }
+    aux = aux_stream();
+    cudaStream_t ps = P.stream;
+    if (aux && record(aux->fork, P.stream) == LF_OK && wait_event(aux->s, aux->fork) == LF_OK) ps = aux->s;
+    else aux = nullptr;
+    st = global_partials<T>(P, ws, ps);
+    if (aux) {
+      // join even on failure so nothing on the side stream outlives the scratch
+      lf_status j = record(aux->join, aux->s);
+      if (j == LF_OK) j = wait_event(P.stream, aux->join);
+      if (st == LF_OK) st = j;
+    }
+    if (st != LF_OK) {
+      cudaFreeAsync(ws, P.stream);
+      return st;
+    }
+  }
+  // ---- band kernel on the caller's stream
+  st = LF_OK;
+  if (t_band_start) st = record(t_band_start, P.stream);
+  for (int b0 = 0; st == LF_OK && b0 < P.B; b0 += kMaxBatch) {
+    const int nb = std::min(kMaxBatch, P.B - b0);
+    st = bf16 ? run_band_bf16(P, b0, nb) : run_band_f32(P, b0, nb);
+  }
+  if (st == LF_OK && t_band_stop) st = record(t_band_stop, P.stream);
+  // ---- merge (after the band kernel, which also wrote the global tokens' rows)
+  if (P.G > 0) {
+    if (st == LF_OK) st = global_merges<T>(P, ws);
+    cudaError_t fe = cudaFreeAsync(ws, P.stream);
+    if (st == LF_OK && fe != cudaSuccess) {
+      set_error("scratch free failed: %s", cudaGetErrorString(fe));
+      st = LF_ERR_CUDA;
+    }
+  }
+  return st;
+}
+
 static lf_status forward(const Problem& P, bool bf16) {
   t_msg[0] = 0;
   lf_status st = validate(P, bf16);
@@ -391,31 +515,7 @@ static lf_status forward(const Problem& P, bool bf16) {
     return LF_ERR_CUDA;
   }
   cudaGetLastError();  // a stale error from someone else must not be reported as ours
-  if (t_band_start) {
-    cudaError_t e = cudaEventRecord(t_band_start, P.stream);
-    if (e != cudaSuccess) {
-      set_error("cudaEventRecord: %s", cudaGetErrorString(e));
-      return LF_ERR_CUDA;
-    }
-  }
-  for (int b0 = 0; b0 < P.B; b0 += kMaxBatch) {
-    const int nb = std::min(kMaxBatch, P.B - b0);
-    st = bf16 ? run_band_bf16(P, b0, nb) : run_band_f32(P, b0, nb);
-    if (st != LF_OK) return st;
-  }
-  if (t_band_stop) {
-    cudaError_t e = cudaEventRecord(t_band_stop, P.stream);
-    if (e != cudaSuccess) {
-      set_error("cudaEventRecord: %s", cudaGetErrorString(e));
-      return LF_ERR_CUDA;
-    }
-  }
-  for (int b0 = 0; b0 < P.B; b0 += kMaxBatch) {
-    const int nb = std::min(kMaxBatch, P.B - b0);
-    st = bf16 ? run_global_rows<__nv_bfloat16>(P, b0, nb) : run_global_rows<float>(P, b0, nb);
-    if (st != LF_OK) return st;
-  }
-  return LF_OK;
+  return bf16 ? forward_t<__nv_bfloat16>(P, true) : forward_t<float>(P, false);
 }
 
 }  // namespace lf
