@@ -142,6 +142,7 @@ global_partial_kernel(const __grid_constant__ PatternParams p, const T* __restri
 #pragma unroll
         for (int g = 0; g < kGQ; ++g) {
           const float w = sc[g][t];
+          if (w == 0.f) continue;  // an unattended key's value never enters the sum
 #pragma unroll
           for (int u = 0; u < 4; ++u) acc[g][u] = fmaf(w, vv[u], acc[g][u]);
         }
@@ -164,8 +165,7 @@ global_partial_kernel(const __grid_constant__ PatternParams p, const T* __restri
       const float mo = run_m[g], ms = sub_m[g];
       const float mn = fmaxf(mo, ms);
       const float fo = (mo == NEG_INF) ? 0.f : ex2_approx(mo - mn);
-      const float fs = (ms == NEG_INF) ? 0.f : ex2_approx(ms - mn);
-      run_acc[g][c] = run_acc[g][c] * fo + a * fs;
+      if (ms != NEG_INF) run_acc[g][c] = run_acc[g][c] * fo + a * ex2_approx(ms - mn);
     }
     __syncthreads();
     if (tid < kGQ) {
@@ -389,7 +389,8 @@ global_merge_kernel(const __grid_constant__ PatternParams p, const float* __rest
     for (int ch = 0; ch < nchunks; ++ch) {
       const float* e = base + ch * cstride;
       const float me = e[0];
-      const float f = (me == NEG_INF) ? 0.f : ex2_approx(me - M);
+      if (me == NEG_INF) continue;  // nothing attended in this chunk: skip, never scale by 0
+      const float f = ex2_approx(me - M);
       l = fmaf(e[1], f, l);
       a = fmaf(e[2 + c], f, a);
     }
