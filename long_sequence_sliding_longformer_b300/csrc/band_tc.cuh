@@ -8,20 +8,35 @@
 //
 // Dilation is handled by residue classes: with dilation delta, row
 // i = r + delta*m only ever attends rows of the same residue r, and in the
-// coordinate m the window is a plain +-w/2 band.  Each work item is one tile
-// of 128 consecutive m of one (batch, head, residue); a TMA tensor map whose
-// row stride is delta rows gives the tile and its key tiles directly.
+// coordinate m the window is a plain band of half steps back and `right`
+// steps ahead.  A TMA tensor map whose row stride is delta rows presents a
+// residue class as a dense matrix.
 //
-// Per CTA (one per SM, persistent over work items), 6 warps:
-//   warp 0     producer: TMA loads of Q and of the K/V tiles that intersect
-//              the item's window into a ring of shared-memory stages, and a
-//              gather of the global tokens' K/V rows for the global-column tile
-//   warp 1     allocates TMEM; lane 0 issues tcgen05.mma:
-//              S = Q K^T into one of two TMEM score buffers, O += P V into TMEM
-//   warps 2-5  one query row per thread: read S from TMEM, apply the window,
-//              padding and global-column masks, fp32 online softmax (exp2),
-//              write P (bf16) to shared memory, rescale O in TMEM when the
-//              running maximum grows, and finally normalise O and store it.
+// Work item: two consecutive 128-row query tiles X = 0, 1 (256 rows of m) of
+// one (batch, head, residue).  Their key tiles overlap, so the item streams
+// the union of the two windows once (128-key "entries", then the gathered
+// global-token keys) and both tiles consume the shared entries.
+//
+// One CTA per SM, persistent over items, 10 warps:
+//   warps 0-3  softmax of tile 0, warps 4-7 softmax of tile 1: one query row
+//              per thread; S rows are read from TMEM, masked, turned into
+//              P = exp2(S*scale - m) with a lazily updated row maximum, and P
+//              (bf16) is written back to TMEM for the P.V product
+//   warp 8     producer: TMA loads of Q and of the K/V entries into two
+//              rings of shared-memory slots; gathers of global-token rows
+//   warp 9     allocates TMEM; lane 0 issues every tcgen05.mma:
+//              S_X = Q_X K^T (both operands in shared memory) and
+//              O_X += P_X V (P from TMEM, V from shared memory)
+// While the softmax warps of one tile work, the tensor cores run the other
+// tile's products (ping-pong), so the exponentials and the MMAs overlap.
+//
+// TMEM: S_0, S_1 (128 columns each) and O_0, O_1 (D columns each).  P_X
+// (two bf16 per column) overwrites the first 64 columns of S_X once the row
+// has been read, chunk by chunk, so no register array holds all of P; the MMA
+// of the next entry's S_X is issued after the P.V that reads P_X (the tensor
+// core executes one thread's MMAs in order).  The completion of S_X(j+1)
+// therefore also tells the softmax that P_X(j).V is done and O_X is stable.
+//
 // Every wait is bounded; a timeout sets the device error word and all roles
 // leave their loops, drain their in-flight copies and free TMEM.
 #pragma once
@@ -32,29 +47,53 @@ namespace lf {
 
 template <int D>
 struct BandCfg {
-  static constexpr int kStages = (D == 64) ? 4 : 2;
-  static constexpr int kTile = 128 * D * 2;  // bytes of one [128, D] bf16 tile
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffKV = kTile;       // stage s: K at +2*s*kTile, V at +(2*s+1)*kTile
-  static constexpr int kOffP = kOffKV + kStages * 2 * kTile;
-  static constexpr int kOffGcol = kOffP + 128 * 128 * 2;  // per stage: gpos[128], gm[128]
-  static constexpr int kOffBar = kOffGcol + kStages * 2 * 128 * 4;
-  // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], s_empty[2], p_full, pv_done, o_empty, fin
-  static constexpr int kNumBar = 2 + 2 * kStages + 4 + 4;
+  static constexpr int kQBuf = (D == 64) ? 2 : 1;
+  static constexpr int kKSt = (D == 64) ? 4 : 3;
+  static constexpr int kVSt = (D == 64) ? 4 : 2;
+  static constexpr int kTile = 128 * D * 2;     // bytes of one [128, D] bf16 tile
+  static constexpr int kOffQ = 0;               // Q[qb][X] at kOffQ + (2*qb + X) * kTile
+  static constexpr int kOffK = kQBuf * 2 * kTile;
+  static constexpr int kOffV = kOffK + kKSt * kTile;
+  static constexpr int kOffBar = kOffV + kVSt * kTile;
+  // q_full[2], q_empty[2], k_full[4], k_empty[4], v_full[4], v_empty[4], v_land,
+  // s_full[2], (unused)[2], p_full[2], pv_done[2], o_empty[2], fin
+  static constexpr int kNumBar = 2 + 2 + 4 + 4 + 4 + 4 + 1 + 2 + 2 + 2 + 2 + 2 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBar * 8;
   static constexpr int kSmem = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
-  static constexpr int kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256, 256+D)
-  static constexpr int kOCol = 256;
+  static constexpr int kTmemCols = 512;
+  static constexpr uint32_t kColS = 0;     // S_X (and P_X) at 128*X
+  static constexpr uint32_t kColO = 256;   // O_X at 256 + D*X
 };
 
-struct ItemInfo {
-  int b, h, r, delta, n_r, set, m0, Lb, Lm, kstart, kend, nb, ngt;
-  int i_last;  // position of the tile's last valid query row
-  bool zero;
+// Everything the roles need to know about one work item.  Computed the same
+// way by every role from the item number alone.
+struct PairItem {
+  int b, h, r, delta, n_r, set, m0, Lb, Lm, bh;
+  bool zero;        // no valid row in the pair: output zeros only
+  int act[2];       // tile X has at least one valid row
+  int U0, nU, nE;   // first key (m coordinate) of the band entries, their count, all entries
+  int khi;          // last key any row of the pair attends in the band
+  int b0[2], nb[2]; // band entries of tile X: [b0, b0 + nb)
+  int klo[2], kend[2]; // first and last key (m coordinate) tile X attends in the band
+  int gcnt[2];      // global tokens visible to tile X (a prefix of the sorted list)
+  int ngt[2];       // global entries of tile X
+  int gbase[2];     // first global entry of tile X
+  int len[2];       // entries tile X consumes
+  bool gsplit;      // causal: each tile has global entries of its own
 };
 
-__device__ __forceinline__ ItemInfo decode_item(const BandParams& p, int item) {
-  ItemInfo it;
+__device__ __forceinline__ int upper_bound_gidx(const BandParams& p, int lim) {
+  // number of global positions <= lim (gidx is strictly increasing)
+  int lo = 0, hi = p.G;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (p.gidx[mid] <= lim) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ PairItem decode_pair(const BandParams& p, int item) {
+  PairItem it;
   it.b = item / p.items_per_b;
   const int rem = item - it.b * p.items_per_b;
   int lo = 0, hi = p.nseg - 1;
@@ -62,28 +101,104 @@ __device__ __forceinline__ ItemInfo decode_item(const BandParams& p, int item) {
     const int mid = (lo + hi + 1) >> 1;
     if (p.seg[mid].begin <= rem) lo = mid; else hi = mid - 1;
   }
-  it.h = p.seg[lo].h;
-  it.r = p.seg[lo].r;
-  it.delta = p.seg[lo].delta;
-  it.n_r = p.seg[lo].n_r;
-  it.set = p.seg[lo].set;
-  it.m0 = (rem - p.seg[lo].begin) * 128;
+  const BandSeg& sg = p.seg[lo];
+  it.h = sg.h;
+  it.r = sg.r;
+  it.delta = sg.delta;
+  it.n_r = sg.n_r;
+  it.set = sg.set;
+  it.m0 = (rem - sg.begin) * 256;
+  it.bh = it.b * p.H + it.h;
   it.Lb = p.n - p.pad[it.b];
   const int Lm = (it.Lb > it.r) ? (it.Lb - it.r + it.delta - 1) / it.delta : 0;
   it.Lm = min(Lm, it.n_r);
-  it.zero = it.m0 >= it.Lm;
-  it.kstart = max(0, it.m0 - p.half);
-  const int lastq = min(it.m0 + 127, it.Lm - 1);
-  it.kend = min(it.Lm - 1, lastq + p.right);  // last key any row of the tile attends
-  it.i_last = it.r + it.delta * lastq;
-  it.nb = it.zero ? 0 : (it.kend - it.kstart) / 128 + 1;
-  it.ngt = it.zero ? 0 : (p.G + 127) / 128;
+#pragma unroll
+  for (int X = 0; X < 2; ++X) {
+    const int q0 = it.m0 + 128 * X;
+    it.act[X] = q0 < it.Lm;
+    const int qlast = min(q0 + 127, it.Lm - 1);
+    it.klo[X] = max(0, q0 - p.half);
+    it.kend[X] = min(it.Lm - 1, qlast + p.right);
+    int glim = it.Lb - 1;
+    if (p.causal) glim = min(glim, it.r + it.delta * qlast);
+    it.gcnt[X] = (it.act[X] && p.G > 0) ? upper_bound_gidx(p, glim) : 0;
+    it.ngt[X] = (it.gcnt[X] + 127) >> 7;
+  }
+  it.zero = !it.act[0];
+  if (it.zero) {
+    it.nE = it.nU = 0;
+    it.len[0] = it.len[1] = 0;
+    return it;
+  }
+  it.U0 = it.klo[0];
+  it.khi = it.act[1] ? it.kend[1] : it.kend[0];
+  it.nU = (it.khi - it.U0) / 128 + 1;
+#pragma unroll
+  for (int X = 0; X < 2; ++X) {
+    if (it.act[X]) {
+      it.b0[X] = (it.klo[X] - it.U0) / 128;
+      it.nb[X] = (it.kend[X] - it.U0) / 128 - it.b0[X] + 1;
+    } else {
+      it.b0[X] = 0;
+      it.nb[X] = 0;
+    }
+    it.len[X] = it.nb[X] + it.ngt[X];
+  }
+  // global entries: shared by both tiles unless causal (then each tile sees its own prefix)
+  it.gbase[0] = it.nU;
+  it.gsplit = p.causal != 0;
+  if (it.gsplit) {
+    it.gbase[1] = it.nU + it.ngt[0];
+    it.nE = it.nU + it.ngt[0] + it.ngt[1];
+  } else {
+    it.gbase[1] = it.nU;
+    it.nE = it.nU + max(it.ngt[0], it.ngt[1]);
+  }
   return it;
 }
 
-// keys of global tile gt: ranks [128*gt, 128*gt + cnt), padded to a multiple of 16
-__device__ __forceinline__ int global_tile_count(const BandParams& p, int gt) {
-  return min(128, p.G - gt * 128);
+// entry consumed by tile X at its step j
+__device__ __forceinline__ int entry_of(const PairItem& it, int X, int j) {
+  const int nb = X ? it.nb[1] : it.nb[0];
+  return j < nb ? (X ? it.b0[1] : it.b0[0]) + j : (X ? it.gbase[1] : it.gbase[0]) + (j - nb);
+}
+
+// step at which tile Y consumes entry e, or -1
+__device__ __forceinline__ int step_of(const PairItem& it, int Y, int e) {
+  if (!(Y ? it.act[1] : it.act[0])) return -1;
+  const int nb = Y ? it.nb[1] : it.nb[0];
+  if (e < it.nU) {
+    const int j = e - (Y ? it.b0[1] : it.b0[0]);
+    return (j >= 0 && j < nb) ? j : -1;
+  }
+  const int g = e - (Y ? it.gbase[1] : it.gbase[0]);
+  return (g >= 0 && g < (Y ? it.ngt[1] : it.ngt[0])) ? nb + g : -1;
+}
+
+// The MMAs of an item are issued in the order of (step, tile); the entry may
+// be released after the product of its last consumer in that order.
+__device__ __forceinline__ bool last_consumer(const PairItem& it, int X, int j) {
+  const int jy = step_of(it, 1 - X, entry_of(it, X, j));
+  return jy < 0 || j > jy || (j == jy && X == 1);
+}
+
+// global entry e (>= nU): the tile whose visible set it holds, and its tile index
+__device__ __forceinline__ void global_entry(const PairItem& it, int e, int& X, int& gt) {
+  if (!it.gsplit || e < it.gbase[0] + it.ngt[0]) {
+    X = 0;
+    gt = e - it.gbase[0];
+  } else {
+    X = 1;
+    gt = e - it.gbase[1];
+  }
+}
+
+// a[X] for a two-element member array without dynamic indexing (which would
+// send the whole item descriptor to local memory)
+__device__ __forceinline__ int pick(const int (&a)[2], int X) { return X ? a[1] : a[0]; }
+
+__device__ __forceinline__ int global_count(const PairItem& it, int X, int gt) {
+  return min(128, pick(it.gcnt, X) - 128 * gt);
 }
 
 template <int D>
@@ -91,26 +206,24 @@ struct BandSmem {
   using C = BandCfg<D>;
   uint8_t* base;
   uint32_t sbase;
-  __device__ __forceinline__ uint32_t q() const { return sbase + C::kOffQ; }
-  __device__ __forceinline__ uint32_t k(int s) const { return sbase + C::kOffKV + 2 * s * C::kTile; }
-  __device__ __forceinline__ uint32_t v(int s) const { return sbase + C::kOffKV + (2 * s + 1) * C::kTile; }
-  __device__ __forceinline__ uint8_t* k_ptr(int s) const { return base + C::kOffKV + 2 * s * C::kTile; }
-  __device__ __forceinline__ uint8_t* v_ptr(int s) const { return base + C::kOffKV + (2 * s + 1) * C::kTile; }
-  __device__ __forceinline__ uint32_t pbuf() const { return sbase + C::kOffP; }
-  __device__ __forceinline__ uint8_t* p_ptr() const { return base + C::kOffP; }
-  __device__ __forceinline__ int* gpos(int s) const { return reinterpret_cast<int*>(base + C::kOffGcol + s * 1024); }
-  __device__ __forceinline__ int* gm(int s) const { return gpos(s) + 128; }
+  __device__ __forceinline__ uint32_t q(int qb, int X) const { return sbase + C::kOffQ + (2 * qb + X) * C::kTile; }
+  __device__ __forceinline__ uint32_t k(int s) const { return sbase + C::kOffK + s * C::kTile; }
+  __device__ __forceinline__ uint32_t v(int s) const { return sbase + C::kOffV + s * C::kTile; }
+  __device__ __forceinline__ uint8_t* k_ptr(int s) const { return base + C::kOffK + s * C::kTile; }
+  __device__ __forceinline__ uint8_t* v_ptr(int s) const { return base + C::kOffV + s * C::kTile; }
   __device__ __forceinline__ uint32_t bar(int i) const { return sbase + C::kOffBar + 8 * i; }
-  __device__ __forceinline__ uint32_t q_full() const { return bar(0); }
-  __device__ __forceinline__ uint32_t q_empty() const { return bar(1); }
-  __device__ __forceinline__ uint32_t kv_full(int s) const { return bar(2 + s); }
-  __device__ __forceinline__ uint32_t kv_empty(int s) const { return bar(2 + C::kStages + s); }
-  __device__ __forceinline__ uint32_t s_full(int b) const { return bar(2 + 2 * C::kStages + b); }
-  __device__ __forceinline__ uint32_t s_empty(int b) const { return bar(4 + 2 * C::kStages + b); }
-  __device__ __forceinline__ uint32_t p_full() const { return bar(6 + 2 * C::kStages); }
-  __device__ __forceinline__ uint32_t pv_done() const { return bar(7 + 2 * C::kStages); }
-  __device__ __forceinline__ uint32_t o_empty() const { return bar(8 + 2 * C::kStages); }
-  __device__ __forceinline__ uint32_t fin() const { return bar(9 + 2 * C::kStages); }
+  __device__ __forceinline__ uint32_t q_full(int b) const { return bar(0 + b); }
+  __device__ __forceinline__ uint32_t q_empty(int b) const { return bar(2 + b); }
+  __device__ __forceinline__ uint32_t k_full(int s) const { return bar(4 + s); }
+  __device__ __forceinline__ uint32_t k_empty(int s) const { return bar(8 + s); }
+  __device__ __forceinline__ uint32_t v_full(int s) const { return bar(12 + s); }
+  __device__ __forceinline__ uint32_t v_empty(int s) const { return bar(16 + s); }
+  __device__ __forceinline__ uint32_t v_land() const { return bar(20); }
+  __device__ __forceinline__ uint32_t s_full(int X) const { return bar(21 + X); }
+  __device__ __forceinline__ uint32_t p_full(int X) const { return bar(25 + X); }
+  __device__ __forceinline__ uint32_t pv_done(int X) const { return bar(27 + X); }
+  __device__ __forceinline__ uint32_t o_empty(int X) const { return bar(29 + X); }
+  __device__ __forceinline__ uint32_t fin() const { return bar(31); }
   __device__ __forceinline__ uint32_t* tmem_holder() const { return reinterpret_cast<uint32_t*>(base + C::kOffMisc); }
   __device__ __forceinline__ volatile int* abort_flag() const { return reinterpret_cast<volatile int*>(base + C::kOffMisc + 4); }
 };
@@ -121,106 +234,153 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int ch) {
   return (uint32_t)((ch >> 3) * 16384 + row * 128 + (((ch & 7) ^ (row & 7)) << 4));
 }
 
+// m coordinate of global position g in residue class r, or a value that is
+// never inside a band when g is not in the class
+__device__ __forceinline__ int residue_coord(int g, int r, int delta) {
+  if (delta == 1) return g;
+  const int d = g - r;
+  return (d >= 0 && d % delta == 0) ? d / delta : -(1 << 29);
+}
+
 // ------------------------------------------------------------------ producer
 template <int D>
 __device__ void band_producer(const BandParams& p, const BandSmem<D>& sm, int lane) {
   using C = BandCfg<D>;
   volatile int* abort = sm.abort_flag();
-  uint32_t kv_it = 0, q_it = 0;
-  int last_fill[C::kStages];
+  uint32_t kv = 0, q_it = 0, land = 0;
+  int land_pending = -1;  // v_land phase of a zeroing load not yet seen to land
+  int last_k[C::kKSt], last_v[C::kVSt], last_q[C::kQBuf];
 #pragma unroll
-  for (int s = 0; s < C::kStages; ++s) last_fill[s] = -1;
-  int last_q = -1;
+  for (int s = 0; s < C::kKSt; ++s) last_k[s] = -1;
+#pragma unroll
+  for (int s = 0; s < C::kVSt; ++s) last_v[s] = -1;
+#pragma unroll
+  for (int s = 0; s < C::kQBuf; ++s) last_q[s] = -1;
   bool ok = true;
 
   for (int item = blockIdx.x; ok && item < p.total_items; item += gridDim.x) {
-    const ItemInfo it = decode_item(p, item);
+    const PairItem it = decode_pair(p, item);
     if (it.zero) continue;
-    const int bh = it.b * p.H + it.h;
 
-    if (!warp_wait(sm.q_empty(), (q_it & 1) ^ 1, abort, kRoleProducer)) { ok = false; break; }
+    // ---- Q of both tiles
+    const int qb = q_it % C::kQBuf;
+    if (!warp_wait(sm.q_empty(qb), ((q_it / C::kQBuf) & 1) ^ 1, abort, kRoleProducer)) { ok = false; break; }
     if (lane == 0) {
-      mbar_arrive_expect_tx(sm.q_full(), C::kTile);
+      mbar_arrive_expect_tx(sm.q_full(qb), (it.act[1] ? 2 : 1) * C::kTile);
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_3d(sm.q() + c * 16384, &p.tq[it.set], c * 64, it.m0, bh, sm.q_full());
+      for (int X = 0; X < 2; ++X) {
+        if (!it.act[X]) continue;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sm.q(qb, X) + c * 16384, &p.tq[it.set], c * 64, it.m0 + 128 * X, it.bh, sm.q_full(qb));
+      }
     }
-    last_q = (int)q_it;
+    last_q[qb] = (int)q_it;
     ++q_it;
 
-    for (int j = 0; j < it.nb; ++j, ++kv_it) {
-      const int s = kv_it % C::kStages;
-      const uint32_t ph = (kv_it / C::kStages) & 1;
-      if (!warp_wait(sm.kv_empty(s), ph ^ 1, abort, kRoleProducer)) { ok = false; break; }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(sm.kv_full(s), 2 * C::kTile);
-        const int y = it.kstart + 128 * j;
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_3d(sm.k(s) + c * 16384, &p.tk[it.set], c * 64, y, bh, sm.kv_full(s));
-          tma_load_3d(sm.v(s) + c * 16384, &p.tv[it.set], c * 64, y, bh, sm.kv_full(s));
-        }
-      }
-      last_fill[s] = (int)kv_it;
-    }
-    if (!ok) break;
+    const __nv_bfloat16* kb = p.k + (size_t)it.bh * p.n * D;
+    const __nv_bfloat16* vb = p.v + (size_t)it.bh * p.n * D;
+    constexpr int CH = D / 8;  // 16-byte chunks per row
 
-    for (int gt = 0; gt < it.ngt; ++gt, ++kv_it) {
-      const int s = kv_it % C::kStages;
-      const uint32_t ph = (kv_it / C::kStages) & 1;
-      if (!warp_wait(sm.kv_empty(s), ph ^ 1, abort, kRoleProducer)) { ok = false; break; }
-      const int g0 = gt * 128;
-      const int cnt = global_tile_count(p, gt);
-      const int ng = (cnt + 15) & ~15;
-      int* gpos = sm.gpos(s);
-      int* gm = sm.gm(s);
-      // a global key no row of this tile may attend (padding, or after the
-      // tile's last row when causal) is stored as zeros
-      const int g_lim = p.causal ? min(it.Lb - 1, it.i_last) : it.Lb - 1;
-      for (int c = lane; c < 128; c += 32) {
-        const int g = (c < cnt) ? p.gidx[g0 + c] : -1;
-        const bool valid = (c < cnt) && g <= g_lim;
-        gpos[c] = valid ? g : -1;
-        int mg = -(1 << 29);  // "not in this residue class": never inside the band
-        if (valid && (g - it.r) % it.delta == 0) mg = (g - it.r) / it.delta;
-        gm[c] = mg;
-      }
-      const __nv_bfloat16* kb = p.k + (size_t)bh * p.n * D;
-      const __nv_bfloat16* vb = p.v + (size_t)bh * p.n * D;
-      constexpr int CH = D / 8;  // 16-byte chunks per row
-      uint8_t* ks = sm.k_ptr(s);
-      uint8_t* vs = sm.v_ptr(s);
-      for (int idx = lane; idx < ng * CH; idx += 32) {
-        const int row = idx / CH, ch = idx - (idx / CH) * CH;
-        uint4 kx = make_uint4(0, 0, 0, 0), vx = make_uint4(0, 0, 0, 0);
-        if (row < cnt) {
-          const int g = p.gidx[g0 + row];
-          if (g <= g_lim) {
-            kx = __ldg(reinterpret_cast<const uint4*>(kb + (size_t)g * D) + ch);
-            vx = __ldg(reinterpret_cast<const uint4*>(vb + (size_t)g * D) + ch);
-          }
+    for (int e = 0; e < it.nE; ++e, ++kv) {
+      const int ks = kv % C::kKSt, vs = kv % C::kVSt;
+      // ---------------- K
+      if (!warp_wait(sm.k_empty(ks), ((kv / C::kKSt) & 1) ^ 1, abort, kRoleProducer)) { ok = false; break; }
+      if (e < it.nU) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(sm.k_full(ks), C::kTile);
+          const int y = it.U0 + 128 * e;
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(sm.k(ks) + c * 16384, &p.tk[it.set], c * 64, y, it.bh, sm.k_full(ks));
         }
-        const uint32_t off = sw128_offset(row, ch);
-        *reinterpret_cast<uint4*>(ks + off) = kx;
-        *reinterpret_cast<uint4*>(vs + off) = vx;
+        last_k[ks] = (int)kv;
+      } else {
+        int X, gt;
+        global_entry(it, e, X, gt);
+        const int cnt = global_count(it, X, gt);
+        const int ng = (cnt + 15) & ~15;
+        uint8_t* dst = sm.k_ptr(ks);
+        for (int idx = lane; idx < ng * CH; idx += 32) {
+          const int row = idx / CH, ch = idx - (idx / CH) * CH;
+          uint4 x = make_uint4(0, 0, 0, 0);
+          if (row < cnt) x = __ldg(reinterpret_cast<const uint4*>(kb + (size_t)p.gidx[128 * gt + row] * D) + ch);
+          *reinterpret_cast<uint4*>(dst + sw128_offset(row, ch)) = x;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.k_full(ks));
+        last_k[ks] = -1;  // completed synchronously
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sm.kv_full(s));
-      last_fill[s] = -1;  // completed synchronously
+      // ---------------- V
+      if (!warp_wait(sm.v_empty(vs), ((kv / C::kVSt) & 1) ^ 1, abort, kRoleProducer)) { ok = false; break; }
+      if (e < it.nU) {
+        const int y = it.U0 + 128 * e;
+        // rows past the last key any row of the pair attends (padding, or the
+        // end of the window union) but inside the tensor are zeroed, so that
+        // whatever they hold cannot reach the output through 0 * value
+        const int z0 = it.khi - y + 1, z1 = min(128, it.n_r - y);
+        if (z0 < z1) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(sm.v_land(), C::kTile);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_3d(sm.v(vs) + c * 16384, &p.tv[it.set], c * 64, y, it.bh, sm.v_land());
+          }
+          land_pending = (int)land;
+          const bool landed = warp_wait(sm.v_land(), land & 1, abort, kRoleProducer);
+          ++land;
+          if (!landed) { ok = false; break; }
+          land_pending = -1;
+          uint8_t* dst = sm.v_ptr(vs);
+          for (int idx = lane; idx < (z1 - z0) * CH; idx += 32) {
+            const int row = z0 + idx / CH, ch = idx - (idx / CH) * CH;
+            *reinterpret_cast<uint4*>(dst + sw128_offset(row, ch)) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sm.v_full(vs));
+          last_v[vs] = -1;
+        } else {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(sm.v_full(vs), C::kTile);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_3d(sm.v(vs) + c * 16384, &p.tv[it.set], c * 64, y, it.bh, sm.v_full(vs));
+          }
+          last_v[vs] = (int)kv;
+        }
+      } else {
+        int X, gt;
+        global_entry(it, e, X, gt);
+        const int cnt = global_count(it, X, gt);
+        const int ng = (cnt + 15) & ~15;
+        uint8_t* dst = sm.v_ptr(vs);
+        for (int idx = lane; idx < ng * CH; idx += 32) {
+          const int row = idx / CH, ch = idx - (idx / CH) * CH;
+          uint4 x = make_uint4(0, 0, 0, 0);
+          if (row < cnt) x = __ldg(reinterpret_cast<const uint4*>(vb + (size_t)p.gidx[128 * gt + row] * D) + ch);
+          *reinterpret_cast<uint4*>(dst + sw128_offset(row, ch)) = x;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.v_full(vs));
+        last_v[vs] = -1;
+      }
     }
   }
   // Let every TMA copy this warp issued land before the CTA can exit.
+  int dummy = 0;
 #pragma unroll
-  for (int s = 0; s < C::kStages; ++s)
-    if (last_fill[s] >= 0) {
-      int dummy = 0;
-      mbar_wait(sm.kv_full(s), ((uint32_t)last_fill[s] / C::kStages) & 1, &dummy, kRoleDrain, 200000000ull);
-    }
-  if (last_q >= 0) {
-    int dummy = 0;
-    mbar_wait(sm.q_full(), (uint32_t)last_q & 1, &dummy, kRoleDrain, 200000000ull);
-  }
+  for (int s = 0; s < C::kKSt; ++s)
+    if (last_k[s] >= 0) mbar_wait(sm.k_full(s), ((uint32_t)last_k[s] / C::kKSt) & 1, &dummy, kRoleDrain, 200000000ull);
+#pragma unroll
+  for (int s = 0; s < C::kVSt; ++s)
+    if (last_v[s] >= 0) mbar_wait(sm.v_full(s), ((uint32_t)last_v[s] / C::kVSt) & 1, &dummy, kRoleDrain, 200000000ull);
+#pragma unroll
+  for (int s = 0; s < C::kQBuf; ++s)
+    if (last_q[s] >= 0) mbar_wait(sm.q_full(s), ((uint32_t)last_q[s] / C::kQBuf) & 1, &dummy, kRoleDrain, 200000000ull);
+  if (land_pending >= 0) mbar_wait(sm.v_land(), (uint32_t)land_pending & 1, &dummy, kRoleDrain, 200000000ull);
 }
 
 // ------------------------------------------------------------------ MMA issuer (one thread)
@@ -228,68 +388,95 @@ template <int D>
 __device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tmem) {
   using C = BandCfg<D>;
   volatile int* abort = sm.abort_flag();
-  const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0);
   const uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
-  uint32_t kv_it = 0, q_it = 0, s_it = 0, pf_it = 0, o_it = 0;
+  uint32_t kv = 0, q_it = 0;
+  uint32_t p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
   bool ok = true;
 
   for (int item = blockIdx.x; ok && item < p.total_items; item += gridDim.x) {
-    const ItemInfo it = decode_item(p, item);
+    const PairItem it = decode_pair(p, item);
     if (it.zero) continue;
-    const int J = it.nb + it.ngt;
-    if (!mbar_wait(sm.q_full(), q_it & 1, abort, kRoleMma)) { ok = false; break; }
+    const int qb = q_it % C::kQBuf;
+    if (!mbar_wait(sm.q_full(qb), (q_it / C::kQBuf) & 1, abort, kRoleMma)) { ok = false; break; }
     ++q_it;
     tc_fence_after();
+    const int s_total = it.len[0] + it.len[1];
+    int s_done = 0;
 
-    auto issue_s = [&](int j) -> bool {
-      const uint32_t kvj = kv_it + j;
-      const int s = kvj % C::kStages;
-      if (!mbar_wait(sm.kv_full(s), (kvj / C::kStages) & 1, abort, kRoleMma)) return false;
-      const int sb = s_it & 1;
-      if (!mbar_wait(sm.s_empty(sb), ((s_it >> 1) & 1) ^ 1, abort, kRoleMma)) return false;
+    // columns of the entry (128 for band entries, the padded global count otherwise)
+    auto ncols = [&](int X, int e) -> int {
+      if (e < it.nU) return 128;
+      int Xg, gt;
+      global_entry(it, e, Xg, gt);
+      return (global_count(it, Xg, gt) + 15) & ~15;
+    };
+
+    auto issue_s = [&](int X, int j) -> bool {
+      const int e = entry_of(it, X, j);
+      const uint32_t ke = kv + e;
+      const int ks = ke % C::kKSt;
+      if (!mbar_wait(sm.k_full(ks), (ke / C::kKSt) & 1, abort, kRoleMma)) return false;
       tc_fence_after();
-      int N = 128;
-      if (j >= it.nb) N = (global_tile_count(p, j - it.nb) + 15) & ~15;
-      const uint32_t idesc = (N == 128) ? idesc_s : idesc_bf16_f32(128, N, 0);
-      const uint32_t dt = tmem + sb * 128;
+      const int N = ncols(X, e);
+      const uint32_t idesc = idesc_bf16_f32(128, N, 0);
+      const uint32_t dt = tmem + C::kColS + 128 * X;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t qa = sm.q() + (kk >> 2) * 16384 + (kk & 3) * 32;
-        const uint32_t ka = sm.k(s) + (kk >> 2) * 16384 + (kk & 3) * 32;
+        const uint32_t qa = sm.q(qb, X) + (kk >> 2) * 16384 + (kk & 3) * 32;
+        const uint32_t ka = sm.k(ks) + (kk >> 2) * 16384 + (kk & 3) * 32;
         mma_bf16_ss(dt, smem_desc_sw128(qa, 16, 1024), smem_desc_sw128(ka, 16, 1024), idesc, kk > 0);
       }
-      mma_commit(sm.s_full(sb));
-      ++s_it;
+      mma_commit(sm.s_full(X));
+      if (last_consumer(it, X, j)) mma_commit(sm.k_empty(ks));
+      if (++s_done == s_total) mma_commit(sm.q_empty(qb));  // Q may be replaced
       return true;
     };
 
-    if (!issue_s(0)) { ok = false; break; }
-    for (int j = 0; j < J; ++j) {
-      if (j + 1 < J) {
-        if (!issue_s(j + 1)) { ok = false; break; }
-      } else {
-        mma_commit(sm.q_empty());  // Q may be replaced once every S of this item is done
-      }
-      if (!mbar_wait(sm.p_full(), pf_it & 1, abort, kRoleMma)) { ok = false; break; }
-      ++pf_it;
+    auto issue_pv = [&](int X, int j) -> bool {
+      const int e = entry_of(it, X, j);
+      const uint32_t ve = kv + e;
+      const int vs = ve % C::kVSt;
+      if (!mbar_wait(sm.v_full(vs), (ve / C::kVSt) & 1, abort, kRoleMma)) return false;
+      if (!mbar_wait(sm.p_full(X), p_cnt[X] & 1, abort, kRoleMma)) return false;
+      ++p_cnt[X];
       if (j == 0) {
-        if (!mbar_wait(sm.o_empty(), (o_it & 1) ^ 1, abort, kRoleMma)) { ok = false; break; }
-        ++o_it;
+        if (!mbar_wait(sm.o_empty(X), (o_cnt[X] & 1) ^ 1, abort, kRoleMma)) return false;
+        ++o_cnt[X];
       }
       tc_fence_after();
-      const int s = (kv_it + j) % C::kStages;
-      int K = 128;
-      if (j >= it.nb) K = (global_tile_count(p, j - it.nb) + 15) & ~15;
-      for (int kk = 0; kk < K / 16; ++kk) {
-        const uint32_t pa = sm.pbuf() + (kk >> 2) * 16384 + (kk & 3) * 32;
-        const uint32_t va = sm.v(s) + kk * 2048;
-        mma_bf16_ss(tmem + C::kOCol, smem_desc_sw128(pa, 16, 1024), smem_desc_sw128(va, 16384, 1024),
-                    idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+      // key steps of 16 that some row of tile X attends: value rows outside
+      // them (the partner tile's keys) are never read
+      int kk0 = 0, kk1 = ncols(X, e) / 16 - 1;
+      if (e < it.nU) {
+        const int kb = it.U0 + 128 * e;
+        kk0 = max(0, pick(it.klo, X) - kb) >> 4;
+        kk1 = min(127, pick(it.kend, X) - kb) >> 4;
       }
-      mma_commit(sm.kv_empty(s));
-      mma_commit(sm.pv_done());
+      const uint32_t pt = tmem + C::kColS + 128 * X;
+      const uint32_t ot = tmem + C::kColO + D * X;
+      for (int kk = kk0; kk <= kk1; ++kk) {
+        const uint32_t va = sm.v(vs) + kk * 2048;
+        mma_bf16_ts(ot, pt + kk * 8, smem_desc_sw128(va, 16384, 1024), idesc_pv, (j > 0 || kk > kk0) ? 1u : 0u);
+      }
+      if (j + 1 == pick(it.len, X)) mma_commit(sm.pv_done(X));  // O_X complete
+      if (last_consumer(it, X, j)) mma_commit(sm.v_empty(vs));
+      return true;
+    };
+
+#pragma unroll
+    for (int X = 0; X < 2; ++X)
+      if (ok && pick(it.len, X) > 0 && !issue_s(X, 0)) ok = false;
+    const int steps = max(it.len[0], it.len[1]);
+    for (int j = 0; ok && j < steps; ++j) {
+#pragma unroll
+      for (int X = 0; X < 2; ++X) {
+        const int lenX = pick(it.len, X);
+        if (!ok || j >= lenX) continue;
+        if (!issue_pv(X, j)) ok = false;
+        else if (j + 1 < lenX && !issue_s(X, j + 1)) ok = false;
+      }
     }
-    kv_it += J;
+    kv += it.nE;
   }
   // Wait until every MMA this thread issued has finished before TMEM is freed.
   mma_commit(sm.fin());
@@ -298,187 +485,213 @@ __device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tm
 }
 
 // ------------------------------------------------------------------ softmax / epilogue
-template <int D>
-__device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_t tmem, int warp,
+// Lazy rescaling: the running maximum of a row is raised only when a new
+// score exceeds it by more than kLazy in the exp2 domain, so that O is
+// rescaled rarely; P values stay below 2^kLazy.
+constexpr float kLazy = 8.0f;
+
+// Softmax of tile X (one query row per thread; warp quarter wq of TMEM lanes).
+template <int D, int X>
+__device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_t tmem, int wq,
                              int lane) {
   using C = BandCfg<D>;
   volatile int* abort = sm.abort_flag();
-  const int wq = warp & 3;  // TMEM lane quarter this warp may access
   const int row = wq * 32 + lane;
   const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+  const uint32_t tS = tmem + lane_base + C::kColS + 128 * X;  // S_X, then P_X
+  const uint32_t tO = tmem + lane_base + C::kColO + D * X;
   const float NEG_INF = -__int_as_float(0x7f800000);
-  uint32_t kv_it = 0, s_it = 0, pv_it = 0;
+  const float sl2 = p.sl2;
+  uint32_t s_cnt = 0, pv_cnt = 0;
   bool ok = true;
 
   for (int item = blockIdx.x; ok && item < p.total_items; item += gridDim.x) {
-    const ItemInfo it = decode_item(p, item);
-    const int bh = it.b * p.H + it.h;
-    const int m_q = it.m0 + row;
+    const PairItem it = decode_pair(p, item);
+    const int m_q = it.m0 + 128 * X + row;
     const int i_q = it.r + it.delta * m_q;
     const bool row_exists = m_q < it.n_r;
     const bool row_valid = m_q < it.Lm;
-    uint4* orow = reinterpret_cast<uint4*>(p.out + ((size_t)bh * p.n + (row_exists ? i_q : 0)) * D);
-    if (it.zero) {
+    uint4* orow = reinterpret_cast<uint4*>(p.out + ((size_t)it.bh * p.n + (row_exists ? i_q : 0)) * D);
+    if (it.zero || !it.act[X]) {
       if (row_exists) {
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
       }
       continue;
     }
-    const int J = it.nb + it.ngt;
+    const int len = it.len[X], nb = it.nb[X], b0 = it.b0[X], gb = it.gbase[X];
+    const int nU = it.nU, U0 = it.U0, Lm = it.Lm;
     float m_run = NEG_INF, l_run = 0.f;
 
-    for (int j = 0; j < J; ++j) {
-      const uint32_t kvj = kv_it + j;
-      const int s = kvj % C::kStages;
-      const bool is_band = j < it.nb;
-      const int sb = s_it & 1;
-      if (!warp_wait(sm.s_full(sb), (s_it >> 1) & 1, abort, kRoleSoftmax)) { ok = false; break; }
-      tc_fence_after();
-      float sv[128];
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        float tmp[32];
-        tmem_ld32(tmem + lane_base + sb * 128 + c4 * 32, tmp);
-#pragma unroll
-        for (int t = 0; t < 32; ++t) sv[c4 * 32 + t] = tmp[t];
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sm.s_empty(sb));
-      ++s_it;
-
-      // ---- masks, scaling to the exp2 domain, tile maximum
-      float tmax = NEG_INF;
+    for (int j = 0; j < len; ++j) {
+      const bool is_band = j < nb;
+      const int e = is_band ? b0 + j : gb + (j - nb);
+      // ---- which 32-column chunks this warp needs, and which are fully valid
+      int clo, chi;  // valid columns of this row
+      int gt = 0, gcnt = 0;
       if (is_band) {
-        const int kb = it.kstart + 128 * j;
-        int clo = max(0, m_q - kb - p.half);
-        int chi = min(127, min(m_q - kb + p.right, it.Lm - 1 - kb));
-        if (!row_valid) { clo = 1; chi = 0; }
-        if (clo == 0 && chi == 127) {
+        const int kb = U0 + 128 * e;
+        clo = max(0, m_q - p.half - kb);
+        chi = min(127, min(m_q + p.right, Lm - 1) - kb);
+        if (!row_valid || clo > chi) { clo = 128; chi = -1; }
+      } else {
+        int gx;
+        global_entry(it, e, gx, gt);
+        gcnt = global_count(it, gx, gt);
+        clo = row_valid ? 0 : 128;
+        chi = row_valid ? gcnt - 1 : -1;
+      }
+      const int wlo = __reduce_min_sync(0xffffffffu, clo);
+      const int whi = __reduce_max_sync(0xffffffffu, chi);
+      const int flo = __reduce_max_sync(0xffffffffu, clo);
+      const int fhi = __reduce_min_sync(0xffffffffu, chi);
+      uint32_t on = 0, full = 0;
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            sv[c] *= p.sl2;
-            tmax = fmaxf(tmax, sv[c]);
-          }
-        } else {
+      for (int c = 0; c < 4; ++c) {
+        if (32 * c + 31 >= wlo && 32 * c <= whi) on |= 1u << c;
+        if (is_band && flo <= 32 * c && fhi >= 32 * c + 31) full |= 1u << c;
+      }
+
+      // S_X(j) complete; it was issued after P_X(j-1).V, so that is complete too
+      if (!warp_wait(sm.s_full(X), s_cnt & 1, abort, kRoleSoftmax)) { ok = false; break; }
+      ++s_cnt;
+      tc_fence_after();
+      uint32_t sr[128];
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            sv[c] = (c >= clo && c <= chi) ? sv[c] * p.sl2 : NEG_INF;
-            tmax = fmaxf(tmax, sv[c]);
+      for (int c = 0; c < 4; ++c) tmem_ld32_nw(tS + 32 * c, sr + 32 * c);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) reg_fence32(sr + 32 * c);
+      float* s = reinterpret_cast<float*>(sr);
+
+      // ---- masks
+      if (is_band) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (!(full & (1u << c))) {
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+              const int col = 32 * c + t;
+              s[col] = (col >= clo && col <= chi) ? s[col] : NEG_INF;
+            }
           }
         }
       } else {
-        // global-key columns: wait for the gather (its shared-memory tables)
-        if (!warp_wait(sm.kv_full(s), (kvj / C::kStages) & 1, abort, kRoleSoftmax)) { ok = false; break; }
-        const int* gpos = sm.gpos(s);
-        const int* gmv = sm.gm(s);
+        const int gofs = 128 * gt;
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const int g = gpos[c];
-          const int mg = gmv[c];
-          const bool in_band = (m_q - mg <= p.half) && (mg - m_q <= p.right);
-          const bool keep = row_valid && g >= 0 && (!p.causal || g <= i_q) && !in_band;
-          sv[c] = keep ? sv[c] * p.sl2 : NEG_INF;
-          tmax = fmaxf(tmax, sv[c]);
-        }
-      }
-      const float m_new = fmaxf(m_run, tmax);
-      const float m_use = (m_new == NEG_INF) ? 0.f : m_new;
-      const float alpha = ex2_approx(m_run - m_use);
-
-      uint32_t pk[64];
-      float lsum = 0.f;
+        for (int c = 0; c < 4; ++c) {
+          {
+            // bit t of `keep`: this row attends global column 32c + t (a
+            // global key already in the row's band is counted there, once)
+            uint32_t keep = 0;
+            const int tend = max(0, min(32, gcnt - 32 * c));
+#pragma unroll 1
+            for (int t = 0; t < tend; ++t) {
+              const int g = p.gidx[gofs + 32 * c + t];
+              const int mg = residue_coord(g, it.r, it.delta);
+              const bool in_band = (m_q - mg <= p.half) && (mg - m_q <= p.right);
+              const bool k = row_valid && (!p.causal || g <= i_q) && !in_band;
+              keep |= (uint32_t)k << t;
+            }
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float p0 = ex2_approx(sv[2 * c] - m_use);
-        const float p1 = ex2_approx(sv[2 * c + 1] - m_use);
-        lsum += p0 + p1;
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-        pk[c] = *reinterpret_cast<uint32_t*>(&h2);
-      }
-      l_run = l_run * alpha + lsum;
-
-      // ---- the previous P.V must be done: P buffer free, O stable
-      if (j > 0) {
-        if (!warp_wait(sm.pv_done(), pv_it & 1, abort, kRoleSoftmax)) { ok = false; break; }
-        ++pv_it;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-#pragma unroll
-          for (int c4 = 0; c4 < D / 32; ++c4) {
-            float o[32];
-            tmem_ld32(tmem + lane_base + C::kOCol + c4 * 32, o);
-#pragma unroll
-            for (int t = 0; t < 32; ++t) o[t] *= alpha;
-            tmem_st32(tmem + lane_base + C::kOCol + c4 * 32, o);
+            for (int t = 0; t < 32; ++t) s[32 * c + t] = ((keep >> t) & 1u) ? s[32 * c + t] : NEG_INF;
           }
         }
       }
-      // ---- value rows after the last key any row of the tile attends (the
-      // padding, and keys outside every window of the tile) are zeroed, so
-      // whatever they hold cannot reach the output through 0 * value
-      if (is_band) {
-        const int kb = it.kstart + 128 * j;
-        if (kb + 127 > it.kend) {
-          if (!warp_wait(sm.kv_full(s), (kvj / C::kStages) & 1, abort, kRoleSoftmax)) { ok = false; break; }
-          if (kb + row > it.kend) {
-            uint8_t* vs = sm.v_ptr(s);
+      // ---- maximum of the raw scores (the scale is positive)
+      float mx = NEG_INF;
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c)
+      for (int c = 0; c < 4; ++c) {
 #pragma unroll
-              for (int t = 0; t < 8; ++t)
-                *reinterpret_cast<uint4*>(vs + c * 16384 + row * 128 + t * 16) = make_uint4(0, 0, 0, 0);
-          }
+        for (int t = 0; t < 32; t += 2) mx = max3f(mx, s[32 * c + t], s[32 * c + t + 1]);
+      }
+      const float mt = mx * sl2;
+      float alpha = 1.f;
+      bool resc = false;
+      if (mt > m_run + kLazy) {
+        alpha = ex2_approx(m_run - mt);  // 0 while m_run is -inf
+        m_run = mt;
+        resc = true;
+      }
+      // ---- O_X *= alpha where the maximum moved (O_X is overwritten at j = 0)
+      if (j > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32_nw(tO + 32 * c, o);
+          tmem_wait_ld();
+          reg_fence32(o);
+          float2* of = reinterpret_cast<float2*>(o);
+          const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+          for (int t = 0; t < 16; ++t) of[t] = __fmul2_rn(of[t], a2);
+          tmem_st16_nw(tO + 32 * c, o);
+          tmem_st16_nw(tO + 32 * c + 16, o + 16);
         }
       }
-      // ---- P row to shared memory (two [128, 64] swizzled blocks)
-      uint8_t* pb = sm.p_ptr();
+      // ---- P = exp2(s * scale - m) chunk by chunk into TMEM, row sum
+      const float mneg = (m_run == NEG_INF) ? 0.f : -m_run;
+      float2 sum2 = make_float2(0.f, 0.f);
+      const float2 sc2 = make_float2(sl2, sl2), of2 = make_float2(mneg, mneg);
 #pragma unroll
-      for (int ch = 0; ch < 16; ++ch)
-        *reinterpret_cast<uint4*>(pb + sw128_offset(row, ch)) =
-            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-      fence_proxy_async_smem();
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+        if (on & (1u << c)) {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            const float2 x = __ffma2_rn(make_float2(s[32 * c + 2 * t], s[32 * c + 2 * t + 1]), sc2, of2);
+            const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+            sum2 = __fadd2_rn(sum2, make_float2(p0, p1));
+            pk[t] = pack_bf16x2(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) pk[t] = 0u;
+        }
+        tmem_st16_nw(tS + 16 * c, pk);
+      }
+      l_run = l_run * alpha + (sum2.x + sum2.y);
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(sm.p_full());
-      m_run = m_new;
+      if (lane == 0) mbar_arrive(sm.p_full(X));
     }
     if (!ok) break;
-    kv_it += J;
 
-    // ---- epilogue: O / l -> bf16 -> global
-    if (!warp_wait(sm.pv_done(), pv_it & 1, abort, kRoleSoftmax)) { ok = false; break; }
-    ++pv_it;
+    // ---- epilogue: O / l -> bf16 (32 columns at a time) -> global
+    if (!warp_wait(sm.pv_done(X), pv_cnt & 1, abort, kRoleSoftmax)) { ok = false; break; }
+    ++pv_cnt;
     tc_fence_after();
-    float o[D];
+    const float inv = (row_valid && l_run > 0.f) ? 1.0f / l_run : 0.f;
+    uint32_t ob[D / 2];  // the row in bf16 pairs
 #pragma unroll
-    for (int c4 = 0; c4 < D / 32; ++c4) {
-      float tmp[32];
-      tmem_ld32(tmem + lane_base + C::kOCol + c4 * 32, tmp);
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      tmem_ld32_nw(tO + 32 * c, o);
+      tmem_wait_ld();
+      reg_fence32(o);
+      const float* of = reinterpret_cast<const float*>(o);
 #pragma unroll
-      for (int t = 0; t < 32; ++t) o[c4 * 32 + t] = tmp[t];
+      for (int t = 0; t < 16; ++t) ob[16 * c + t] = pack_bf16x2(of[2 * t] * inv, of[2 * t + 1] * inv);
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(sm.o_empty());
-    const float inv = (row_valid && l_run > 0.f) ? 1.0f / l_run : 0.f;
+    if (lane == 0) mbar_arrive(sm.o_empty(X));
     if (row_exists) {
+      // padded rows (inv = 0) are written as zeros; O is finite there since
+      // every value row such a row could meet is finite or zeroed
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        __nv_bfloat162 a = __floats2bfloat162_rn(o[8 * c + 0] * inv, o[8 * c + 1] * inv);
-        __nv_bfloat162 b = __floats2bfloat162_rn(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
-        __nv_bfloat162 e = __floats2bfloat162_rn(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
-        __nv_bfloat162 f = __floats2bfloat162_rn(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
-        orow[c] = make_uint4(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b),
-                             *reinterpret_cast<uint32_t*>(&e), *reinterpret_cast<uint32_t*>(&f));
-      }
+      for (int c = 0; c < D / 8; ++c)
+        orow[c] = row_valid ? make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3])
+                            : make_uint4(0, 0, 0, 0);
     }
   }
 }
 
+constexpr int kBandThreads = 320;
+
 template <int D>
-__global__ void __launch_bounds__(192, 1) band_tc_kernel(const __grid_constant__ BandParams p) {
+__global__ void __launch_bounds__(kBandThreads, 1) band_tc_kernel(const __grid_constant__ BandParams p) {
   using C = BandCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   BandSmem<D> sm;
@@ -491,25 +704,29 @@ __global__ void __launch_bounds__(192, 1) band_tc_kernel(const __grid_constant__
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(sm.q_full(), 1);
-    mbar_init(sm.q_empty(), 1);
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(sm.kv_full(s), 1);
-      mbar_init(sm.kv_empty(s), 1);
-    }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(sm.s_full(b), 1);
-      mbar_init(sm.s_empty(b), 4);
+      mbar_init(sm.q_full(b), 1);
+      mbar_init(sm.q_empty(b), 1);
     }
-    mbar_init(sm.p_full(), 4);
-    mbar_init(sm.pv_done(), 1);
-    mbar_init(sm.o_empty(), 4);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(sm.k_full(s), 1);
+      mbar_init(sm.k_empty(s), 1);
+      mbar_init(sm.v_full(s), 1);
+      mbar_init(sm.v_empty(s), 1);
+    }
+    mbar_init(sm.v_land(), 1);
+    for (int X = 0; X < 2; ++X) {
+      mbar_init(sm.s_full(X), 1);
+      mbar_init(sm.p_full(X), 4);
+      mbar_init(sm.pv_done(X), 1);
+      mbar_init(sm.o_empty(X), 4);
+    }
     mbar_init(sm.fin(), 1);
     *sm.abort_flag() = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
   }
-  if (warp == 1) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(sm.tmem_holder()), C::kTmemCols);
     tmem_relinquish();
   }
@@ -518,18 +735,19 @@ __global__ void __launch_bounds__(192, 1) band_tc_kernel(const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = *sm.tmem_holder();
 
-  if (warp == 0) {
+  if (warp < 8) {
+    if (warp < 4) band_softmax<D, 0>(p, sm, tmem, warp & 3, lane);
+    else band_softmax<D, 1>(p, sm, tmem, warp & 3, lane);
+  } else if (warp == 8) {
     band_producer<D>(p, sm, lane);
-  } else if (warp == 1) {
+  } else {
     if (lane == 0) band_mma<D>(p, sm, tmem);
     __syncwarp();
-  } else {
-    band_softmax<D>(p, sm, tmem, warp, lane);
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
@@ -547,7 +765,7 @@ static lf_status launch_band_tc_d(const BandParams& p, int grid, cudaStream_t s)
     }
     attr_set = true;
   }
-  band_tc_kernel<D><<<grid, 192, C::kSmem, s>>>(p);
+  band_tc_kernel<D><<<grid, kBandThreads, C::kSmem, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("band kernel launch: %s", cudaGetErrorString(e));

@@ -317,20 +317,11 @@ static lf_status global_merges(const Problem& P, const float* ws) {
 }
 
 // ------------------------------------------------------------------ bf16 band planning
-struct SegPlan {
-  int h, r, delta, n_r, tiles;
-};
-
-static lf_status run_band_bf16(const Problem& P, int b0, int nbat) {
-  // every (head, residue) class with at least one row
-  std::vector<SegPlan> segs;
-  for (int h = 0; h < P.H; ++h) {
-    const int delta = P.dil[h];
-    for (int r = 0; r < delta && r < P.n; ++r) {
-      const int n_r = (P.n - r + delta - 1) / delta;
-      segs.push_back({h, r, delta, n_r, (n_r + 127) / 128});
-    }
-  }
+// Every (head, residue) class with at least one row is a segment; its work
+// items are pairs of 128-row tiles.  Segments are generated in order straight
+// into the parameter block `p` (no heap use), one launch per kMaxSeg segments
+// or kMaxSets (dilation, residue) tensor-map sets.
+static lf_status run_band_bf16(const Problem& P, int b0, int nbat, BandParams& p) {
   const int grid_cap = sm_count();
   const size_t off = (size_t)b0 * P.H * P.n * P.d;
   const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(P.q) + off;
@@ -338,47 +329,46 @@ static lf_status run_band_bf16(const Problem& P, int b0, int nbat) {
   const __nv_bfloat16* v = reinterpret_cast<const __nv_bfloat16*>(P.v) + off;
   __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(P.out) + off;
   const int64_t planes = (int64_t)nbat * P.H;
-
-  static thread_local BandParams* bp = nullptr;  // ~25 KB: keep it off the stack
-  if (!bp) bp = new (std::nothrow) BandParams;
-  if (!bp) {
-    set_error("host allocation of the band parameter block failed");
-    return LF_ERR_NO_MEMORY;
-  }
-  size_t s0 = 0;
-  while (s0 < segs.size()) {
-    BandParams& p = *bp;
+  const int64_t half = std::min<int64_t>(P.w / 2, P.n);
+  int h = 0, r = 0;  // next segment to place
+  while (h < P.H) {
     memset(&p, 0, sizeof p);
-    int nsets = 0;
+    int nsets = 0, nseg = 0, items_per_b = 0;
     int set_delta[kMaxSets], set_r[kMaxSets];
-    size_t s1 = s0;
-    int items_per_b = 0;
-    for (; s1 < segs.size() && (int)(s1 - s0) < kMaxSeg; ++s1) {
-      const SegPlan& sg = segs[s1];
+    while (h < P.H && nseg < kMaxSeg) {
+      const int delta = P.dil[h];
+      if (r >= delta || r >= P.n) {
+        ++h;
+        r = 0;
+        continue;
+      }
       int set = -1;
       for (int t = 0; t < nsets; ++t)
-        if (set_delta[t] == sg.delta && set_r[t] == sg.r) set = t;
+        if (set_delta[t] == delta && set_r[t] == r) set = t;
       if (set < 0) {
         if (nsets == kMaxSets) break;
         set = nsets++;
-        set_delta[set] = sg.delta;
-        set_r[set] = sg.r;
+        set_delta[set] = delta;
+        set_r[set] = r;
       }
-      BandSeg& bs = p.seg[s1 - s0];
-      bs.h = sg.h;
-      bs.r = sg.r;
-      bs.delta = sg.delta;
-      bs.n_r = sg.n_r;
-      bs.tiles = sg.tiles;
+      const int n_r = (P.n - r + delta - 1) / delta;
+      BandSeg& bs = p.seg[nseg++];
+      bs.h = h;
+      bs.r = r;
+      bs.delta = delta;
+      bs.n_r = n_r;
+      bs.pairs = (n_r + 255) / 256;
       bs.set = set;
       bs.begin = items_per_b;
-      items_per_b += sg.tiles;
+      items_per_b += bs.pairs;
+      ++r;
     }
+    if (nseg == 0) break;
     for (int t = 0; t < nsets; ++t) {
-      const int delta = set_delta[t], r = set_r[t];
-      const int64_t n_r = (P.n - r + delta - 1) / delta;
+      const int delta = set_delta[t], rr = set_r[t];
+      const int64_t n_r = (P.n - rr + delta - 1) / delta;
       const int64_t rs = (int64_t)delta * P.d, ps = (int64_t)P.n * P.d;
-      const size_t ro = (size_t)r * P.d;
+      const size_t ro = (size_t)rr * P.d;
       lf_status st;
       if ((st = make_map(&p.tq[t], q + ro, P.d, n_r, planes, rs, ps)) != LF_OK) return st;
       if ((st = make_map(&p.tk[t], k + ro, P.d, n_r, planes, rs, ps)) != LF_OK) return st;
@@ -390,28 +380,26 @@ static lf_status run_band_bf16(const Problem& P, int b0, int nbat) {
     p.B = nbat;
     p.H = P.H;
     p.n = P.n;
-    const int64_t half = std::min<int64_t>(P.w / 2, P.n);
     p.half = (int32_t)half;
     p.right = P.causal ? 0 : (int32_t)half;
     p.causal = P.causal;
     p.G = P.G;
-    p.nseg = (int32_t)(s1 - s0);
+    p.nseg = nseg;
     p.items_per_b = items_per_b;
     const int64_t total = (int64_t)items_per_b * nbat;
     if (total > 0x7fffffff) {
-      set_error("too many band tiles (%lld)", (long long)total);
+      set_error("too many band work items (%lld)", (long long)total);
       return LF_ERR_UNSUPPORTED;
     }
     p.total_items = (int32_t)total;
     p.sl2 = (float)(1.4426950408889634 / std::sqrt((double)P.d));
     for (int b = 0; b < nbat; ++b) p.pad[b] = P.pad ? P.pad[b0 + b] : 0;
-    for (int r = 0; r < P.G; ++r) p.gidx[r] = P.gidx[r];
+    for (int g = 0; g < P.G; ++g) p.gidx[g] = P.gidx[g];
     const int grid = (int)std::min<int64_t>(total, grid_cap);
     if (grid > 0) {
       lf_status st = launch_band_tc(p, P.d, grid, P.stream);
       if (st != LF_OK) return st;
     }
-    s0 = s1;
   }
   return LF_OK;
 }
@@ -436,6 +424,21 @@ static lf_status record(cudaEvent_t e, cudaStream_t s) {
   cudaError_t r = cudaEventRecord(e, s);
   if (r != cudaSuccess) {
     set_error("cudaEventRecord: %s", cudaGetErrorString(r));
+    return LF_ERR_CUDA;
+  }
+  return LF_OK;
+}
+
+// A timing event: inside a stream capture it becomes an event-record node of
+// the graph (recorded again on every replay) instead of a capture dependency.
+static lf_status record_timing(cudaEvent_t e, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t r = cudaStreamIsCapturing(s, &cs);
+  if (r == cudaSuccess)
+    r = (cs == cudaStreamCaptureStatusActive) ? cudaEventRecordWithFlags(e, s, cudaEventRecordExternal)
+                                              : cudaEventRecord(e, s);
+  if (r != cudaSuccess) {
+    set_error("recording a timing event: %s", cudaGetErrorString(r));
     return LF_ERR_CUDA;
   }
   return LF_OK;
@@ -487,12 +490,23 @@ static lf_status forward_t(const Problem& P, bool bf16) {
   }
   // ---- band kernel on the caller's stream
   st = LF_OK;
-  if (t_band_start) st = record(t_band_start, P.stream);
+  if (t_band_start) st = record_timing(t_band_start, P.stream);
   for (int b0 = 0; st == LF_OK && b0 < P.B; b0 += kMaxBatch) {
     const int nb = std::min(kMaxBatch, P.B - b0);
-    st = bf16 ? run_band_bf16(P, b0, nb) : run_band_f32(P, b0, nb);
+    if (bf16) {
+      static thread_local BandParams* bp = nullptr;  // ~25 KB: keep it off the stack
+      if (!bp) bp = new (std::nothrow) BandParams;
+      if (!bp) {
+        set_error("host allocation of the band parameter block failed");
+        st = LF_ERR_NO_MEMORY;
+      } else {
+        st = run_band_bf16(P, b0, nb, *bp);
+      }
+    } else {
+      st = run_band_f32(P, b0, nb);
+    }
   }
-  if (st == LF_OK && t_band_stop) st = record(t_band_stop, P.stream);
+  if (st == LF_OK && t_band_stop) st = record_timing(t_band_stop, P.stream);
   // ---- merge (after the band kernel, which also wrote the global tokens' rows)
   if (P.G > 0) {
     if (st == LF_OK) st = global_merges<T>(P, ws);

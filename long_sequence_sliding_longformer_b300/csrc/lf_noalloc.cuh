@@ -78,93 +78,6 @@ static int64_t static_scratch_chunk(const Problem& P, int nbat) {
   return bytes(chunk) <= kStaticScratchBytes ? chunk : 0;
 }
 
-// The band launches of run_band_bf16, planned without heap memory: the
-// (head, residue) segments are generated in order straight into a parameter
-// block on the stack, one launch per kMaxSeg segments or kMaxSets map sets.
-static lf_status run_band_bf16_fixed(const Problem& P, int b0, int nbat) {
-  const int grid_cap = sm_count();
-  const size_t off = (size_t)b0 * P.H * P.n * P.d;
-  const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(P.q) + off;
-  const __nv_bfloat16* k = reinterpret_cast<const __nv_bfloat16*>(P.k) + off;
-  const __nv_bfloat16* v = reinterpret_cast<const __nv_bfloat16*>(P.v) + off;
-  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(P.out) + off;
-  const int64_t planes = (int64_t)nbat * P.H;
-  const int64_t half = std::min<int64_t>(P.w / 2, P.n);
-  BandParams p;
-  int h = 0, r = 0;  // next segment to place
-  while (h < P.H) {
-    memset(&p, 0, sizeof p);
-    int nsets = 0, nseg = 0, items_per_b = 0;
-    int set_delta[kMaxSets], set_r[kMaxSets];
-    while (h < P.H && nseg < kMaxSeg) {
-      const int delta = P.dil[h];
-      if (r >= delta || r >= P.n) {
-        ++h;
-        r = 0;
-        continue;
-      }
-      int set = -1;
-      for (int t = 0; t < nsets; ++t)
-        if (set_delta[t] == delta && set_r[t] == r) set = t;
-      if (set < 0) {
-        if (nsets == kMaxSets) break;
-        set = nsets++;
-        set_delta[set] = delta;
-        set_r[set] = r;
-      }
-      const int n_r = (P.n - r + delta - 1) / delta;
-      BandSeg& bs = p.seg[nseg++];
-      bs.h = h;
-      bs.r = r;
-      bs.delta = delta;
-      bs.n_r = n_r;
-      bs.tiles = (n_r + 127) / 128;
-      bs.set = set;
-      bs.begin = items_per_b;
-      items_per_b += bs.tiles;
-      ++r;
-    }
-    if (nseg == 0) break;
-    for (int t = 0; t < nsets; ++t) {
-      const int delta = set_delta[t], rr = set_r[t];
-      const int64_t n_r = (P.n - rr + delta - 1) / delta;
-      const int64_t rs = (int64_t)delta * P.d, ps = (int64_t)P.n * P.d;
-      const size_t ro = (size_t)rr * P.d;
-      lf_status st;
-      if ((st = make_map(&p.tq[t], q + ro, P.d, n_r, planes, rs, ps)) != LF_OK) return st;
-      if ((st = make_map(&p.tk[t], k + ro, P.d, n_r, planes, rs, ps)) != LF_OK) return st;
-      if ((st = make_map(&p.tv[t], v + ro, P.d, n_r, planes, rs, ps)) != LF_OK) return st;
-    }
-    p.k = k;
-    p.v = v;
-    p.out = out;
-    p.B = nbat;
-    p.H = P.H;
-    p.n = P.n;
-    p.half = (int32_t)half;
-    p.right = P.causal ? 0 : (int32_t)half;
-    p.causal = P.causal;
-    p.G = P.G;
-    p.nseg = nseg;
-    p.items_per_b = items_per_b;
-    const int64_t total = (int64_t)items_per_b * nbat;
-    if (total > 0x7fffffff) {
-      set_error("too many band tiles (%lld)", (long long)total);
-      return LF_ERR_UNSUPPORTED;
-    }
-    p.total_items = (int32_t)total;
-    p.sl2 = (float)(1.4426950408889634 / std::sqrt((double)P.d));
-    for (int b = 0; b < nbat; ++b) p.pad[b] = P.pad ? P.pad[b0 + b] : 0;
-    for (int g = 0; g < P.G; ++g) p.gidx[g] = P.gidx[g];
-    const int grid = (int)std::min<int64_t>(total, grid_cap);
-    if (grid > 0) {
-      lf_status st = launch_band_tc(p, P.d, grid, P.stream);
-      if (st != LF_OK) return st;
-    }
-  }
-  return LF_OK;
-}
-
 static lf_status forward_noalloc(const Problem& P) {
   t_msg[0] = 0;
   lf_status st = validate(P, true);
@@ -190,24 +103,13 @@ static lf_status forward_noalloc(const Problem& P) {
   float* ws = nullptr;
   if (P.G > 0 && (st = static_scratch_for_current_device(&ws)) != LF_OK) return st;
   cudaGetLastError();
-  if (t_band_start) {
-    cudaError_t e = cudaEventRecord(t_band_start, P.stream);
-    if (e != cudaSuccess) {
-      set_error("cudaEventRecord: %s", cudaGetErrorString(e));
-      return LF_ERR_CUDA;
-    }
-  }
+  if (t_band_start && (st = record_timing(t_band_start, P.stream)) != LF_OK) return st;
   for (int b0 = 0; b0 < P.B; b0 += kMaxBatch) {
     const int nb = std::min(kMaxBatch, P.B - b0);
-    if ((st = run_band_bf16_fixed(P, b0, nb)) != LF_OK) return st;
+    BandParams bp;  // on the stack: no heap use on this path
+    if ((st = run_band_bf16(P, b0, nb, bp)) != LF_OK) return st;
   }
-  if (t_band_stop) {
-    cudaError_t e = cudaEventRecord(t_band_stop, P.stream);
-    if (e != cudaSuccess) {
-      set_error("cudaEventRecord: %s", cudaGetErrorString(e));
-      return LF_ERR_CUDA;
-    }
-  }
+  if (t_band_stop && (st = record_timing(t_band_stop, P.stream)) != LF_OK) return st;
   if (P.G == 0) return LF_OK;
   // batch chunks run one after another on the stream, so they can share the array
   for (int b0 = 0; b0 < P.B; b0 += kMaxBatch) {
