@@ -17,7 +17,7 @@
 // the union of the two windows once (128-key "entries", then the gathered
 // global-token keys) and both tiles consume the shared entries.
 //
-// One CTA per SM, persistent over items, 10 warps:
+// One CTA per SM, persistent over items, 12 warps:
 //   warps 0-3  softmax of tile 0, warps 4-7 softmax of tile 1: one query row
 //              per thread; S rows are read from TMEM, masked, turned into
 //              P = exp2(S*scale - m) with a lazily updated row maximum, and P
@@ -27,6 +27,8 @@
 //   warp 9     allocates TMEM; lane 0 issues every tcgen05.mma:
 //              S_X = Q_X K^T (both operands in shared memory) and
 //              O_X += P_X V (P from TMEM, V from shared memory)
+//   warps 10-11 idle (they complete the third warpgroup, whose registers go
+//              to the softmax warps)
 // While the softmax warps of one tile work, the tensor cores run the other
 // tile's products (ping-pong), so the exponentials and the MMAs overlap.
 //
@@ -490,10 +492,19 @@ __device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tm
 // rescaled rarely; P values stay below 2^kLazy.
 constexpr float kLazy = 8.0f;
 
+// Bits [lo, hi] of a 32-bit word (empty when hi < lo); lo, hi may lie outside [0, 31].
+__device__ __forceinline__ uint32_t bit_range(int lo, int hi) {
+  lo = max(lo, 0);
+  hi = min(hi, 31);
+  if (hi < lo) return 0u;
+  const uint32_t upto = (hi == 31) ? 0xffffffffu : ((1u << (hi + 1)) - 1u);
+  return upto & ~((1u << lo) - 1u);
+}
+
 // Softmax of tile X (one query row per thread; warp quarter wq of TMEM lanes).
-template <int D, int X>
-__device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_t tmem, int wq,
-                             int lane) {
+template <int D>
+__device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_t tmem, int X,
+                             int wq, int lane) {
   using C = BandCfg<D>;
   volatile int* abort = sm.abort_flag();
   const int row = wq * 32 + lane;
@@ -508,48 +519,56 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
   for (int item = blockIdx.x; ok && item < p.total_items; item += gridDim.x) {
     const PairItem it = decode_pair(p, item);
     const int m_q = it.m0 + 128 * X + row;
-    const int i_q = it.r + it.delta * m_q;
     const bool row_exists = m_q < it.n_r;
     const bool row_valid = m_q < it.Lm;
-    uint4* orow = reinterpret_cast<uint4*>(p.out + ((size_t)it.bh * p.n + (row_exists ? i_q : 0)) * D);
-    if (it.zero || !it.act[X]) {
+    if (it.zero || !(X ? it.act[1] : it.act[0])) {
       if (row_exists) {
+        uint4* orow = reinterpret_cast<uint4*>(p.out + ((size_t)it.bh * p.n + it.r + (size_t)it.delta * m_q) * D);
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
       }
       continue;
     }
-    const int len = it.len[X], nb = it.nb[X], b0 = it.b0[X], gb = it.gbase[X];
-    const int nU = it.nU, U0 = it.U0, Lm = it.Lm;
+    const int len = pick(it.len, X), nb = pick(it.nb, X), b0 = pick(it.b0, X), gb = pick(it.gbase, X);
     float m_run = NEG_INF, l_run = 0.f;
 
     for (int j = 0; j < len; ++j) {
       const bool is_band = j < nb;
       const int e = is_band ? b0 + j : gb + (j - nb);
-      // ---- which 32-column chunks this warp needs, and which are fully valid
-      int clo, chi;  // valid columns of this row
-      int gt = 0, gcnt = 0;
+      // ---- keep[c]: bit t set where this row attends column 32c + t
+      uint32_t keep[4];
       if (is_band) {
-        const int kb = U0 + 128 * e;
-        clo = max(0, m_q - p.half - kb);
-        chi = min(127, min(m_q + p.right, Lm - 1) - kb);
-        if (!row_valid || clo > chi) { clo = 128; chi = -1; }
+        const int kb = it.U0 + 128 * e;
+        int clo = m_q - p.half - kb;
+        int chi = min(m_q + p.right, it.Lm - 1) - kb;
+        if (!row_valid) chi = clo - 1;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) keep[c] = bit_range(clo - 32 * c, chi - 32 * c);
       } else {
-        int gx;
+        int gx, gt;
         global_entry(it, e, gx, gt);
-        gcnt = global_count(it, gx, gt);
-        clo = row_valid ? 0 : 128;
-        chi = row_valid ? gcnt - 1 : -1;
+        const int gcnt = global_count(it, gx, gt);
+        const int i_q = it.r + it.delta * m_q;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t k = 0;
+          const int tend = max(0, min(32, gcnt - 32 * c));
+#pragma unroll 1
+          for (int t = 0; t < tend; ++t) {
+            const int g = p.gidx[128 * gt + 32 * c + t];
+            const int mg = residue_coord(g, it.r, it.delta);
+            const bool in_band = (m_q - mg <= p.half) && (mg - m_q <= p.right);
+            k |= (uint32_t)((!p.causal || g <= i_q) && !in_band) << t;
+          }
+          keep[c] = row_valid ? k : 0u;
+        }
       }
-      const int wlo = __reduce_min_sync(0xffffffffu, clo);
-      const int whi = __reduce_max_sync(0xffffffffu, chi);
-      const int flo = __reduce_max_sync(0xffffffffu, clo);
-      const int fhi = __reduce_min_sync(0xffffffffu, chi);
+      // chunks some lane of the warp needs, and chunks every lane needs whole
       uint32_t on = 0, full = 0;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        if (32 * c + 31 >= wlo && 32 * c <= whi) on |= 1u << c;
-        if (is_band && flo <= 32 * c && fhi >= 32 * c + 31) full |= 1u << c;
+        if (__any_sync(0xffffffffu, keep[c] != 0u)) on |= 1u << c;
+        if (__all_sync(0xffffffffu, keep[c] == 0xffffffffu)) full |= 1u << c;
       }
 
       // S_X(j) complete; it was issued after P_X(j-1).V, so that is complete too
@@ -564,44 +583,14 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
       for (int c = 0; c < 4; ++c) reg_fence32(sr + 32 * c);
       float* s = reinterpret_cast<float*>(sr);
 
-      // ---- masks
-      if (is_band) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (!(full & (1u << c))) {
-#pragma unroll
-            for (int t = 0; t < 32; ++t) {
-              const int col = 32 * c + t;
-              s[col] = (col >= clo && col <= chi) ? s[col] : NEG_INF;
-            }
-          }
-        }
-      } else {
-        const int gofs = 128 * gt;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          {
-            // bit t of `keep`: this row attends global column 32c + t (a
-            // global key already in the row's band is counted there, once)
-            uint32_t keep = 0;
-            const int tend = max(0, min(32, gcnt - 32 * c));
-#pragma unroll 1
-            for (int t = 0; t < tend; ++t) {
-              const int g = p.gidx[gofs + 32 * c + t];
-              const int mg = residue_coord(g, it.r, it.delta);
-              const bool in_band = (m_q - mg <= p.half) && (mg - m_q <= p.right);
-              const bool k = row_valid && (!p.causal || g <= i_q) && !in_band;
-              keep |= (uint32_t)k << t;
-            }
-#pragma unroll
-            for (int t = 0; t < 32; ++t) s[32 * c + t] = ((keep >> t) & 1u) ? s[32 * c + t] : NEG_INF;
-          }
-        }
-      }
-      // ---- maximum of the raw scores (the scale is positive)
+      // ---- masks, and the maximum of the raw scores (the scale is positive)
       float mx = NEG_INF;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
+        if (!(full & (1u << c))) {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) s[32 * c + t] = ((keep[c] >> t) & 1u) ? s[32 * c + t] : NEG_INF;
+        }
 #pragma unroll
         for (int t = 0; t < 32; t += 2) mx = max3f(mx, s[32 * c + t], s[32 * c + t + 1]);
       }
@@ -615,7 +604,7 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
       }
       // ---- O_X *= alpha where the maximum moved (O_X is overwritten at j = 0)
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           tmem_ld32_nw(tO + 32 * c, o);
@@ -678,6 +667,7 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
     __syncwarp();
     if (lane == 0) mbar_arrive(sm.o_empty(X));
     if (row_exists) {
+      uint4* orow = reinterpret_cast<uint4*>(p.out + ((size_t)it.bh * p.n + it.r + (size_t)it.delta * m_q) * D);
       // padded rows (inv = 0) are written as zeros; O is finite there since
       // every value row such a row could meet is finite or zeroed
 #pragma unroll
@@ -688,7 +678,15 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
   }
 }
 
-constexpr int kBandThreads = 320;
+// Three warpgroups: two of softmax warps, one holding the producer warp, the
+// MMA warp and two idle warps.  Launched at 168 registers per thread
+// (384 x 168 = 64512 of the SM's 65536), the third warpgroup gives registers
+// back (setmaxnreg.dec to kRegsOther) and the softmax warpgroups take them
+// (setmaxnreg.inc to kRegsSoftmax): 256 x 200 + 128 x 96 = 63488 <= 64512.
+constexpr int kBandThreads = 384;
+constexpr int kRegsSoftmax = 200;
+constexpr int kRegsOther = 96;
+constexpr int kRegsAtLaunchMin = (256 * kRegsSoftmax + 128 * kRegsOther + kBandThreads - 1) / kBandThreads;
 
 template <int D>
 __global__ void __launch_bounds__(kBandThreads, 1) band_tc_kernel(const __grid_constant__ BandParams p) {
@@ -736,13 +734,16 @@ __global__ void __launch_bounds__(kBandThreads, 1) band_tc_kernel(const __grid_c
   const uint32_t tmem = *sm.tmem_holder();
 
   if (warp < 8) {
-    if (warp < 4) band_softmax<D, 0>(p, sm, tmem, warp & 3, lane);
-    else band_softmax<D, 1>(p, sm, tmem, warp & 3, lane);
-  } else if (warp == 8) {
-    band_producer<D>(p, sm, lane);
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    band_softmax<D>(p, sm, tmem, warp >> 2, warp & 3, lane);
   } else {
-    if (lane == 0) band_mma<D>(p, sm, tmem);
-    __syncwarp();
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
+    if (warp == 8) {
+      band_producer<D>(p, sm, lane);
+    } else if (warp == 9) {
+      if (lane == 0) band_mma<D>(p, sm, tmem);
+      __syncwarp();
+    }
   }
 
   tc_fence_before();
@@ -762,6 +763,20 @@ static lf_status launch_band_tc_d(const BandParams& p, int grid, cudaStream_t s)
     if (e != cudaSuccess) {
       set_error("cudaFuncSetAttribute(band kernel): %s", cudaGetErrorString(e));
       return LF_ERR_CUDA;
+    }
+    // The register hand-over between warpgroups needs the launch allocation
+    // it was planned for; with fewer registers setmaxnreg.inc could never be
+    // satisfied, so refuse to launch rather than wait.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, band_tc_kernel<D>);
+    if (e != cudaSuccess) {
+      set_error("cudaFuncGetAttributes(band kernel): %s", cudaGetErrorString(e));
+      return LF_ERR_CUDA;
+    }
+    if (fa.numRegs < kRegsAtLaunchMin || fa.numRegs * kBandThreads > 65536) {
+      set_error("band kernel built with %d registers per thread; its register split needs %d..%d",
+                fa.numRegs, kRegsAtLaunchMin, 65536 / kBandThreads);
+      return LF_ERR_UNSUPPORTED;
     }
     attr_set = true;
   }
