@@ -18,19 +18,20 @@
 // global-token keys) and both tiles consume the shared entries.
 //
 // One CTA per SM, persistent over items, 12 warps:
-//   warps 0-3  softmax of tile 0, warps 4-7 softmax of tile 1: one query row
+//   warp 0     allocates TMEM; V producer: TMA loads of the V entries into
+//              a ring of shared-memory slots, gathers of global-token rows
+//   warp 1     Q/K producer: TMA loads of Q and of the K entries
+//   warps 2-3  transpose each V entry into V^T (the layout the P.V MMA reads
+//              at full rate)
+//   warps 4-7  softmax of tile 0, warps 8-11 softmax of tile 1: one query row
 //              per thread; S rows are read from TMEM, masked, turned into
 //              P = exp2(S*scale - m) with a lazily updated row maximum, and P
-//              (bf16) is written back to TMEM for the P.V product
-//   warp 8     producer: TMA loads of Q and of the K/V entries into two
-//              rings of shared-memory slots; gathers of global-token rows
-//   warp 9     allocates TMEM; lane 0 issues every tcgen05.mma:
-//              S_X = Q_X K^T (both operands in shared memory) and
-//              O_X += P_X V (P from TMEM, V from shared memory)
-//   warps 10-11 idle (they complete the third warpgroup, whose registers go
-//              to the softmax warps)
-// While the softmax warps of one tile work, the tensor cores run the other
-// tile's products (ping-pong), so the exponentials and the MMAs overlap.
+//              (bf16) is written back to TMEM; an elected lane of the tile's
+//              first warp then issues the tile's tcgen05.mma products,
+//              O_X += P_X V (V^T from shared memory) and the next
+//              S_X = Q_X K^T (both operands in shared memory)
+// While the softmax warps of one tile compute, the tensor cores can run the
+// other tile's products.
 //
 // TMEM: S_0, S_1 (128 columns each) and O_0, O_1 (D columns each).  P_X
 // (two bf16 per column) overwrites the first 64 columns of S_X once the row
@@ -49,22 +50,26 @@ namespace lf {
 
 template <int D>
 struct BandCfg {
-  static constexpr int kQBuf = (D == 64) ? 2 : 1;
-  static constexpr int kKSt = (D == 64) ? 4 : 3;
-  static constexpr int kVSt = (D == 64) ? 4 : 2;
+  static constexpr int kQBuf = 1;                  // Q is reloaded ~2 steps before an item ends
+  static constexpr int kKSt = (D == 64) ? 5 : 2;   // K slots
+  static constexpr int kVSt = (D == 64) ? 3 : 1;   // V slots (as loaded: [keys, D])
+  static constexpr int kTSt = (D == 64) ? 4 : 2;   // V^T slots ([D, keys], the P.V operand)
   static constexpr int kTile = 128 * D * 2;     // bytes of one [128, D] bf16 tile
   static constexpr int kOffQ = 0;               // Q[qb][X] at kOffQ + (2*qb + X) * kTile
   static constexpr int kOffK = kQBuf * 2 * kTile;
   static constexpr int kOffV = kOffK + kKSt * kTile;
-  static constexpr int kOffBar = kOffV + kVSt * kTile;
-  // q_full[2], q_empty[2], k_full[4], k_empty[4], v_full[4], v_empty[4], v_land,
-  // s_full[2], (unused)[2], p_full[2], pv_done[2], o_empty[2], fin
-  static constexpr int kNumBar = 2 + 2 + 4 + 4 + 4 + 4 + 1 + 2 + 2 + 2 + 2 + 2 + 1;
+  static constexpr int kOffVT = kOffV + kVSt * kTile;
+  static constexpr int kOffBar = kOffVT + kTSt * kTile;
+  // q_full[2], q_empty[2], k_full[8], k_empty[8], v_full[4], v_empty[4], v_land,
+  // s_full[2], (unused)[2], p_full[2], pv_done[2], (unused)[2], fin, vt_full[4], vt_empty[4]
+  static constexpr int kNumBar = 2 + 2 + 8 + 8 + 4 + 4 + 1 + 2 + 2 + 2 + 2 + 2 + 1 + 4 + 4;
+  static_assert(kKSt <= 8 && kVSt <= 4 && kTSt <= 4 && kQBuf <= 2, "barrier arrays");
   static constexpr int kOffMisc = kOffBar + kNumBar * 8;
-  static constexpr int kSmem = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
+  static constexpr int kSmem = kOffMisc + 16 + kMaxSeg * (int)sizeof(BandSeg) + 1024;  // + slack to align the base to 1024
   static constexpr int kTmemCols = 512;
-  static constexpr uint32_t kColS = 0;     // S_X (and P_X) at 128*X
+  static constexpr uint32_t kColS = 0;     // S_X at 128*X
   static constexpr uint32_t kColO = 256;   // O_X at 256 + D*X
+
 };
 
 // Everything the roles need to know about one work item.  Computed the same
@@ -94,16 +99,18 @@ __device__ __forceinline__ int upper_bound_gidx(const BandParams& p, int lim) {
   return lo;
 }
 
-__device__ __forceinline__ PairItem decode_pair(const BandParams& p, int item) {
+// `segs`: the launch's segment table, copied to shared memory at kernel start
+// (a search over the kernel parameters would miss the constant cache).
+__device__ __forceinline__ PairItem decode_pair(const BandParams& p, const BandSeg* segs, int item) {
   PairItem it;
   it.b = item / p.items_per_b;
   const int rem = item - it.b * p.items_per_b;
   int lo = 0, hi = p.nseg - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (p.seg[mid].begin <= rem) lo = mid; else hi = mid - 1;
+    if (segs[mid].begin <= rem) lo = mid; else hi = mid - 1;
   }
-  const BandSeg& sg = p.seg[lo];
+  const BandSeg sg = segs[lo];
   it.h = sg.h;
   it.r = sg.r;
   it.delta = sg.delta;
@@ -211,23 +218,26 @@ struct BandSmem {
   __device__ __forceinline__ uint32_t q(int qb, int X) const { return sbase + C::kOffQ + (2 * qb + X) * C::kTile; }
   __device__ __forceinline__ uint32_t k(int s) const { return sbase + C::kOffK + s * C::kTile; }
   __device__ __forceinline__ uint32_t v(int s) const { return sbase + C::kOffV + s * C::kTile; }
+  __device__ __forceinline__ uint32_t vt(int s) const { return sbase + C::kOffVT + s * C::kTile; }
   __device__ __forceinline__ uint8_t* k_ptr(int s) const { return base + C::kOffK + s * C::kTile; }
   __device__ __forceinline__ uint8_t* v_ptr(int s) const { return base + C::kOffV + s * C::kTile; }
   __device__ __forceinline__ uint32_t bar(int i) const { return sbase + C::kOffBar + 8 * i; }
   __device__ __forceinline__ uint32_t q_full(int b) const { return bar(0 + b); }
   __device__ __forceinline__ uint32_t q_empty(int b) const { return bar(2 + b); }
   __device__ __forceinline__ uint32_t k_full(int s) const { return bar(4 + s); }
-  __device__ __forceinline__ uint32_t k_empty(int s) const { return bar(8 + s); }
-  __device__ __forceinline__ uint32_t v_full(int s) const { return bar(12 + s); }
-  __device__ __forceinline__ uint32_t v_empty(int s) const { return bar(16 + s); }
-  __device__ __forceinline__ uint32_t v_land() const { return bar(20); }
-  __device__ __forceinline__ uint32_t s_full(int X) const { return bar(21 + X); }
-  __device__ __forceinline__ uint32_t p_full(int X) const { return bar(25 + X); }
-  __device__ __forceinline__ uint32_t pv_done(int X) const { return bar(27 + X); }
-  __device__ __forceinline__ uint32_t o_empty(int X) const { return bar(29 + X); }
-  __device__ __forceinline__ uint32_t fin() const { return bar(31); }
+  __device__ __forceinline__ uint32_t k_empty(int s) const { return bar(12 + s); }
+  __device__ __forceinline__ uint32_t v_full(int s) const { return bar(20 + s); }
+  __device__ __forceinline__ uint32_t v_empty(int s) const { return bar(24 + s); }
+  __device__ __forceinline__ uint32_t v_land() const { return bar(28); }
+  __device__ __forceinline__ uint32_t s_full(int X) const { return bar(29 + X); }
+  __device__ __forceinline__ uint32_t p_full(int X) const { return bar(33 + X); }
+  __device__ __forceinline__ uint32_t pv_done(int X) const { return bar(35 + X); }
+  __device__ __forceinline__ uint32_t fin() const { return bar(39); }
+  __device__ __forceinline__ uint32_t vt_full(int s) const { return bar(40 + s); }
+  __device__ __forceinline__ uint32_t vt_empty(int s) const { return bar(44 + s); }
   __device__ __forceinline__ uint32_t* tmem_holder() const { return reinterpret_cast<uint32_t*>(base + C::kOffMisc); }
   __device__ __forceinline__ volatile int* abort_flag() const { return reinterpret_cast<volatile int*>(base + C::kOffMisc + 4); }
+  __device__ __forceinline__ BandSeg* segs() const { return reinterpret_cast<BandSeg*>(base + C::kOffMisc + 16); }
 };
 
 // 16-byte chunk `ch` of row `row` inside a [rows, D] bf16 tile stored as D/64
@@ -244,246 +254,301 @@ __device__ __forceinline__ int residue_coord(int g, int r, int delta) {
   return (d >= 0 && d % delta == 0) ? d / delta : -(1 << 29);
 }
 
-// ------------------------------------------------------------------ producer
-template <int D>
+// ------------------------------------------------------------------ producers
+// Two warps: KV = false loads Q and the K entries, KV = true the V entries,
+// so that a full V ring (waiting for the transposer) never holds back the K
+// an S product needs.
+template <int D, bool kIsV>
 __device__ void band_producer(const BandParams& p, const BandSmem<D>& sm, int lane) {
   using C = BandCfg<D>;
+  constexpr int kSt = kIsV ? C::kVSt : C::kKSt;
   volatile int* abort = sm.abort_flag();
   uint32_t kv = 0, q_it = 0, land = 0;
   int land_pending = -1;  // v_land phase of a zeroing load not yet seen to land
-  int last_k[C::kKSt], last_v[C::kVSt], last_q[C::kQBuf];
+  int last_fill[kSt], last_q[C::kQBuf];
 #pragma unroll
-  for (int s = 0; s < C::kKSt; ++s) last_k[s] = -1;
-#pragma unroll
-  for (int s = 0; s < C::kVSt; ++s) last_v[s] = -1;
+  for (int s = 0; s < kSt; ++s) last_fill[s] = -1;
 #pragma unroll
   for (int s = 0; s < C::kQBuf; ++s) last_q[s] = -1;
   bool ok = true;
+  Tracer tr;
+  if (blockIdx.x == 0 && lane == 0) tr.track = kIsV ? 5 : 3;
 
   for (int item = blockIdx.x; ok && item < p.total_items; item += gridDim.x) {
-    const PairItem it = decode_pair(p, item);
+    const PairItem it = decode_pair(p, sm.segs(), item);
     if (it.zero) continue;
 
-    // ---- Q of both tiles
-    const int qb = q_it % C::kQBuf;
-    if (!warp_wait(sm.q_empty(qb), ((q_it / C::kQBuf) & 1) ^ 1, abort, kRoleProducer)) { ok = false; break; }
-    if (lane == 0) {
-      mbar_arrive_expect_tx(sm.q_full(qb), (it.act[1] ? 2 : 1) * C::kTile);
+    if (!kIsV) {
+      // ---- Q of both tiles
+      const int qb = q_it % C::kQBuf;
+      if (!warp_wait(sm.q_empty(qb), ((q_it / C::kQBuf) & 1) ^ 1, abort, kRoleProducer)) { ok = false; break; }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(sm.q_full(qb), (it.act[1] ? 2 : 1) * C::kTile);
 #pragma unroll
-      for (int X = 0; X < 2; ++X) {
-        if (!it.act[X]) continue;
+        for (int X = 0; X < 2; ++X) {
+          if (!it.act[X]) continue;
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sm.q(qb, X) + c * 16384, &p.tq[it.set], c * 64, it.m0 + 128 * X, it.bh, sm.q_full(qb));
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(sm.q(qb, X) + c * 16384, &p.tq[it.set], c * 64, it.m0 + 128 * X, it.bh, sm.q_full(qb));
+        }
       }
+      last_q[qb] = (int)q_it;
+      ++q_it;
     }
-    last_q[qb] = (int)q_it;
-    ++q_it;
 
-    const __nv_bfloat16* kb = p.k + (size_t)it.bh * p.n * D;
-    const __nv_bfloat16* vb = p.v + (size_t)it.bh * p.n * D;
+    const __nv_bfloat16* src = (kIsV ? p.v : p.k) + (size_t)it.bh * p.n * D;
+    const CUtensorMap* map = kIsV ? &p.tv[it.set] : &p.tk[it.set];
     constexpr int CH = D / 8;  // 16-byte chunks per row
 
     for (int e = 0; e < it.nE; ++e, ++kv) {
-      const int ks = kv % C::kKSt, vs = kv % C::kVSt;
-      // ---------------- K
-      if (!warp_wait(sm.k_empty(ks), ((kv / C::kKSt) & 1) ^ 1, abort, kRoleProducer)) { ok = false; break; }
-      if (e < it.nU) {
-        if (lane == 0) {
-          mbar_arrive_expect_tx(sm.k_full(ks), C::kTile);
-          const int y = it.U0 + 128 * e;
-#pragma unroll
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(sm.k(ks) + c * 16384, &p.tk[it.set], c * 64, y, it.bh, sm.k_full(ks));
-        }
-        last_k[ks] = (int)kv;
-      } else {
-        int X, gt;
-        global_entry(it, e, X, gt);
-        const int cnt = global_count(it, X, gt);
-        const int ng = (cnt + 15) & ~15;
-        uint8_t* dst = sm.k_ptr(ks);
-        for (int idx = lane; idx < ng * CH; idx += 32) {
-          const int row = idx / CH, ch = idx - (idx / CH) * CH;
-          uint4 x = make_uint4(0, 0, 0, 0);
-          if (row < cnt) x = __ldg(reinterpret_cast<const uint4*>(kb + (size_t)p.gidx[128 * gt + row] * D) + ch);
-          *reinterpret_cast<uint4*>(dst + sw128_offset(row, ch)) = x;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sm.k_full(ks));
-        last_k[ks] = -1;  // completed synchronously
-      }
-      // ---------------- V
-      if (!warp_wait(sm.v_empty(vs), ((kv / C::kVSt) & 1) ^ 1, abort, kRoleProducer)) { ok = false; break; }
+      const int slot = kv % kSt;
+      const uint32_t full = kIsV ? sm.v_full(slot) : sm.k_full(slot);
+      const uint32_t empty = kIsV ? sm.v_empty(slot) : sm.k_empty(slot);
+      const uint32_t dst = kIsV ? sm.v(slot) : sm.k(slot);
+      uint8_t* dst_ptr = kIsV ? sm.v_ptr(slot) : sm.k_ptr(slot);
+      tr.ev(30);
+      if (!warp_wait(empty, ((kv / kSt) & 1) ^ 1, abort, kRoleProducer)) { ok = false; break; }
+      tr.ev(31);
       if (e < it.nU) {
         const int y = it.U0 + 128 * e;
-        // rows past the last key any row of the pair attends (padding, or the
-        // end of the window union) but inside the tensor are zeroed, so that
-        // whatever they hold cannot reach the output through 0 * value
+        // value rows past the last key any row of the pair attends (padding,
+        // or the end of the window union) but inside the tensor are zeroed,
+        // so that whatever they hold cannot reach the output through 0 * value
         const int z0 = it.khi - y + 1, z1 = min(128, it.n_r - y);
-        if (z0 < z1) {
+        if (kIsV && z0 < z1) {
           if (lane == 0) {
             mbar_arrive_expect_tx(sm.v_land(), C::kTile);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c)
-              tma_load_3d(sm.v(vs) + c * 16384, &p.tv[it.set], c * 64, y, it.bh, sm.v_land());
+              tma_load_3d(dst + c * 16384, map, c * 64, y, it.bh, sm.v_land());
           }
           land_pending = (int)land;
           const bool landed = warp_wait(sm.v_land(), land & 1, abort, kRoleProducer);
           ++land;
           if (!landed) { ok = false; break; }
           land_pending = -1;
-          uint8_t* dst = sm.v_ptr(vs);
           for (int idx = lane; idx < (z1 - z0) * CH; idx += 32) {
             const int row = z0 + idx / CH, ch = idx - (idx / CH) * CH;
-            *reinterpret_cast<uint4*>(dst + sw128_offset(row, ch)) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(dst_ptr + sw128_offset(row, ch)) = make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(sm.v_full(vs));
-          last_v[vs] = -1;
+          if (lane == 0) mbar_arrive(full);
+          last_fill[slot] = -1;
         } else {
           if (lane == 0) {
-            mbar_arrive_expect_tx(sm.v_full(vs), C::kTile);
+            mbar_arrive_expect_tx(full, C::kTile);
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c)
-              tma_load_3d(sm.v(vs) + c * 16384, &p.tv[it.set], c * 64, y, it.bh, sm.v_full(vs));
+            for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * 16384, map, c * 64, y, it.bh, full);
           }
-          last_v[vs] = (int)kv;
+          last_fill[slot] = (int)kv;
         }
       } else {
+        // rows of the global tokens visible to the entry's tile, zeros after
         int X, gt;
         global_entry(it, e, X, gt);
         const int cnt = global_count(it, X, gt);
         const int ng = (cnt + 15) & ~15;
-        uint8_t* dst = sm.v_ptr(vs);
         for (int idx = lane; idx < ng * CH; idx += 32) {
           const int row = idx / CH, ch = idx - (idx / CH) * CH;
           uint4 x = make_uint4(0, 0, 0, 0);
-          if (row < cnt) x = __ldg(reinterpret_cast<const uint4*>(vb + (size_t)p.gidx[128 * gt + row] * D) + ch);
-          *reinterpret_cast<uint4*>(dst + sw128_offset(row, ch)) = x;
+          if (row < cnt) x = __ldg(reinterpret_cast<const uint4*>(src + (size_t)p.gidx[128 * gt + row] * D) + ch);
+          *reinterpret_cast<uint4*>(dst_ptr + sw128_offset(row, ch)) = x;
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(sm.v_full(vs));
-        last_v[vs] = -1;
+        if (lane == 0) mbar_arrive(full);
+        last_fill[slot] = -1;  // completed synchronously
       }
+      tr.ev(32);
     }
   }
+  tr.done();
   // Let every TMA copy this warp issued land before the CTA can exit.
   int dummy = 0;
 #pragma unroll
-  for (int s = 0; s < C::kKSt; ++s)
-    if (last_k[s] >= 0) mbar_wait(sm.k_full(s), ((uint32_t)last_k[s] / C::kKSt) & 1, &dummy, kRoleDrain, 200000000ull);
-#pragma unroll
-  for (int s = 0; s < C::kVSt; ++s)
-    if (last_v[s] >= 0) mbar_wait(sm.v_full(s), ((uint32_t)last_v[s] / C::kVSt) & 1, &dummy, kRoleDrain, 200000000ull);
+  for (int s = 0; s < kSt; ++s)
+    if (last_fill[s] >= 0)
+      mbar_wait(kIsV ? sm.v_full(s) : sm.k_full(s), ((uint32_t)last_fill[s] / kSt) & 1, &dummy, kRoleDrain, 200000000ull);
 #pragma unroll
   for (int s = 0; s < C::kQBuf; ++s)
     if (last_q[s] >= 0) mbar_wait(sm.q_full(s), ((uint32_t)last_q[s] / C::kQBuf) & 1, &dummy, kRoleDrain, 200000000ull);
   if (land_pending >= 0) mbar_wait(sm.v_land(), (uint32_t)land_pending & 1, &dummy, kRoleDrain, 200000000ull);
 }
 
-// ------------------------------------------------------------------ MMA issuer (one thread)
+// ------------------------------------------------------------------ MMA issue (per tile)
+// Each softmax warpgroup issues the products of its own tile: after the four
+// warps have written P_X(j) they meet at a named barrier, and one elected
+// lane of the first warp issues O_X += P_X(j) V(j) and then S_X(j+1) =
+// Q_X K(j+1)^T (in that order: S_X(j+1) overwrites P_X(j)).  The whole warp
+// runs the bookkeeping so that descriptors stay in uniform registers.
+//
+// K and V^T slots are released by both tiles: each slot's "empty" barrier
+// takes one arrival per tile and fill, from tcgen05.commit after the tile's
+// last product that reads it, or a plain arrival from a tile that does not
+// use the entry once that fill is visible (so the arrival cannot count
+// towards the slot's previous fill).
 template <int D>
-__device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tmem) {
+struct TileIssuer {
   using C = BandCfg<D>;
-  volatile int* abort = sm.abort_flag();
-  const uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
-  uint32_t kv = 0, q_it = 0;
-  uint32_t p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
-  bool ok = true;
+  static constexpr uint32_t kTile16 = C::kTile >> 4;  // a slot, in descriptor address units
+  const BandSmem<D>& sm;
+  volatile int* abort;
+  Tracer* tr = nullptr;
+  int X;
+  uint32_t tmem;
+  uint64_t qdesc0, kdesc0, vdesc0;
+  uint32_t idesc_s128, idesc_pv;
 
-  for (int item = blockIdx.x; ok && item < p.total_items; item += gridDim.x) {
-    const PairItem it = decode_pair(p, item);
-    if (it.zero) continue;
-    const int qb = q_it % C::kQBuf;
-    if (!mbar_wait(sm.q_full(qb), (q_it / C::kQBuf) & 1, abort, kRoleMma)) { ok = false; break; }
-    ++q_it;
+  __device__ TileIssuer(const BandSmem<D>& sm_, uint32_t tmem_, int X_)
+      : sm(sm_), abort(sm_.abort_flag()), X(X_), tmem(tmem_) {
+    qdesc0 = smem_desc_sw128(sm.q(0, 0), 16, 1024);
+    kdesc0 = smem_desc_sw128(sm.k(0), 16, 1024);
+    vdesc0 = smem_desc_sw128(sm.vt(0), 16, 1024);
+    idesc_s128 = idesc_bf16_f32(128, 128, 0);
+    idesc_pv = idesc_bf16_f32(128, D, 0);  // V^T: K-major
+  }
+
+  // columns of global entry e (its padded token count)
+  __device__ __forceinline__ int gcols(const PairItem& it, int e) const {
+    int Xg, gt;
+    global_entry(it, e, Xg, gt);
+    return (global_count(it, Xg, gt) + 15) & ~15;
+  }
+
+  // entry e (fill kv + e) is not read by this tile: release both its slots
+  __device__ bool skip(uint32_t kv, int e) const {
+    const uint32_t f = kv + e;
+    const int ks = f % C::kKSt, ts = f % C::kTSt;
+    if (!warp_wait(sm.k_full(ks), (f / C::kKSt) & 1, abort, kRoleSoftmax)) return false;
+    if (!warp_wait(sm.vt_full(ts), (f / C::kTSt) & 1, abort, kRoleSoftmax)) return false;
+    if (elect_one()) {
+      mbar_arrive(sm.k_empty(ks));
+      mbar_arrive(sm.vt_empty(ts));
+    }
+    __syncwarp();
+    return true;
+  }
+
+  // S_X = Q_X K(e)^T into TMEM; `last_s` also releases Q
+  __device__ bool issue_s(const PairItem& it, uint32_t kv, int qb, int e, bool last_s) const {
+    const uint32_t f = kv + e;
+    const int ks = f % C::kKSt;
+    const uint32_t idesc = (e < it.nU) ? idesc_s128 : idesc_bf16_f32(128, gcols(it, e), 0);
+    const uint64_t qd = qdesc0 + (2 * qb + X) * kTile16;
+    const uint64_t kd = kdesc0 + ks * kTile16;
+    const uint32_t dt = tmem + C::kColS + 128 * X;
+    if (!warp_wait(sm.k_full(ks), (f / C::kKSt) & 1, abort, kRoleSoftmax)) return false;
+    if (tr) tr->ev(22);
     tc_fence_after();
-    const int s_total = it.len[0] + it.len[1];
-    int s_done = 0;
-
-    // columns of the entry (128 for band entries, the padded global count otherwise)
-    auto ncols = [&](int X, int e) -> int {
-      if (e < it.nU) return 128;
-      int Xg, gt;
-      global_entry(it, e, Xg, gt);
-      return (global_count(it, Xg, gt) + 15) & ~15;
-    };
-
-    auto issue_s = [&](int X, int j) -> bool {
-      const int e = entry_of(it, X, j);
-      const uint32_t ke = kv + e;
-      const int ks = ke % C::kKSt;
-      if (!mbar_wait(sm.k_full(ks), (ke / C::kKSt) & 1, abort, kRoleMma)) return false;
-      tc_fence_after();
-      const int N = ncols(X, e);
-      const uint32_t idesc = idesc_bf16_f32(128, N, 0);
-      const uint32_t dt = tmem + C::kColS + 128 * X;
+    if (elect_one()) {
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t qa = sm.q(qb, X) + (kk >> 2) * 16384 + (kk & 3) * 32;
-        const uint32_t ka = sm.k(ks) + (kk >> 2) * 16384 + (kk & 3) * 32;
-        mma_bf16_ss(dt, smem_desc_sw128(qa, 16, 1024), smem_desc_sw128(ka, 16, 1024), idesc, kk > 0);
+        const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+        mma_bf16_ss(dt, qd + off, kd + off, idesc, kk > 0);
       }
       mma_commit(sm.s_full(X));
-      if (last_consumer(it, X, j)) mma_commit(sm.k_empty(ks));
-      if (++s_done == s_total) mma_commit(sm.q_empty(qb));  // Q may be replaced
-      return true;
-    };
-
-    auto issue_pv = [&](int X, int j) -> bool {
-      const int e = entry_of(it, X, j);
-      const uint32_t ve = kv + e;
-      const int vs = ve % C::kVSt;
-      if (!mbar_wait(sm.v_full(vs), (ve / C::kVSt) & 1, abort, kRoleMma)) return false;
-      if (!mbar_wait(sm.p_full(X), p_cnt[X] & 1, abort, kRoleMma)) return false;
-      ++p_cnt[X];
-      if (j == 0) {
-        if (!mbar_wait(sm.o_empty(X), (o_cnt[X] & 1) ^ 1, abort, kRoleMma)) return false;
-        ++o_cnt[X];
-      }
-      tc_fence_after();
-      // key steps of 16 that some row of tile X attends: value rows outside
-      // them (the partner tile's keys) are never read
-      int kk0 = 0, kk1 = ncols(X, e) / 16 - 1;
-      if (e < it.nU) {
-        const int kb = it.U0 + 128 * e;
-        kk0 = max(0, pick(it.klo, X) - kb) >> 4;
-        kk1 = min(127, pick(it.kend, X) - kb) >> 4;
-      }
-      const uint32_t pt = tmem + C::kColS + 128 * X;
-      const uint32_t ot = tmem + C::kColO + D * X;
-      for (int kk = kk0; kk <= kk1; ++kk) {
-        const uint32_t va = sm.v(vs) + kk * 2048;
-        mma_bf16_ts(ot, pt + kk * 8, smem_desc_sw128(va, 16384, 1024), idesc_pv, (j > 0 || kk > kk0) ? 1u : 0u);
-      }
-      if (j + 1 == pick(it.len, X)) mma_commit(sm.pv_done(X));  // O_X complete
-      if (last_consumer(it, X, j)) mma_commit(sm.v_empty(vs));
-      return true;
-    };
-
-#pragma unroll
-    for (int X = 0; X < 2; ++X)
-      if (ok && pick(it.len, X) > 0 && !issue_s(X, 0)) ok = false;
-    const int steps = max(it.len[0], it.len[1]);
-    for (int j = 0; ok && j < steps; ++j) {
-#pragma unroll
-      for (int X = 0; X < 2; ++X) {
-        const int lenX = pick(it.len, X);
-        if (!ok || j >= lenX) continue;
-        if (!issue_pv(X, j)) ok = false;
-        else if (j + 1 < lenX && !issue_s(X, j + 1)) ok = false;
-      }
+      mma_commit(sm.k_empty(ks));
+      if (last_s) mma_commit(sm.q_empty(qb));
     }
-    kv += it.nE;
+    __syncwarp();
+    if (tr) tr->ev(23);
+    return true;
   }
-  // Wait until every MMA this thread issued has finished before TMEM is freed.
-  mma_commit(sm.fin());
-  int dummy = 0;
-  mbar_wait(sm.fin(), 0, &dummy, kRoleDrain, 200000000ull);
+
+  // O_X (+)= P_X V(e); `first` starts the accumulation, `last` signals O_X complete
+  __device__ bool issue_pv(const PairItem& it, uint32_t kv, int e, bool first, bool last) const {
+    const uint32_t f = kv + e;
+    const int ts = f % C::kTSt;
+    // key steps of 16 that some row of this tile attends: value rows outside
+    // them (the partner tile's keys) are never read
+    int kk0 = 0, kk1;
+    if (e < it.nU) {
+      const int kb = it.U0 + 128 * e;
+      kk0 = max(0, pick(it.klo, X) - kb) >> 4;
+      kk1 = min(127, pick(it.kend, X) - kb) >> 4;
+    } else {
+      kk1 = gcols(it, e) / 16 - 1;
+    }
+    const bool full = kk0 == 0 && kk1 == 7;
+    const uint32_t acc0 = first ? 0u : 1u;
+    const uint32_t pt = tmem + C::kColS + 128 * X;  // P_X over the first 64 columns of S_X
+    const uint32_t ot = tmem + C::kColO + D * X;
+    // V^T: 64-key blocks of [D rows, 128 bytes]; a 16-key step is 32 bytes
+    const uint64_t vd = vdesc0 + ts * kTile16;
+    if (!warp_wait(sm.vt_full(ts), (f / C::kTSt) & 1, abort, kRoleSoftmax)) return false;
+    if (tr) tr->ev(20);
+    tc_fence_after();
+    if (elect_one()) {
+      if (full) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = ((kk >> 2) * (D * 128) + (kk & 3) * 32) >> 4;
+          mma_bf16_ts(ot, pt + kk * 8, vd + off, idesc_pv, kk > 0 ? 1u : acc0);
+        }
+      } else {
+        for (int kk = kk0; kk <= kk1; ++kk) {
+          const uint32_t off = ((kk >> 2) * (D * 128) + (kk & 3) * 32) >> 4;
+          mma_bf16_ts(ot, pt + kk * 8, vd + off, idesc_pv, kk > kk0 ? 1u : acc0);
+        }
+      }
+      if (last) mma_commit(sm.pv_done(X));  // O_X complete: the epilogue may read it
+      mma_commit(sm.vt_empty(ts));
+    }
+    __syncwarp();
+    if (tr) tr->ev(21);
+    return true;
+  }
+};
+
+// ------------------------------------------------------------------ V transposer (two warps)
+// The P.V product takes V as a K-major operand (keys contiguous), which the
+// tensor cores read at full rate from a [D, keys] layout.  TMA delivers V as
+// [keys, D]; warp w of the pair moves keys [64w, 64w + 64) of every entry
+// into 8x8 blocks of V^T with ldmatrix.trans / stmatrix, both 128-byte
+// swizzled.
+template <int D>
+__device__ void band_transposer(const BandParams& p, const BandSmem<D>& sm, int w, int lane) {
+  using C = BandCfg<D>;
+  volatile int* abort = sm.abort_flag();
+  uint32_t kv = 0;
+  bool ok = true;
+  const int m = lane >> 3, r = lane & 7;  // this lane addresses row r of matrix m
+  Tracer tr;
+  if (blockIdx.x == 0 && w == 0 && lane == 0) tr.track = 4;
+  for (int item = blockIdx.x; ok && item < p.total_items; item += gridDim.x) {
+    const PairItem it = decode_pair(p, sm.segs(), item);
+    if (it.zero) continue;
+    for (int e = 0; e < it.nE; ++e, ++kv) {
+      const int vs = kv % C::kVSt, ts = kv % C::kTSt;
+      tr.ev(40);
+      if (!warp_wait(sm.v_full(vs), (kv / C::kVSt) & 1, abort, kRoleTranspose)) { ok = false; break; }
+      tr.ev(41);
+      if (!warp_wait(sm.vt_empty(ts), ((kv / C::kTSt) & 1) ^ 1, abort, kRoleTranspose)) { ok = false; break; }
+      tr.ev(42);
+      const uint32_t src = sm.v(vs), dst = sm.vt(ts) + w * (D * 128);
+#pragma unroll
+      for (int ki = 0; ki < 8; ++ki) {
+        const int key = 64 * w + 8 * ki + r;  // source row of this lane
+#pragma unroll
+        for (int dg = 0; dg < D / 32; ++dg) {
+          const int di = 4 * dg + m;  // 8-column group of D
+          uint32_t x0, x1, x2, x3;
+          ldmatrix_x4_trans(src + (di >> 3) * 16384 + key * 128 + (((di & 7) ^ (key & 7)) << 4), x0, x1, x2, x3);
+          const int dr = 8 * di + r;  // destination row (a column of V)
+          stmatrix_x4(dst + dr * 128 + ((ki ^ (dr & 7)) << 4), x0, x1, x2, x3);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(sm.v_empty(vs));
+        mbar_arrive(sm.vt_full(ts));
+      }
+      tr.ev(43);
+    }
+  }
+  tr.done();
 }
 
 // ------------------------------------------------------------------ softmax / epilogue
@@ -501,6 +566,71 @@ __device__ __forceinline__ uint32_t bit_range(int lo, int hi) {
   return upto & ~((1u << lo) - 1u);
 }
 
+// Global entry e, chunk c: bit t set where this row attends global column
+// 32c + t (a global key already in the row's band is counted there, once).
+__device__ __forceinline__ uint32_t global_keep(const BandParams& p, const PairItem& it, int e, int c,
+                                                int m_q, bool row_valid) {
+  int gx, gt;
+  global_entry(it, e, gx, gt);
+  const int tend = max(0, min(32, global_count(it, gx, gt) - 32 * c));
+  const int i_q = it.r + it.delta * m_q;
+  uint32_t k = 0;
+#pragma unroll 1
+  for (int t = 0; t < tend; ++t) {
+    const int g = p.gidx[128 * gt + 32 * c + t];
+    const int mg = residue_coord(g, it.r, it.delta);
+    const bool in_band = (m_q - mg <= p.half) && (mg - m_q <= p.right);
+    k |= (uint32_t)((!p.causal || g <= i_q) && !in_band) << t;
+  }
+  return row_valid ? k : 0u;
+}
+
+// Maximum over the kept columns of a 32-column chunk of raw scores.
+__device__ __forceinline__ float chunk_max(const uint32_t (&x)[32], uint32_t keep, uint32_t whole) {
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  float v[32];
+  if (whole) {
+#pragma unroll
+    for (int t = 0; t < 32; ++t) v[t] = __uint_as_float(x[t]);
+  } else {
+#pragma unroll
+    for (int t = 0; t < 32; ++t) v[t] = ((keep >> t) & 1u) ? __uint_as_float(x[t]) : NEG_INF;
+  }
+  float a = max3f(v[0], v[1], v[2]), b = max3f(v[3], v[4], v[5]), c = max3f(v[6], v[7], v[8]),
+        d = max3f(v[9], v[10], v[11]);
+#pragma unroll
+  for (int t = 12; t < 28; t += 8) {
+    a = max3f(a, v[t], v[t + 1]);
+    b = max3f(b, v[t + 2], v[t + 3]);
+    c = max3f(c, v[t + 4], v[t + 5]);
+    d = max3f(d, v[t + 6], v[t + 7]);
+  }
+  return fmaxf(max3f(a, b, v[28]), max3f(c, d, max3f(v[29], v[30], v[31])));
+}
+
+// P for a 32-column chunk: p = exp2(s * sl2 - m) on the kept columns, 0
+// elsewhere, packed to bf16 pairs; returns the two partial row sums.
+__device__ __forceinline__ float2 chunk_exp(const uint32_t (&x)[32], uint32_t keep, uint32_t whole,
+                                            float sl2, float mneg, uint32_t (&pk)[16]) {
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  const float2 sc2 = make_float2(sl2, sl2), of2 = make_float2(mneg, mneg);
+  float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    float s0 = __uint_as_float(x[2 * t]), s1 = __uint_as_float(x[2 * t + 1]);
+    if (!whole) {
+      s0 = ((keep >> (2 * t)) & 1u) ? s0 : NEG_INF;
+      s1 = ((keep >> (2 * t + 1)) & 1u) ? s1 : NEG_INF;
+    }
+    const float2 y = __ffma2_rn(make_float2(s0, s1), sc2, of2);
+    const float p0 = ex2_approx(y.x), p1 = ex2_approx(y.y);
+    if (t & 1) sb = __fadd2_rn(sb, make_float2(p0, p1));
+    else sa = __fadd2_rn(sa, make_float2(p0, p1));
+    pk[t] = pack_bf16x2(p0, p1);
+  }
+  return __fadd2_rn(sa, sb);
+}
+
 // Softmax of tile X (one query row per thread; warp quarter wq of TMEM lanes).
 template <int D>
 __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_t tmem, int X,
@@ -513,11 +643,19 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
   const uint32_t tO = tmem + lane_base + C::kColO + D * X;
   const float NEG_INF = -__int_as_float(0x7f800000);
   const float sl2 = p.sl2;
-  uint32_t s_cnt = 0, pv_cnt = 0;
+  uint32_t s_cnt = 0, pv_cnt = 0, p_cnt = 0, kv = 0, q_it = 0;
   bool ok = true;
+  const bool leader = wq == 0;  // issues this tile's MMAs
+  TileIssuer<D> iss(sm, tmem, X);
+  Tracer tr;
+  if (blockIdx.x == 0 && wq == 0 && lane == 0) tr.track = X;
+#ifdef LF_TRACE
+  iss.tr = &tr;
+#endif
 
   for (int item = blockIdx.x; ok && item < p.total_items; item += gridDim.x) {
-    const PairItem it = decode_pair(p, item);
+    const PairItem it = decode_pair(p, sm.segs(), item);
+    tr.ev(0);
     const int m_q = it.m0 + 128 * X + row;
     const bool row_exists = m_q < it.n_r;
     const bool row_valid = m_q < it.Lm;
@@ -527,74 +665,85 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
       }
+      if (!it.zero) {
+        // the pair is active but this tile is not: release Q and every entry
+        if (leader) {
+          const int qb = q_it % C::kQBuf;
+          if (!warp_wait(sm.q_full(qb), (q_it / C::kQBuf) & 1, abort, kRoleSoftmax)) { ok = false; break; }
+          if (elect_one()) mbar_arrive(sm.q_empty(qb));
+          __syncwarp();
+          for (int e = 0; ok && e < it.nE; ++e) ok = iss.skip(kv, e);
+          if (!ok) break;
+        }
+        kv += it.nE;
+        ++q_it;
+      }
       continue;
     }
     const int len = pick(it.len, X), nb = pick(it.nb, X), b0 = pick(it.b0, X), gb = pick(it.gbase, X);
+    const int qb = q_it % C::kQBuf;
+    auto entry = [&](int j) { return j < nb ? b0 + j : gb + (j - nb); };
+    if (leader) {
+      // Q, the entries before this tile's first one, and S_X(0)
+      if (!warp_wait(sm.q_full(qb), (q_it / C::kQBuf) & 1, abort, kRoleSoftmax)) { ok = false; break; }
+      for (int e = 0; ok && e < entry(0); ++e) ok = iss.skip(kv, e);
+      if (!ok || !iss.issue_s(it, kv, qb, entry(0), len == 1)) { ok = false; break; }
+    }
     float m_run = NEG_INF, l_run = 0.f;
 
     for (int j = 0; j < len; ++j) {
       const bool is_band = j < nb;
-      const int e = is_band ? b0 + j : gb + (j - nb);
-      // ---- keep[c]: bit t set where this row attends column 32c + t
-      uint32_t keep[4];
+      const int e = entry(j);
+      // ---- keep c: bit t set where this row attends column 32c + t
+      uint32_t keep0, keep1, keep2, keep3;
       if (is_band) {
         const int kb = it.U0 + 128 * e;
-        int clo = m_q - p.half - kb;
+        const int clo = m_q - p.half - kb;
         int chi = min(m_q + p.right, it.Lm - 1) - kb;
         if (!row_valid) chi = clo - 1;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) keep[c] = bit_range(clo - 32 * c, chi - 32 * c);
+        keep0 = bit_range(clo, chi);
+        keep1 = bit_range(clo - 32, chi - 32);
+        keep2 = bit_range(clo - 64, chi - 64);
+        keep3 = bit_range(clo - 96, chi - 96);
       } else {
-        int gx, gt;
-        global_entry(it, e, gx, gt);
-        const int gcnt = global_count(it, gx, gt);
-        const int i_q = it.r + it.delta * m_q;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t k = 0;
-          const int tend = max(0, min(32, gcnt - 32 * c));
-#pragma unroll 1
-          for (int t = 0; t < tend; ++t) {
-            const int g = p.gidx[128 * gt + 32 * c + t];
-            const int mg = residue_coord(g, it.r, it.delta);
-            const bool in_band = (m_q - mg <= p.half) && (mg - m_q <= p.right);
-            k |= (uint32_t)((!p.causal || g <= i_q) && !in_band) << t;
-          }
-          keep[c] = row_valid ? k : 0u;
-        }
+        keep0 = global_keep(p, it, e, 0, m_q, row_valid);
+        keep1 = global_keep(p, it, e, 1, m_q, row_valid);
+        keep2 = global_keep(p, it, e, 2, m_q, row_valid);
+        keep3 = global_keep(p, it, e, 3, m_q, row_valid);
       }
       // chunks some lane of the warp needs, and chunks every lane needs whole
-      uint32_t on = 0, full = 0;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (__any_sync(0xffffffffu, keep[c] != 0u)) on |= 1u << c;
-        if (__all_sync(0xffffffffu, keep[c] == 0xffffffffu)) full |= 1u << c;
-      }
+      const uint32_t onm = (__any_sync(0xffffffffu, keep0 != 0u) ? 1u : 0u) |
+                     (__any_sync(0xffffffffu, keep1 != 0u) ? 2u : 0u) |
+                     (__any_sync(0xffffffffu, keep2 != 0u) ? 4u : 0u) |
+                     (__any_sync(0xffffffffu, keep3 != 0u) ? 8u : 0u);
+      const uint32_t fullm = (__all_sync(0xffffffffu, keep0 == ~0u) ? 1u : 0u) |
+                             (__all_sync(0xffffffffu, keep1 == ~0u) ? 2u : 0u) |
+                             (__all_sync(0xffffffffu, keep2 == ~0u) ? 4u : 0u) |
+                             (__all_sync(0xffffffffu, keep3 == ~0u) ? 8u : 0u);
 
       // S_X(j) complete; it was issued after P_X(j-1).V, so that is complete too
+      tr.ev(1);
       if (!warp_wait(sm.s_full(X), s_cnt & 1, abort, kRoleSoftmax)) { ok = false; break; }
+      tr.ev(2);
       ++s_cnt;
       tc_fence_after();
-      uint32_t sr[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32_nw(tS + 32 * c, sr + 32 * c);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < 4; ++c) reg_fence32(sr + 32 * c);
-      float* s = reinterpret_cast<float*>(sr);
 
-      // ---- masks, and the maximum of the raw scores (the scale is positive)
+      // ---- pass 1: row maximum of the raw scores (the scale is positive),
+      // one 32-column chunk at a time (TMEM reads are cheap; the loop body
+      // stays small for the instruction cache)
       float mx = NEG_INF;
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < 4; ++c) {
-        if (!(full & (1u << c))) {
-#pragma unroll
-          for (int t = 0; t < 32; ++t) s[32 * c + t] = ((keep[c] >> t) & 1u) ? s[32 * c + t] : NEG_INF;
-        }
-#pragma unroll
-        for (int t = 0; t < 32; t += 2) mx = max3f(mx, s[32 * c + t], s[32 * c + t + 1]);
+        if (!((onm >> c) & 1u)) continue;
+        uint32_t x[32];
+        tmem_ld32_nw(tS + 32 * c, x);
+        tmem_wait_ld();
+        reg_fence32(x);
+        const uint32_t kc = c == 0 ? keep0 : c == 1 ? keep1 : c == 2 ? keep2 : keep3;
+        mx = fmaxf(mx, chunk_max(x, kc, (fullm >> c) & 1u));
       }
       const float mt = mx * sl2;
+      tr.ev(3);
       float alpha = 1.f;
       bool resc = false;
       if (mt > m_run + kLazy) {
@@ -618,21 +767,20 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
           tmem_st16_nw(tO + 32 * c + 16, o + 16);
         }
       }
-      // ---- P = exp2(s * scale - m) chunk by chunk into TMEM, row sum
+      // ---- pass 2: P = exp2(s * scale - m) chunk by chunk; P chunk c goes to
+      // columns [16c, 16c + 16) of S_X, whose scores (chunk c/2) are already read
       const float mneg = (m_run == NEG_INF) ? 0.f : -m_run;
       float2 sum2 = make_float2(0.f, 0.f);
-      const float2 sc2 = make_float2(sl2, sl2), of2 = make_float2(mneg, mneg);
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
-        if (on & (1u << c)) {
-#pragma unroll
-          for (int t = 0; t < 16; ++t) {
-            const float2 x = __ffma2_rn(make_float2(s[32 * c + 2 * t], s[32 * c + 2 * t + 1]), sc2, of2);
-            const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-            sum2 = __fadd2_rn(sum2, make_float2(p0, p1));
-            pk[t] = pack_bf16x2(p0, p1);
-          }
+        if ((onm >> c) & 1u) {
+          uint32_t x[32];
+          tmem_ld32_nw(tS + 32 * c, x);
+          tmem_wait_ld();
+          reg_fence32(x);
+          const uint32_t kc = c == 0 ? keep0 : c == 1 ? keep1 : c == 2 ? keep2 : keep3;
+          sum2 = __fadd2_rn(sum2, chunk_exp(x, kc, (fullm >> c) & 1u, sl2, mneg, pk));
         } else {
 #pragma unroll
           for (int t = 0; t < 16; ++t) pk[t] = 0u;
@@ -644,11 +792,31 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(sm.p_full(X));
+      tr.ev(4);
+      if (leader) {
+        // all four warps have written P_X(j) (a bounded wait, never bar.sync:
+        // a warp that gave up must not leave the others blocked)
+        if (!warp_wait(sm.p_full(X), p_cnt & 1, abort, kRoleSoftmax)) { ok = false; break; }
+        tr.ev(9);
+        ++p_cnt;
+        tc_fence_after();
+        if (!iss.issue_pv(it, kv, e, j == 0, j + 1 == len)) { ok = false; break; }
+        // S_X(j+1) overwrites P_X(j): issued after the P.V that reads it
+        const int e_next = (j + 1 < len) ? entry(j + 1) : it.nE;
+        for (int e2 = e + 1; ok && e2 < e_next; ++e2) ok = iss.skip(kv, e2);
+        if (!ok) break;
+        if (j + 1 < len && !iss.issue_s(it, kv, qb, e_next, j + 2 == len)) { ok = false; break; }
+        tr.ev(8);
+      }
     }
     if (!ok) break;
+    kv += it.nE;
+    ++q_it;
 
     // ---- epilogue: O / l -> bf16 (32 columns at a time) -> global
+    tr.ev(5);
     if (!warp_wait(sm.pv_done(X), pv_cnt & 1, abort, kRoleSoftmax)) { ok = false; break; }
+    tr.ev(6);
     ++pv_cnt;
     tc_fence_after();
     const float inv = (row_valid && l_run > 0.f) ? 1.0f / l_run : 0.f;
@@ -664,8 +832,6 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
       for (int t = 0; t < 16; ++t) ob[16 * c + t] = pack_bf16x2(of[2 * t] * inv, of[2 * t + 1] * inv);
     }
     tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(sm.o_empty(X));
     if (row_exists) {
       uint4* orow = reinterpret_cast<uint4*>(p.out + ((size_t)it.bh * p.n + it.r + (size_t)it.delta * m_q) * D);
       // padded rows (inv = 0) are written as zeros; O is finite there since
@@ -675,11 +841,21 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
         orow[c] = row_valid ? make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3])
                             : make_uint4(0, 0, 0, 0);
     }
+    tr.ev(7);
+  }
+  tr.done();
+  if (leader) {
+    // every MMA this tile issued must finish before TMEM is freed
+    if (elect_one()) mma_commit(sm.fin());
+    __syncwarp();
+    int dummy = 0;
+    mbar_wait(sm.fin(), 0, &dummy, kRoleDrain, 200000000ull);
+    __syncwarp();
   }
 }
 
-// Three warpgroups: two of softmax warps, one holding the producer warp, the
-// MMA warp and two idle warps.  Launched at 168 registers per thread
+// Three warpgroups: the MMA, producer and two transposer warps, then two of
+// softmax warps.  Launched at 168 registers per thread
 // (384 x 168 = 64512 of the SM's 65536), the third warpgroup gives registers
 // back (setmaxnreg.dec to kRegsOther) and the softmax warpgroups take them
 // (setmaxnreg.inc to kRegsSoftmax): 256 x 200 + 128 x 96 = 63488 <= 64512.
@@ -704,27 +880,31 @@ __global__ void __launch_bounds__(kBandThreads, 1) band_tc_kernel(const __grid_c
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(sm.q_full(b), 1);
-      mbar_init(sm.q_empty(b), 1);
+      mbar_init(sm.q_empty(b), 2);   // one arrival per tile
+    }
+    for (int s = 0; s < 8; ++s) {
+      mbar_init(sm.k_full(s), 1);
+      mbar_init(sm.k_empty(s), 2);   // one arrival per tile
     }
     for (int s = 0; s < 4; ++s) {
-      mbar_init(sm.k_full(s), 1);
-      mbar_init(sm.k_empty(s), 1);
       mbar_init(sm.v_full(s), 1);
-      mbar_init(sm.v_empty(s), 1);
+      mbar_init(sm.v_empty(s), 2);   // both transposer warps
+      mbar_init(sm.vt_full(s), 2);   // both transposer warps
+      mbar_init(sm.vt_empty(s), 2);  // one arrival per tile
     }
     mbar_init(sm.v_land(), 1);
     for (int X = 0; X < 2; ++X) {
       mbar_init(sm.s_full(X), 1);
-      mbar_init(sm.p_full(X), 4);
+      mbar_init(sm.p_full(X), 4);   // the tile's four softmax warps
       mbar_init(sm.pv_done(X), 1);
-      mbar_init(sm.o_empty(X), 4);
     }
-    mbar_init(sm.fin(), 1);
+    mbar_init(sm.fin(), 2);  // one commit per tile's issuing lane
     *sm.abort_flag() = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
   }
-  if (warp == 9) {
+  for (int i = threadIdx.x; i < p.nseg; i += blockDim.x) sm.segs()[i] = p.seg[i];
+  if (warp == 0) {
     tmem_alloc(smem_u32(sm.tmem_holder()), C::kTmemCols);
     tmem_relinquish();
   }
@@ -733,22 +913,25 @@ __global__ void __launch_bounds__(kBandThreads, 1) band_tc_kernel(const __grid_c
   tc_fence_after();
   const uint32_t tmem = *sm.tmem_holder();
 
-  if (warp < 8) {
+  if (warp >= 4) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-    band_softmax<D>(p, sm, tmem, warp >> 2, warp & 3, lane);
+    band_softmax<D>(p, sm, tmem, (warp >> 2) - 1, warp & 3, lane);
   } else {
+    // the issuing warps are the oldest of the CTA: the schedulers favour them
+    // over the busy softmax warps that share their sub-partitions
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
-    if (warp == 8) {
-      band_producer<D>(p, sm, lane);
-    } else if (warp == 9) {
-      if (lane == 0) band_mma<D>(p, sm, tmem);
-      __syncwarp();
+    if (warp == 0) {
+      band_producer<D, true>(p, sm, lane);
+    } else if (warp == 1) {
+      band_producer<D, false>(p, sm, lane);
+    } else {
+      band_transposer<D>(p, sm, warp - 2, lane);
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }

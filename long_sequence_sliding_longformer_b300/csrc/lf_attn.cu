@@ -650,6 +650,17 @@ lf_status lf_device_error(uint32_t* code, int32_t clear) {
   return LF_OK;
 }
 
+#ifdef LF_TRACE
+// Diagnostic builds only: copies the band kernel's timeline (first CTA) to
+// host arrays dst[8][4096] and counts[8].
+int lf_trace_dump(unsigned long long* dst, int* counts) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+  if (cudaMemcpyFromSymbol(dst, lf::g_trace, sizeof(lf::g_trace)) != cudaSuccess) return -1;
+  if (cudaMemcpyFromSymbol(counts, lf::g_trace_n, sizeof(lf::g_trace_n)) != cudaSuccess) return -1;
+  return 0;
+}
+#endif
+
 }  // extern "C"
 
 // The allocation-free variant of lf_attn_fwd (same translation unit).

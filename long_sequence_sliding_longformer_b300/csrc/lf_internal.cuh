@@ -17,15 +17,25 @@ namespace lf {
 
 // ----------------------------------------------------------------- limits
 constexpr int kMaxSets = 8;      // (dilation, residue) tensor-map sets per band launch
-constexpr int kMaxSeg = 128;     // (head, residue) segments per band launch
+constexpr int kMaxSeg = 32;      // (head, residue) segments per band launch (copied to shared memory)
 constexpr int kMaxBatch = 256;   // batch rows per launch (larger B is split on the host)
 constexpr int kMaxGlobal = LF_MAX_GLOBAL;
 
 // ----------------------------------------------------------------- error word
 // Bits 0-7: lf_status of the failure; bits 8-15: role that gave up.
-enum Role : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleDrain = 4 };
+enum Role : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleDrain = 4, kRoleTranspose = 5 };
 // Defined once here: the library is built as a single translation unit.
 __device__ uint32_t g_device_error = 0;
+
+// ----------------------------------------------------------------- timeline trace
+// Built only with -DLF_TRACE (a diagnostic build, never the product): the
+// first CTA of the band kernel records (SM clock << 8 | event code) per
+// role into g_trace[track], read back with lf_trace_dump().
+#ifdef LF_TRACE
+constexpr int kTraceTracks = 8, kTraceLen = 4096;
+__device__ unsigned long long g_trace[kTraceTracks][kTraceLen];
+__device__ int g_trace_n[kTraceTracks];
+#endif
 
 // ----------------------------------------------------------------- band kernel params
 // A segment is one (head, residue class) of the dilated window: rows
@@ -97,6 +107,24 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+#ifdef LF_TRACE
+struct Tracer {
+  int track = -1, n = 0;
+  __device__ void ev(int code) {
+    if (track >= 0 && n < kTraceLen) g_trace[track][n++] = ((unsigned long long)clock64() << 8) | (unsigned)code;
+  }
+  __device__ void done() {
+    if (track >= 0) g_trace_n[track] = n;
+  }
+};
+#else
+struct Tracer {
+  int track = -1;
+  __device__ __forceinline__ void ev(int) {}
+  __device__ __forceinline__ void done() {}
+};
+#endif
+
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
@@ -110,14 +138,20 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+// Tests the phase; if it is not complete the thread may sleep until it
+// completes or about `hint_ns` pass (so waiting warps do not spin on the
+// issue slots of working ones).
+#ifndef LF_EXP_HINT
+#define LF_EXP_HINT 20000
+#endif
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t hint_ns = LF_EXP_HINT) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
@@ -317,6 +351,34 @@ __device__ __forceinline__ void tmem_st16_nw(uint32_t taddr, const uint32_t* r) 
 
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// One lane of the (fully active) warp is elected; the others get false.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+// Four 8x8 b16 matrices, transposed on the way into registers (row addresses
+// from lanes 8i..8i+7 for matrix i).
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& x0, uint32_t& x1,
+                                                  uint32_t& x2, uint32_t& x3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void stmatrix_x4(uint32_t addr, uint32_t x0, uint32_t x1, uint32_t x2,
+                                            uint32_t x3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+               "r"(x0), "r"(x1), "r"(x2), "r"(x3)
+               : "memory");
 }
 
 __device__ __forceinline__ float max3f(float a, float b, float c) {
