@@ -65,7 +65,7 @@ struct BandCfg {
   static constexpr int kNumBar = 2 + 2 + 8 + 8 + 4 + 4 + 1 + 2 + 2 + 2 + 2 + 2 + 1 + 4 + 4;
   static_assert(kKSt <= 8 && kVSt <= 4 && kTSt <= 4 && kQBuf <= 2, "barrier arrays");
   static constexpr int kOffMisc = kOffBar + kNumBar * 8;
-  static constexpr int kSmem = kOffMisc + 16 + kMaxSeg * (int)sizeof(BandSeg) + 1024;  // + slack to align the base to 1024
+  static constexpr int kSmem = kOffMisc + 16 + kMaxSeg * (int)sizeof(BandSeg) + 32 + 1024;  // + slack to align the base to 1024
   static constexpr int kTmemCols = 512;
   static constexpr uint32_t kColS = 0;     // S_X at 128*X
   static constexpr uint32_t kColO = 256;   // O_X at 256 + D*X
@@ -416,29 +416,49 @@ struct TileIssuer {
     return (global_count(it, Xg, gt) + 15) & ~15;
   }
 
-  // entry e (fill kv + e) is not read by this tile: release both its slots
-  __device__ bool skip(uint32_t kv, int e) const {
+  // Entry e (fill kv + e) is not read by this tile: release its K slot
+  // (skip_k) and its V^T slot (skip_v).  A tile must not wait for a V^T fill
+  // it skips before issuing the P.V of its own earlier entries: with a
+  // shallow ring that fill may need the very slot the P.V still holds.
+  __device__ bool skip_k(uint32_t kv, int e) const {
     const uint32_t f = kv + e;
-    const int ks = f % C::kKSt, ts = f % C::kTSt;
+    const int ks = f % C::kKSt;
     if (!warp_wait(sm.k_full(ks), (f / C::kKSt) & 1, abort, kRoleSoftmax)) return false;
-    if (!warp_wait(sm.vt_full(ts), (f / C::kTSt) & 1, abort, kRoleSoftmax)) return false;
-    if (elect_one()) {
-      mbar_arrive(sm.k_empty(ks));
-      mbar_arrive(sm.vt_empty(ts));
-    }
+    if (elect_one()) mbar_arrive(sm.k_empty(ks));
     __syncwarp();
     return true;
   }
+  __device__ bool skip_v(uint32_t kv, int e) const {
+    const uint32_t f = kv + e;
+    const int ts = f % C::kTSt;
+    if (!warp_wait(sm.vt_full(ts), (f / C::kTSt) & 1, abort, kRoleSoftmax)) return false;
+    if (elect_one()) mbar_arrive(sm.vt_empty(ts));
+    __syncwarp();
+    return true;
+  }
+  __device__ bool skip(uint32_t kv, int e) const { return skip_k(kv, e) && skip_v(kv, e); }
 
-  // S_X = Q_X K(e)^T into TMEM; `last_s` also releases Q
-  __device__ bool issue_s(const PairItem& it, uint32_t kv, int qb, int e, bool last_s) const {
+  // K(e) has landed
+  __device__ bool wait_k(uint32_t kv, int e) const {
+    const uint32_t f = kv + e;
+    return warp_wait(sm.k_full(f % C::kKSt), (f / C::kKSt) & 1, abort, kRoleSoftmax);
+  }
+  // V^T(e) is ready
+  __device__ bool wait_v(uint32_t kv, int e) const {
+    const uint32_t f = kv + e;
+    return warp_wait(sm.vt_full(f % C::kTSt), (f / C::kTSt) & 1, abort, kRoleSoftmax);
+  }
+
+  // S_X = Q_X K(e)^T into TMEM (K(e) already waited for); `last_s` also releases Q
+  __device__ bool issue_s(const PairItem& it, uint32_t kv, int qb, int e, bool last_s,
+                          bool waited = false) const {
     const uint32_t f = kv + e;
     const int ks = f % C::kKSt;
     const uint32_t idesc = (e < it.nU) ? idesc_s128 : idesc_bf16_f32(128, gcols(it, e), 0);
     const uint64_t qd = qdesc0 + (2 * qb + X) * kTile16;
     const uint64_t kd = kdesc0 + ks * kTile16;
     const uint32_t dt = tmem + C::kColS + 128 * X;
-    if (!warp_wait(sm.k_full(ks), (f / C::kKSt) & 1, abort, kRoleSoftmax)) return false;
+    if (!waited && !wait_k(kv, e)) return false;
     if (tr) tr->ev(22);
     tc_fence_after();
     if (elect_one()) {
@@ -457,7 +477,8 @@ struct TileIssuer {
   }
 
   // O_X (+)= P_X V(e); `first` starts the accumulation, `last` signals O_X complete
-  __device__ bool issue_pv(const PairItem& it, uint32_t kv, int e, bool first, bool last) const {
+  __device__ bool issue_pv(const PairItem& it, uint32_t kv, int e, bool first, bool last,
+                           bool waited = false) const {
     const uint32_t f = kv + e;
     const int ts = f % C::kTSt;
     // key steps of 16 that some row of this tile attends: value rows outside
@@ -476,7 +497,7 @@ struct TileIssuer {
     const uint32_t ot = tmem + C::kColO + D * X;
     // V^T: 64-key blocks of [D rows, 128 bytes]; a 16-key step is 32 bytes
     const uint64_t vd = vdesc0 + ts * kTile16;
-    if (!warp_wait(sm.vt_full(ts), (f / C::kTSt) & 1, abort, kRoleSoftmax)) return false;
+    if (!waited && !wait_v(kv, e)) return false;
     if (tr) tr->ev(20);
     tc_fence_after();
     if (elect_one()) {
@@ -794,18 +815,23 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
       if (lane == 0) mbar_arrive(sm.p_full(X));
       tr.ev(4);
       if (leader) {
-        // all four warps have written P_X(j) (a bounded wait, never bar.sync:
-        // a warp that gave up must not leave the others blocked)
-        if (!warp_wait(sm.p_full(X), p_cnt & 1, abort, kRoleSoftmax)) { ok = false; break; }
+        // While the other warps finish: the operands of this step's products,
+        // and the entries this tile passes over.  Then all four warps have
+        // written P_X(j) (a bounded wait, never bar.sync: a warp that gave up
+        // must not leave the others blocked).
+        const int e_next = (j + 1 < len) ? entry(j + 1) : it.nE;
+        ok = iss.wait_v(kv, e);
+        for (int e2 = e + 1; ok && e2 < e_next; ++e2) ok = iss.skip_k(kv, e2);
+        if (ok && j + 1 < len) ok = iss.wait_k(kv, e_next);
+        if (!ok || !warp_wait(sm.p_full(X), p_cnt & 1, abort, kRoleSoftmax)) { ok = false; break; }
         tr.ev(9);
         ++p_cnt;
         tc_fence_after();
-        if (!iss.issue_pv(it, kv, e, j == 0, j + 1 == len)) { ok = false; break; }
-        // S_X(j+1) overwrites P_X(j): issued after the P.V that reads it
-        const int e_next = (j + 1 < len) ? entry(j + 1) : it.nE;
-        for (int e2 = e + 1; ok && e2 < e_next; ++e2) ok = iss.skip(kv, e2);
+        if (!iss.issue_pv(it, kv, e, j == 0, j + 1 == len, true)) { ok = false; break; }
+        for (int e2 = e + 1; ok && e2 < e_next; ++e2) ok = iss.skip_v(kv, e2);
         if (!ok) break;
-        if (j + 1 < len && !iss.issue_s(it, kv, qb, e_next, j + 2 == len)) { ok = false; break; }
+        // S_X(j+1) overwrites P_X(j): issued after the P.V that reads it
+        if (j + 1 < len && !iss.issue_s(it, kv, qb, e_next, j + 2 == len, true)) { ok = false; break; }
         tr.ev(8);
       }
     }
@@ -900,6 +926,7 @@ __global__ void __launch_bounds__(kBandThreads, 1) band_tc_kernel(const __grid_c
     }
     mbar_init(sm.fin(), 2);  // one commit per tile's issuing lane
     *sm.abort_flag() = 0;
+    for (int i = 0; i < 8; ++i) reinterpret_cast<volatile int*>(sm.segs() + kMaxSeg)[i] = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
   }

@@ -354,11 +354,18 @@ global_partial_stream_kernel(const __grid_constant__ PatternParams p,
   }
 }
 
+// kMergeGroups groups of 128 threads (thread = output column) split the
+// chunks round-robin; each keeps its own running sums, and the groups are
+// added in a fixed order at the end (deterministic).  The chunk loop keeps
+// four independent loads in flight: the kernel is latency-bound.
+constexpr int kMergeGroups = 4;
+
 template <typename T>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(128 * kMergeGroups)
 global_merge_kernel(const __grid_constant__ PatternParams p, const float* __restrict__ ws,
                     T* __restrict__ out, int nchunks) {
-  __shared__ float red_m[4];
+  __shared__ float red_m[4 * kMergeGroups];
+  __shared__ float part_l[kMergeGroups], part_a[kMergeGroups][128];
   const int g = blockIdx.x;
   const int64_t bh = blockIdx.y;
   const int b = (int)(bh / p.H);
@@ -367,35 +374,63 @@ global_merge_kernel(const __grid_constant__ PatternParams p, const float* __rest
   const int pos = p.gidx[g];
   const float NEG_INF = -__int_as_float(0x7f800000);
   T* orow = out + (bh * p.n + pos) * D;
-  const int c = threadIdx.x;
+  const int tid = threadIdx.x, c = tid & 127, grp = tid >> 7;
   const float* base = ws + ((bh * nchunks) * p.G + g) * (D + 2);
   const int64_t cstride = (int64_t)p.G * (D + 2);
   // maximum over the chunks, all threads at once
   float M = NEG_INF;
-  for (int ch = c; ch < nchunks; ch += 128) M = fmaxf(M, base[ch * cstride]);
+  for (int ch = tid; ch < nchunks; ch += 128 * kMergeGroups) M = fmaxf(M, base[ch * cstride]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if ((c & 31) == 0) red_m[c >> 5] = M;
+  if ((tid & 31) == 0) red_m[tid >> 5] = M;
   __syncthreads();
-  M = fmaxf(fmaxf(red_m[0], red_m[1]), fmaxf(red_m[2], red_m[3]));
-  if (c >= D) return;
-  if (pos >= L) {
-    from_f<T>(orow + c, 0.f);
-    return;
-  }
+  M = red_m[0];
+#pragma unroll
+  for (int w = 1; w < 4 * kMergeGroups; ++w) M = fmaxf(M, red_m[w]);
   float l = 0.f, a = 0.f;
-  if (M != NEG_INF) {
-#pragma unroll 4
-    for (int ch = 0; ch < nchunks; ++ch) {
-      const float* e = base + ch * cstride;
+  if (M != NEG_INF && c < D) {
+    int ch = grp;
+    for (; ch + 3 * kMergeGroups < nchunks; ch += 4 * kMergeGroups) {
+      float me[4], le[4], ae[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float* e = base + (int64_t)(ch + u * kMergeGroups) * cstride;
+        me[u] = e[0];
+        le[u] = e[1];
+        ae[u] = e[2 + c];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (me[u] == NEG_INF) continue;  // nothing attended in this chunk: skip, never scale by 0
+        const float f = ex2_approx(me[u] - M);
+        l = fmaf(le[u], f, l);
+        a = fmaf(ae[u], f, a);
+      }
+    }
+    for (; ch < nchunks; ch += kMergeGroups) {
+      const float* e = base + (int64_t)ch * cstride;
       const float me = e[0];
-      if (me == NEG_INF) continue;  // nothing attended in this chunk: skip, never scale by 0
+      if (me == NEG_INF) continue;
       const float f = ex2_approx(me - M);
       l = fmaf(e[1], f, l);
       a = fmaf(e[2 + c], f, a);
     }
   }
-  from_f<T>(orow + c, l > 0.f ? a / l : 0.f);
+  part_a[grp][c] = a;
+  if (c == 0) part_l[grp] = l;
+  __syncthreads();
+  if (grp != 0 || c >= D) return;
+  if (pos >= L) {
+    from_f<T>(orow + c, 0.f);
+    return;
+  }
+  float lt = part_l[0], at = part_a[0][c];
+#pragma unroll
+  for (int q = 1; q < kMergeGroups; ++q) {
+    lt += part_l[q];
+    at += part_a[q][c];
+  }
+  from_f<T>(orow + c, lt > 0.f ? at / lt : 0.f);
 }
 
 // Query-block size of the streaming kernel for a given number of global tokens.
@@ -456,7 +491,7 @@ template <typename T>
 lf_status launch_global_merge(const PatternParams& p, const float* ws, T* out, int nchunks,
                               cudaStream_t s) {
   dim3 g2(p.G, (unsigned)((int64_t)p.B * p.H));
-  global_merge_kernel<T><<<g2, 128, 0, s>>>(p, ws, out, nchunks);
+  global_merge_kernel<T><<<g2, 128 * kMergeGroups, 0, s>>>(p, ws, out, nchunks);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("global merge kernel launch: %s", cudaGetErrorString(e));
