@@ -1,4 +1,5 @@
-// band_tc.cuh -- bf16 band-attention kernel on the sm_103a tensor cores.
+// band_pair.cuh -- bf16 band-attention kernel for D = 128 on the sm_103a tensor
+// cores: two 128-row query tiles per CTA sharing their key/value entries.
 //
 // Computes the sliding / dilated / causal window part of Longformer attention
 // (velog.io/@lainshower/Longformer, section 3-1 "Sliding Window", "Dilated
@@ -47,6 +48,7 @@
 #include "lf_internal.cuh"
 
 namespace lf {
+namespace pairk {
 
 template <int D>
 struct BandCfg {
@@ -1000,11 +1002,8 @@ static lf_status launch_band_tc_d(const BandParams& p, int grid, cudaStream_t s)
   return LF_OK;
 }
 
-lf_status launch_band_tc(const BandParams& p, int d, int grid, cudaStream_t s) {
-  if (d == 64) return launch_band_tc_d<64>(p, grid, s);
-  if (d == 128) return launch_band_tc_d<128>(p, grid, s);
-  set_error("band kernel: unsupported head dimension %d", d);
-  return LF_ERR_UNSUPPORTED;
-}
+// D = 128 only (D = 64 runs the ring kernel of band_ring.cuh).
+inline lf_status launch(const BandParams& p, int grid, cudaStream_t s) { return launch_band_tc_d<128>(p, grid, s); }
 
+}  // namespace pairk
 }  // namespace lf

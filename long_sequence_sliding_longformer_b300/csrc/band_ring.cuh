@@ -1,0 +1,898 @@
+// band_ring.cuh -- bf16 band-attention kernel for D = 64 on the sm_103a tensor
+// cores: one 128-row query tile per CTA, two CTAs per SM, S computed ahead
+// into a ring of TMEM buffers.
+//
+// Computes the sliding / dilated / causal window part of Longformer attention
+// (velog.io/@lainshower/Longformer, section 3-1 "Sliding Window", "Dilated
+// Sliding Window", section 4.1 for the look-back-only pattern) plus the
+// global tokens' key columns ("Global Attention"), for every row.  Rows of
+// global tokens are overwritten afterwards by the global-row kernels.
+//
+// Dilation is handled by residue classes: with dilation delta, row
+// i = r + delta*m only ever attends rows of the same residue r, and in the
+// coordinate m the window is a plain band of half steps back and `right`
+// steps ahead.  A TMA tensor map whose row stride is delta rows presents a
+// residue class as a dense matrix.
+//
+// Work item: one 128-row query tile of one (batch, head, residue).  It streams
+// the kE-key "entries" that intersect the tile's windows, then the gathered
+// keys of the global tokens, and accumulates O = softmax(S) V online.
+//
+// Persistent CTAs (two per SM for D = 64, one for D = 128), 8 warps each:
+//   warp 0     allocates TMEM; issues every tcgen05.mma (one elected lane):
+//              S = Q K^T for up to kSBuf entries ahead into a ring of TMEM
+//              buffers, and O += P V once the softmax has written P
+//   warp 1     Q/K producer: TMA loads of Q and of the K entries
+//   warp 2     V producer: TMA loads of the V entries (the global tokens'
+//              K/V rows are gathered by the producers with plain loads)
+//   warp 3     transposes each V entry into V^T, the K-major layout the P.V
+//              product reads at full rate
+//   warps 4-7  softmax and epilogue: one query row per thread; S rows are read
+//              from TMEM, masked, turned into P = exp2(S*scale - m) with a
+//              lazily updated row maximum, and P (bf16) is written back over
+//              the S buffer it came from
+// Because S is computed ahead into a ring of buffers, the softmax warps do not
+// wait for the tensor cores between entries, and the products of one entry
+// run while the softmax works on the next.
+//
+// TMEM: S buffers b = 0..kSBuf-1 at kE*b (P over their first kE/2 columns,
+// two bf16 per column), then O (D columns).  The MMA warp issues the S of
+// entry g + kSBuf into buffer g % kSBuf after the P.V of entry g that reads it
+// (one thread's MMAs execute in order).
+//
+// Every wait is bounded; a timeout sets the device error word and all roles
+// leave their loops, drain their in-flight copies and free TMEM.
+#pragma once
+
+#include "lf_internal.cuh"
+
+namespace lf {
+namespace ringk {
+
+// D = 64: two CTAs per SM (so that two softmax warps share each SM
+// sub-partition and hide each other's latencies), 64-key entries, 256 TMEM
+// columns each.  D = 128: one CTA per SM, 128-key entries, all 512 columns.
+template <int D>
+struct BandCfg {
+  static constexpr int kE = (D == 64) ? 64 : 128;   // keys per entry
+  static constexpr int kCtaPerSm = (D == 64) ? 2 : 1;
+  static constexpr int kQBuf = 2;                  // Q tiles (the next item's Q loads early)
+  static constexpr int kKSt = (D == 64) ? 3 : 2;   // K slots
+  static constexpr int kVSt = (D == 64) ? 2 : 1;   // V slots (as loaded: [keys, D])
+  static constexpr int kTSt = (D == 64) ? 4 : 2;   // V^T slots ([D, keys], the P.V operand)
+  static constexpr int kSBuf = 3;                  // S buffers in TMEM
+  static constexpr int kTileQ = 128 * D * 2;       // bytes of one [128, D] bf16 query tile
+  static constexpr int kTile = kE * D * 2;         // bytes of one [kE, D] key/value tile
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kQBuf * kTileQ;
+  static constexpr int kOffV = kOffK + kKSt * kTile;
+  static constexpr int kOffVT = kOffV + kVSt * kTile;
+  static constexpr int kOffBar = kOffVT + kTSt * kTile;
+  // q_full[2], q_empty[2], k_full[4], k_empty[4], v_full[4], v_empty[4],
+  // vt_full[4], vt_empty[4], v_land, s_full[3], p_full[3], pv_done[0], o_empty, fin, pv_done[1]
+  static constexpr int kNumBar = 2 + 2 + 4 * 6 + 1 + 3 + 3 + 1 + 1 + 1 + 1;
+  static_assert(kKSt <= 4 && kVSt <= 4 && kTSt <= 4 && kQBuf <= 2 && kSBuf <= 3, "barrier arrays");
+  static constexpr int kOffMisc = kOffBar + kNumBar * 8;
+  static constexpr int kSmem = kOffMisc + 16 + kMaxSeg * (int)sizeof(BandSeg) + 1024;  // + slack to align the base
+  static constexpr int kTmemCols = (D == 64) ? 256 : 512;
+  static constexpr uint32_t kColO = kSBuf * kE;     // S buffers at kE * b, then O (D columns)
+  static_assert(kColO + D <= kTmemCols, "TMEM budget");
+  static_assert(kCtaPerSm == 1 || 2 * (kSmem + 1024) <= 233472, "two CTAs per SM must fit");
+};
+
+// Everything the roles need to know about one work item.  Computed the same
+// way by every role from the item number alone.
+struct TileItem {
+  int b, h, r, delta, n_r, set, m0, Lb, Lm, bh;
+  bool act;     // the tile has at least one valid row
+  int U0, nU;   // band entries: keys (m coordinate) [U0 + kE*e, U0 + kE*e + kE), e < nU
+  int klo, khi; // first and last key any row of the tile attends in the band
+  int gcnt;     // global tokens visible to the tile (a prefix of the sorted list)
+  int nE;       // entries: nU band entries, then ceil(gcnt / kE) global entries
+};
+
+__device__ __forceinline__ int upper_bound_gidx(const BandParams& p, int lim) {
+  // number of global positions <= lim (gidx is strictly increasing)
+  int lo = 0, hi = p.G;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (p.gidx[mid] <= lim) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+// `segs`: the launch's segment table, copied to shared memory at kernel start
+// (a search over the kernel parameters would miss the constant cache).
+template <int kE>
+__device__ __forceinline__ TileItem decode_tile(const BandParams& p, const BandSeg* segs, int item) {
+  TileItem it;
+  it.b = item / p.items_per_b;
+  const int rem = item - it.b * p.items_per_b;
+  int lo = 0, hi = p.nseg - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (segs[mid].begin <= rem) lo = mid; else hi = mid - 1;
+  }
+  const BandSeg sg = segs[lo];
+  it.h = sg.h;
+  it.r = sg.r;
+  it.delta = sg.delta;
+  it.n_r = sg.n_r;
+  it.set = sg.set;
+  it.m0 = (rem - sg.begin) * 128;
+  it.bh = it.b * p.H + it.h;
+  it.Lb = p.n - p.pad[it.b];
+  const int Lm = (it.Lb > it.r) ? (it.Lb - it.r + it.delta - 1) / it.delta : 0;
+  it.Lm = min(Lm, it.n_r);
+  it.act = it.m0 < it.Lm;
+  if (!it.act) {
+    it.nE = it.nU = it.gcnt = 0;
+    it.U0 = it.klo = it.khi = 0;
+    return it;
+  }
+  const int qlast = min(it.m0 + 127, it.Lm - 1);
+  it.klo = max(0, it.m0 - p.half);
+  it.khi = min(it.Lm - 1, qlast + p.right);
+  it.U0 = it.klo;
+  it.nU = (it.khi - it.klo) / kE + 1;
+  int glim = it.Lb - 1;
+  if (p.causal) glim = min(glim, it.r + it.delta * qlast);
+  it.gcnt = (p.G > 0) ? upper_bound_gidx(p, glim) : 0;
+  it.nE = it.nU + (it.gcnt + kE - 1) / kE;
+  return it;
+}
+
+// tokens held by global entry e (>= nU)
+template <int kE>
+__device__ __forceinline__ int global_count(const TileItem& it, int e) {
+  return min(kE, it.gcnt - kE * (e - it.nU));
+}
+
+template <int D>
+struct BandSmem {
+  using C = BandCfg<D>;
+  uint8_t* base;
+  uint32_t sbase;
+  __device__ __forceinline__ uint32_t q(int qb) const { return sbase + C::kOffQ + qb * C::kTileQ; }
+  __device__ __forceinline__ uint32_t k(int s) const { return sbase + C::kOffK + s * C::kTile; }
+  __device__ __forceinline__ uint32_t v(int s) const { return sbase + C::kOffV + s * C::kTile; }
+  __device__ __forceinline__ uint32_t vt(int s) const { return sbase + C::kOffVT + s * C::kTile; }
+  __device__ __forceinline__ uint8_t* k_ptr(int s) const { return base + C::kOffK + s * C::kTile; }
+  __device__ __forceinline__ uint8_t* v_ptr(int s) const { return base + C::kOffV + s * C::kTile; }
+  __device__ __forceinline__ uint32_t bar(int i) const { return sbase + C::kOffBar + 8 * i; }
+  __device__ __forceinline__ uint32_t q_full(int b) const { return bar(0 + b); }
+  __device__ __forceinline__ uint32_t q_empty(int b) const { return bar(2 + b); }
+  __device__ __forceinline__ uint32_t k_full(int s) const { return bar(4 + s); }
+  __device__ __forceinline__ uint32_t k_empty(int s) const { return bar(8 + s); }
+  __device__ __forceinline__ uint32_t v_full(int s) const { return bar(12 + s); }
+  __device__ __forceinline__ uint32_t v_empty(int s) const { return bar(16 + s); }
+  __device__ __forceinline__ uint32_t vt_full(int s) const { return bar(20 + s); }
+  __device__ __forceinline__ uint32_t vt_empty(int s) const { return bar(24 + s); }
+  __device__ __forceinline__ uint32_t v_land() const { return bar(28); }
+  __device__ __forceinline__ uint32_t s_full(int b) const { return bar(29 + b); }
+  __device__ __forceinline__ uint32_t p_full(int b) const { return bar(32 + b); }
+  // completion of the P.V of entry k arrives on pv_done(k & 1): the softmax
+  // takes them in order up to one entry behind, and with two barriers neither
+  // runs more than one phase ahead of it
+  __device__ __forceinline__ uint32_t pv_done(uint32_t k) const { return (k & 1) ? bar(38) : bar(35); }
+  __device__ __forceinline__ uint32_t o_empty() const { return bar(36); }
+  __device__ __forceinline__ uint32_t fin() const { return bar(37); }
+  __device__ __forceinline__ uint32_t* tmem_holder() const { return reinterpret_cast<uint32_t*>(base + C::kOffMisc); }
+  __device__ __forceinline__ volatile int* abort_flag() const { return reinterpret_cast<volatile int*>(base + C::kOffMisc + 4); }
+  __device__ __forceinline__ BandSeg* segs() const { return reinterpret_cast<BandSeg*>(base + C::kOffMisc + 16); }
+};
+
+// 16-byte chunk `ch` of row `row` inside a [rows, D] bf16 tile stored as D/64
+// blocks of [rows, 64] with the 128-byte swizzle TMA uses.
+__device__ __forceinline__ uint32_t sw128_offset(int row, int ch, int rows) {
+  return (uint32_t)((ch >> 3) * rows * 128 + row * 128 + (((ch & 7) ^ (row & 7)) << 4));
+}
+
+// m coordinate of global position g in residue class r, or a value that is
+// never inside a band when g is not in the class
+__device__ __forceinline__ int residue_coord(int g, int r, int delta) {
+  if (delta == 1) return g;
+  const int d = g - r;
+  return (d >= 0 && d % delta == 0) ? d / delta : -(1 << 29);
+}
+
+// ------------------------------------------------------------------ producers
+// kIsV = false loads Q and the K entries, kIsV = true the V entries, so that a
+// full V ring (waiting for the transposer) never holds back a K.
+template <int D, bool kIsV>
+__device__ void band_producer(const BandParams& p, const BandSmem<D>& sm, int lane) {
+  using C = BandCfg<D>;
+  constexpr int kSt = kIsV ? C::kVSt : C::kKSt;
+  volatile int* abort = sm.abort_flag();
+  uint32_t kv = 0, q_it = 0, land = 0;
+  int land_pending = -1;  // v_land phase of a zeroing load not yet seen to land
+  int last_fill[kSt], last_q[C::kQBuf];
+#pragma unroll
+  for (int s = 0; s < kSt; ++s) last_fill[s] = -1;
+#pragma unroll
+  for (int s = 0; s < C::kQBuf; ++s) last_q[s] = -1;
+  bool ok = true;
+  Tracer tr;
+  if (blockIdx.x == 0 && lane == 0) tr.track = kIsV ? 5 : 3;
+
+  for (int item = blockIdx.x; ok && item < p.total_items; item += gridDim.x) {
+    const TileItem it = decode_tile<C::kE>(p, sm.segs(), item);
+    if (!it.act) continue;
+
+    if (!kIsV) {
+      const int qb = q_it % C::kQBuf;
+      if (!warp_wait(sm.q_empty(qb), ((q_it / C::kQBuf) & 1) ^ 1, abort, kRoleProducer)) { ok = false; break; }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(sm.q_full(qb), C::kTileQ);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sm.q(qb) + c * 16384, &p.tq[it.set], c * 64, it.m0, it.bh, sm.q_full(qb));
+      }
+      last_q[qb] = (int)q_it;
+      ++q_it;
+    }
+
+    const __nv_bfloat16* src = (kIsV ? p.v : p.k) + (size_t)it.bh * p.n * D;
+    const CUtensorMap* map = kIsV ? &p.tv[it.set] : &p.tk[it.set];
+    constexpr int CH = D / 8;  // 16-byte chunks per row
+
+    for (int e = 0; e < it.nE; ++e, ++kv) {
+      const int slot = kv % kSt;
+      const uint32_t full = kIsV ? sm.v_full(slot) : sm.k_full(slot);
+      const uint32_t empty = kIsV ? sm.v_empty(slot) : sm.k_empty(slot);
+      const uint32_t dst = kIsV ? sm.v(slot) : sm.k(slot);
+      uint8_t* dst_ptr = kIsV ? sm.v_ptr(slot) : sm.k_ptr(slot);
+      tr.ev(30);
+      if (!warp_wait(empty, ((kv / kSt) & 1) ^ 1, abort, kRoleProducer)) { ok = false; break; }
+      tr.ev(31);
+      if (e < it.nU) {
+        const int y = it.U0 + C::kE * e;
+        // value rows past the last key any row of the tile attends (padding,
+        // or the end of the tile's windows) but inside the tensor are zeroed,
+        // so that whatever they hold cannot reach the output through 0 * value
+        const int z0 = it.khi - y + 1, z1 = min(C::kE, it.n_r - y);
+        if (kIsV && z0 < z1) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(sm.v_land(), C::kTile);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * C::kE * 128, map, c * 64, y, it.bh, sm.v_land());
+          }
+          land_pending = (int)land;
+          const bool landed = warp_wait(sm.v_land(), land & 1, abort, kRoleProducer);
+          ++land;
+          if (!landed) { ok = false; break; }
+          land_pending = -1;
+          for (int idx = lane; idx < (z1 - z0) * CH; idx += 32) {
+            const int row = z0 + idx / CH, ch = idx - (idx / CH) * CH;
+            *reinterpret_cast<uint4*>(dst_ptr + sw128_offset(row, ch, C::kE)) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full);
+          last_fill[slot] = -1;
+        } else {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(full, C::kTile);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * C::kE * 128, map, c * 64, y, it.bh, full);
+          }
+          last_fill[slot] = (int)kv;
+        }
+      } else {
+        // rows of the global tokens visible to the tile, zeros after
+        const int gt = e - it.nU;
+        const int cnt = global_count<C::kE>(it, e);
+        const int ng = (cnt + 15) & ~15;
+        for (int idx = lane; idx < ng * CH; idx += 32) {
+          const int row = idx / CH, ch = idx - (idx / CH) * CH;
+          uint4 x = make_uint4(0, 0, 0, 0);
+          if (row < cnt) x = __ldg(reinterpret_cast<const uint4*>(src + (size_t)p.gidx[C::kE * gt + row] * D) + ch);
+          *reinterpret_cast<uint4*>(dst_ptr + sw128_offset(row, ch, C::kE)) = x;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full);
+        last_fill[slot] = -1;  // completed synchronously
+      }
+      tr.ev(32);
+    }
+  }
+  tr.done();
+  // Let every TMA copy this warp issued land before the CTA can exit.
+  int dummy = 0;
+#pragma unroll
+  for (int s = 0; s < kSt; ++s)
+    if (last_fill[s] >= 0)
+      mbar_wait(kIsV ? sm.v_full(s) : sm.k_full(s), ((uint32_t)last_fill[s] / kSt) & 1, &dummy, kRoleDrain, 200000000ull);
+#pragma unroll
+  for (int s = 0; s < C::kQBuf; ++s)
+    if (last_q[s] >= 0) mbar_wait(sm.q_full(s), ((uint32_t)last_q[s] / C::kQBuf) & 1, &dummy, kRoleDrain, 200000000ull);
+  if (land_pending >= 0) mbar_wait(sm.v_land(), (uint32_t)land_pending & 1, &dummy, kRoleDrain, 200000000ull);
+}
+
+// ------------------------------------------------------------------ V transposer (one warp)
+// The P.V product takes V as a K-major operand (keys contiguous), which the
+// tensor cores read at full rate from a [D, keys] layout.  TMA delivers V as
+// [keys, D]; the warp moves every entry into 8x8 blocks of V^T with
+// ldmatrix.trans / stmatrix, both sides 128-byte swizzled: V^T is kE/64
+// blocks of 64 keys, each [D rows, 128 bytes].
+template <int D>
+__device__ void band_transposer(const BandParams& p, const BandSmem<D>& sm, int lane) {
+  using C = BandCfg<D>;
+  volatile int* abort = sm.abort_flag();
+  uint32_t kv = 0;
+  bool ok = true;
+  const int m = lane >> 3, r = lane & 7;  // this lane addresses row r of matrix m
+  Tracer tr;
+  if (blockIdx.x == 0 && lane == 0) tr.track = 4;
+  for (int item = blockIdx.x; ok && item < p.total_items; item += gridDim.x) {
+    const TileItem it = decode_tile<C::kE>(p, sm.segs(), item);
+    if (!it.act) continue;
+    for (int e = 0; e < it.nE; ++e, ++kv) {
+      const int vs = kv % C::kVSt, ts = kv % C::kTSt;
+      tr.ev(40);
+      if (!warp_wait(sm.v_full(vs), (kv / C::kVSt) & 1, abort, kRoleTranspose)) { ok = false; break; }
+      if (!warp_wait(sm.vt_empty(ts), ((kv / C::kTSt) & 1) ^ 1, abort, kRoleTranspose)) { ok = false; break; }
+      tr.ev(41);
+      const uint32_t src = sm.v(vs), dst = sm.vt(ts);
+#pragma unroll 2
+      for (int ki = 0; ki < C::kE / 8; ++ki) {  // 8-key groups
+        const int key = 8 * ki + r;              // source row of this lane
+        const uint32_t dblk = dst + (ki >> 3) * (D * 128);
+#pragma unroll
+        for (int dg = 0; dg < D / 32; ++dg) {
+          const int di = 4 * dg + m;  // 8-column group of D
+          uint32_t x0, x1, x2, x3;
+          ldmatrix_x4_trans(src + (di >> 3) * (C::kE * 128) + key * 128 + (((di & 7) ^ (key & 7)) << 4), x0, x1, x2, x3);
+          const int dr = 8 * di + r;  // destination row (a column of V)
+          stmatrix_x4(dblk + dr * 128 + (((ki & 7) ^ (dr & 7)) << 4), x0, x1, x2, x3);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(sm.v_empty(vs));
+        mbar_arrive(sm.vt_full(ts));
+      }
+      tr.ev(43);
+    }
+  }
+  tr.done();
+}
+
+// ------------------------------------------------------------------ MMA issuer (one warp)
+// Walks the same sequence of entries as the softmax warps.  Two cursors: one
+// for the S products, running up to kSBuf entries ahead, and one for the
+// P.V products.  The whole warp runs the bookkeeping (descriptors stay in
+// uniform registers); one elected lane issues.
+struct EntryCursor {
+  TileItem it;
+  int item, e;       // current item and entry in it
+  uint32_t g;        // entry number over the whole stream (selects the S buffer)
+  uint32_t kv;       // first fill of the current item in the K / V rings
+  uint32_t n_items;  // active items before the current one (selects the Q buffer)
+  bool valid;
+};
+
+template <int kE>
+__device__ __forceinline__ void cursor_seek(const BandParams& p, const BandSeg* segs, EntryCursor& c) {
+  // first active item at or after c.item
+  while (c.item < p.total_items) {
+    c.it = decode_tile<kE>(p, segs, c.item);
+    if (c.it.act) return;
+    c.item += gridDim.x;
+  }
+  c.valid = false;
+}
+
+template <int kE>
+__device__ __forceinline__ void cursor_start(const BandParams& p, const BandSeg* segs, EntryCursor& c) {
+  c.item = blockIdx.x;
+  c.e = 0;
+  c.g = 0;
+  c.kv = 0;
+  c.n_items = 0;
+  c.valid = true;
+  cursor_seek<kE>(p, segs, c);
+}
+
+template <int kE>
+__device__ __forceinline__ void cursor_next(const BandParams& p, const BandSeg* segs, EntryCursor& c) {
+  ++c.g;
+  if (++c.e < c.it.nE) return;
+  c.kv += c.it.nE;
+  ++c.n_items;
+  c.e = 0;
+  c.item += gridDim.x;
+  cursor_seek<kE>(p, segs, c);
+}
+
+template <int D>
+__device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tmem) {
+  using C = BandCfg<D>;
+  constexpr uint32_t kTile16 = C::kTile >> 4;    // a K / V^T slot, in descriptor address units
+  constexpr uint32_t kTileQ16 = C::kTileQ >> 4;  // a Q tile
+  volatile int* abort = sm.abort_flag();
+  const uint32_t idesc_sband = idesc_bf16_f32(128, C::kE, 0);
+  const uint32_t idesc_pv = idesc_bf16_f32(128, D, 0);  // V^T: K-major
+  const uint64_t qdesc0 = smem_desc_sw128(sm.q(0), 16, 1024);
+  const uint64_t kdesc0 = smem_desc_sw128(sm.k(0), 16, 1024);
+  const uint64_t vdesc0 = smem_desc_sw128(sm.vt(0), 16, 1024);
+  const uint32_t ot = tmem + C::kColO;
+  uint32_t o_cnt = 0;
+  bool ok = true;
+  Tracer tr;
+  if (blockIdx.x == 0 && (threadIdx.x & 31) == 0) tr.track = 2;
+
+  EntryCursor cs, cp;  // S cursor (ahead), P.V cursor
+  cursor_start<C::kE>(p, sm.segs(), cs);
+  cursor_start<C::kE>(p, sm.segs(), cp);
+
+  // S of the entry under cs into buffer cs.g % kSBuf
+  auto issue_s = [&]() -> bool {
+    const TileItem& it = cs.it;
+    const int qb = cs.n_items % C::kQBuf;
+    if (cs.e == 0) {
+      if (!warp_wait(sm.q_full(qb), (cs.n_items / C::kQBuf) & 1, abort, kRoleMma)) return false;
+    }
+    const uint32_t f = cs.kv + cs.e;
+    const int ks = f % C::kKSt;
+    tr.ev(10);
+    if (!warp_wait(sm.k_full(ks), (f / C::kKSt) & 1, abort, kRoleMma)) return false;
+    tr.ev(11);
+    tc_fence_after();
+    const uint32_t idesc =
+        (cs.e < it.nU) ? idesc_sband : idesc_bf16_f32(128, (global_count<C::kE>(it, cs.e) + 15) & ~15, 0);
+    const uint64_t qd = qdesc0 + qb * kTileQ16;
+    const uint64_t kd = kdesc0 + ks * kTile16;
+    const uint32_t buf = cs.g % C::kSBuf;
+    const uint32_t dt = tmem + C::kE * buf;
+    const bool last = cs.e + 1 == it.nE;
+    if (elect_one()) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        // 16 columns of D: 32 bytes within a 64-column block of 128-byte rows
+        const uint32_t qoff = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+        const uint32_t koff = ((kk >> 2) * (C::kE * 128) + (kk & 3) * 32) >> 4;
+        mma_bf16_ss(dt, qd + qoff, kd + koff, idesc, kk > 0);
+      }
+      mma_commit(sm.s_full(buf));
+      mma_commit(sm.k_empty(ks));
+      if (last) mma_commit(sm.q_empty(qb));  // the item's last S: Q may be replaced
+    }
+    __syncwarp();
+    return true;
+  };
+
+  // P.V of the entry under cp, P from buffer cp.g % kSBuf
+  auto issue_pv = [&]() -> bool {
+    const TileItem& it = cp.it;
+    const uint32_t f = cp.kv + cp.e;
+    const int ts = f % C::kTSt;
+    const uint32_t buf = cp.g % C::kSBuf;
+    tr.ev(12);
+    if (!warp_wait(sm.vt_full(ts), (f / C::kTSt) & 1, abort, kRoleMma)) return false;
+    if (!warp_wait(sm.p_full(buf), (cp.g / C::kSBuf) & 1, abort, kRoleMma)) return false;
+    tr.ev(13);
+    if (cp.e == 0) {  // O is overwritten: the previous item's epilogue must have read it
+      if (!warp_wait(sm.o_empty(), (o_cnt & 1) ^ 1, abort, kRoleMma)) return false;
+      ++o_cnt;
+    }
+    tc_fence_after();
+    const int ksteps = (cp.e < it.nU) ? C::kE / 16 : ((global_count<C::kE>(it, cp.e) + 15) >> 4);
+    const uint32_t pt = tmem + C::kE * buf;  // P over the first kE/2 columns of the buffer
+    const uint64_t vd = vdesc0 + ts * kTile16;
+    const uint32_t acc0 = cp.e > 0 ? 1u : 0u;
+    if (elect_one()) {
+      if (ksteps == C::kE / 16) {
+#pragma unroll
+        for (int kk = 0; kk < C::kE / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * (D * 128) + (kk & 3) * 32) >> 4;
+          mma_bf16_ts(ot, pt + kk * 8, vd + off, idesc_pv, kk > 0 ? 1u : acc0);
+        }
+      } else {
+        for (int kk = 0; kk < ksteps; ++kk) {
+          const uint32_t off = ((kk >> 2) * (D * 128) + (kk & 3) * 32) >> 4;
+          mma_bf16_ts(ot, pt + kk * 8, vd + off, idesc_pv, kk > 0 ? 1u : acc0);
+        }
+      }
+      mma_commit(sm.pv_done(cp.g));
+      mma_commit(sm.vt_empty(ts));
+    }
+    __syncwarp();
+    tr.ev(14);
+    return true;
+  };
+
+  while (ok && cs.valid && cs.g < (uint32_t)C::kSBuf) {
+    ok = issue_s();
+    cursor_next<C::kE>(p, sm.segs(), cs);
+  }
+  while (ok && cp.valid) {
+    ok = issue_pv();
+    if (!ok) break;
+    cursor_next<C::kE>(p, sm.segs(), cp);
+    // the S buffer just read by that P.V is free: refill up to kSBuf ahead
+    while (ok && cs.valid && cs.g < cp.g + C::kSBuf) {
+      ok = issue_s();
+      cursor_next<C::kE>(p, sm.segs(), cs);
+    }
+  }
+  tr.done();
+  // Wait until every MMA this warp issued has finished before TMEM is freed.
+  if (elect_one()) mma_commit(sm.fin());
+  __syncwarp();
+  int dummy = 0;
+  mbar_wait(sm.fin(), 0, &dummy, kRoleDrain, 200000000ull);
+  __syncwarp();
+}
+
+// ------------------------------------------------------------------ softmax / epilogue
+// Lazy rescaling: the running maximum of a row is raised only when a new
+// score exceeds it by more than kLazy in the exp2 domain, so that O is
+// rescaled rarely; P values stay below 2^kLazy.
+constexpr float kLazy = 8.0f;
+
+// Bits [lo, hi] of a 32-bit word (empty when hi < lo); lo, hi may lie outside [0, 31].
+__device__ __forceinline__ uint32_t bit_range(int lo, int hi) {
+  lo = max(lo, 0);
+  hi = min(hi, 31);
+  if (hi < lo) return 0u;
+  const uint32_t upto = (hi == 31) ? 0xffffffffu : ((1u << (hi + 1)) - 1u);
+  return upto & ~((1u << lo) - 1u);
+}
+
+// Global entry e, chunk c: bit t set where this row attends global column
+// 32c + t (a global key already in the row's band is counted there, once).
+template <int kE>
+__device__ __forceinline__ uint32_t global_keep(const BandParams& p, const TileItem& it, int e, int c,
+                                                int m_q, bool row_valid) {
+  const int gt = e - it.nU;
+  const int tend = max(0, min(32, global_count<kE>(it, e) - 32 * c));
+  const int i_q = it.r + it.delta * m_q;
+  uint32_t k = 0;
+#pragma unroll 1
+  for (int t = 0; t < tend; ++t) {
+    const int g = p.gidx[kE * gt + 32 * c + t];
+    const int mg = residue_coord(g, it.r, it.delta);
+    const bool in_band = (m_q - mg <= p.half) && (mg - m_q <= p.right);
+    k |= (uint32_t)((!p.causal || g <= i_q) && !in_band) << t;
+  }
+  return row_valid ? k : 0u;
+}
+
+// Maximum over the kept columns of a 32-column chunk of raw scores.
+__device__ __forceinline__ float chunk_max(const uint32_t (&x)[32], uint32_t keep, uint32_t whole) {
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  float v[32];
+  if (whole) {
+#pragma unroll
+    for (int t = 0; t < 32; ++t) v[t] = __uint_as_float(x[t]);
+  } else {
+#pragma unroll
+    for (int t = 0; t < 32; ++t) v[t] = ((keep >> t) & 1u) ? __uint_as_float(x[t]) : NEG_INF;
+  }
+  float a = max3f(v[0], v[1], v[2]), b = max3f(v[3], v[4], v[5]), c = max3f(v[6], v[7], v[8]),
+        d = max3f(v[9], v[10], v[11]);
+#pragma unroll
+  for (int t = 12; t < 28; t += 8) {
+    a = max3f(a, v[t], v[t + 1]);
+    b = max3f(b, v[t + 2], v[t + 3]);
+    c = max3f(c, v[t + 4], v[t + 5]);
+    d = max3f(d, v[t + 6], v[t + 7]);
+  }
+  return fmaxf(max3f(a, b, v[28]), max3f(c, d, max3f(v[29], v[30], v[31])));
+}
+
+// P for a 32-column chunk: p = exp2(s * sl2 - m) on the kept columns, 0
+// elsewhere, packed to bf16 pairs; returns the two partial row sums.
+__device__ __forceinline__ float2 chunk_exp(const uint32_t (&x)[32], uint32_t keep, uint32_t whole,
+                                            float sl2, float mneg, uint32_t (&pk)[16]) {
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  const float2 sc2 = make_float2(sl2, sl2), of2 = make_float2(mneg, mneg);
+  float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    float s0 = __uint_as_float(x[2 * t]), s1 = __uint_as_float(x[2 * t + 1]);
+    if (!whole) {
+      s0 = ((keep >> (2 * t)) & 1u) ? s0 : NEG_INF;
+      s1 = ((keep >> (2 * t + 1)) & 1u) ? s1 : NEG_INF;
+    }
+    const float2 y = __ffma2_rn(make_float2(s0, s1), sc2, of2);
+    const float p0 = ex2_approx(y.x), p1 = ex2_approx(y.y);
+    if (t & 1) sb = __fadd2_rn(sb, make_float2(p0, p1));
+    else sa = __fadd2_rn(sa, make_float2(p0, p1));
+    pk[t] = pack_bf16x2(p0, p1);
+  }
+  return __fadd2_rn(sa, sb);
+}
+
+// Softmax and epilogue (one query row per thread; warp quarter wq of TMEM lanes).
+template <int D>
+__device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_t tmem, int wq, int lane) {
+  using C = BandCfg<D>;
+  volatile int* abort = sm.abort_flag();
+  const int row = wq * 32 + lane;
+  const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+  const uint32_t tO = tmem + lane_base + C::kColO;
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  const float sl2 = p.sl2;
+  uint32_t g = 0, pv_cnt = 0;
+  bool ok = true;
+  Tracer tr;
+  if (blockIdx.x == 0 && wq == 0 && lane == 0) tr.track = 0;
+
+  for (int item = blockIdx.x; ok && item < p.total_items; item += gridDim.x) {
+    const TileItem it = decode_tile<C::kE>(p, sm.segs(), item);
+    tr.ev(0);
+    const int m_q = it.m0 + row;
+    const bool row_exists = m_q < it.n_r;
+    const bool row_valid = m_q < it.Lm;
+    uint4* orow = reinterpret_cast<uint4*>(p.out + ((size_t)it.bh * p.n + it.r + (size_t)it.delta * m_q) * D);
+    if (!it.act) {
+      if (row_exists) {
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
+      }
+      continue;
+    }
+    float m_run = NEG_INF, l_run = 0.f;
+
+    for (int e = 0; e < it.nE; ++e, ++g) {
+      // ---- keep c: bit t set where this row attends column 32c + t
+      uint32_t keep0, keep1, keep2, keep3;
+      uint32_t onm, fullm;
+      const int kb_w = it.U0 + C::kE * e;
+      const int mw = it.m0 + 32 * wq;  // first row of this warp
+      if (e < it.nU && mw + 31 < it.Lm && kb_w >= mw + 31 - p.half &&
+          kb_w + C::kE - 1 <= min(mw + p.right, it.Lm - 1)) {
+        // every row of the warp attends the whole entry
+        keep0 = keep1 = keep2 = keep3 = ~0u;
+        onm = fullm = (1u << (C::kE / 32)) - 1u;
+      } else {
+      if (e < it.nU) {
+        const int clo = m_q - p.half - kb_w;
+        int chi = min(min(m_q + p.right, it.Lm - 1) - kb_w, C::kE - 1);
+        if (!row_valid) chi = clo - 1;
+        keep0 = bit_range(clo, chi);
+        keep1 = bit_range(clo - 32, chi - 32);
+        keep2 = bit_range(clo - 64, chi - 64);
+        keep3 = bit_range(clo - 96, chi - 96);
+      } else {
+        keep0 = global_keep<C::kE>(p, it, e, 0, m_q, row_valid);
+        keep1 = global_keep<C::kE>(p, it, e, 1, m_q, row_valid);
+        keep2 = C::kE > 64 ? global_keep<C::kE>(p, it, e, 2, m_q, row_valid) : 0u;
+        keep3 = C::kE > 64 ? global_keep<C::kE>(p, it, e, 3, m_q, row_valid) : 0u;
+      }
+      // chunks some lane of the warp needs, and chunks every lane needs whole
+      onm = (__any_sync(0xffffffffu, keep0 != 0u) ? 1u : 0u) |
+            (__any_sync(0xffffffffu, keep1 != 0u) ? 2u : 0u) |
+            (__any_sync(0xffffffffu, keep2 != 0u) ? 4u : 0u) |
+            (__any_sync(0xffffffffu, keep3 != 0u) ? 8u : 0u);
+      fullm = (__all_sync(0xffffffffu, keep0 == ~0u) ? 1u : 0u) |
+              (__all_sync(0xffffffffu, keep1 == ~0u) ? 2u : 0u) |
+              (__all_sync(0xffffffffu, keep2 == ~0u) ? 4u : 0u) |
+              (__all_sync(0xffffffffu, keep3 == ~0u) ? 8u : 0u);
+      }
+
+      const uint32_t buf = g % C::kSBuf;
+      const uint32_t tS = tmem + lane_base + C::kE * buf;  // S of this entry, then P
+      tr.ev(1);
+      if (!warp_wait(sm.s_full(buf), (g / C::kSBuf) & 1, abort, kRoleSoftmax)) { ok = false; break; }
+      tr.ev(2);
+      tc_fence_after();
+
+      // ---- pass 1: row maximum of the raw scores (the scale is positive),
+      // one 32-column chunk at a time (TMEM reads are cheap; the loop body
+      // stays small for the instruction cache)
+      float mx = NEG_INF;
+#pragma unroll 1
+      for (int c = 0; c < C::kE / 32; ++c) {
+        if (!((onm >> c) & 1u)) continue;
+        uint32_t x[32];
+        tmem_ld32_nw(tS + 32 * c, x);
+        tmem_wait_ld();
+        reg_fence32(x);
+        const uint32_t kc = c == 0 ? keep0 : c == 1 ? keep1 : c == 2 ? keep2 : keep3;
+        mx = fmaxf(mx, chunk_max(x, kc, (fullm >> c) & 1u));
+      }
+      const float mt = mx * sl2;
+      float alpha = 1.f;
+      bool resc = false;
+      if (mt > m_run + kLazy) {
+        alpha = ex2_approx(m_run - mt);  // 0 while m_run is -inf
+        m_run = mt;
+        resc = true;
+      }
+      // Completions of the P.V products are taken in order, one entry behind
+      // (long done, no stall); a rescale of O also needs the previous entry's.
+      const bool any_resc = e > 0 && __any_sync(0xffffffffu, resc);
+      const uint32_t need = any_resc ? g : (g > 0 ? g - 1 : 0);  // P.V products that must be done
+      while (ok && pv_cnt < need) {
+        ok = warp_wait(sm.pv_done(pv_cnt), (pv_cnt >> 1) & 1, abort, kRoleSoftmax);
+        ++pv_cnt;
+      }
+      if (!ok) break;
+      if (any_resc) {
+        tc_fence_after();
+        {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32_nw(tO + 32 * c, o);
+            tmem_wait_ld();
+            reg_fence32(o);
+            float2* of = reinterpret_cast<float2*>(o);
+            const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+            for (int t = 0; t < 16; ++t) of[t] = __fmul2_rn(of[t], a2);
+            tmem_st16_nw(tO + 32 * c, o);
+            tmem_st16_nw(tO + 32 * c + 16, o + 16);
+          }
+        }
+      }
+      tr.ev(3);
+      // ---- pass 2: P = exp2(s * scale - m) chunk by chunk; P chunk c goes to
+      // columns [16c, 16c + 16) of the buffer, whose scores (chunk c/2) are read
+      const float mneg = (m_run == NEG_INF) ? 0.f : -m_run;
+      float2 sum2 = make_float2(0.f, 0.f);
+#pragma unroll 1
+      for (int c = 0; c < C::kE / 32; ++c) {
+        uint32_t pk[16];
+        if ((onm >> c) & 1u) {
+          uint32_t x[32];
+          tmem_ld32_nw(tS + 32 * c, x);
+          tmem_wait_ld();
+          reg_fence32(x);
+          const uint32_t kc = c == 0 ? keep0 : c == 1 ? keep1 : c == 2 ? keep2 : keep3;
+          sum2 = __fadd2_rn(sum2, chunk_exp(x, kc, (fullm >> c) & 1u, sl2, mneg, pk));
+        } else {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) pk[t] = 0u;
+        }
+        tmem_st16_nw(tS + 16 * c, pk);
+      }
+      l_run = l_run * alpha + (sum2.x + sum2.y);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.p_full(buf));
+      tr.ev(4);
+    }
+    if (!ok) break;
+
+    // ---- epilogue: O / l -> bf16 (32 columns at a time) -> global
+    tr.ev(5);
+    while (ok && pv_cnt < g) {  // every P.V of the item (entries before g)
+      ok = warp_wait(sm.pv_done(pv_cnt), (pv_cnt >> 1) & 1, abort, kRoleSoftmax);
+      ++pv_cnt;
+    }
+    if (!ok) break;
+    tc_fence_after();
+    const float inv = (row_valid && l_run > 0.f) ? 1.0f / l_run : 0.f;
+    uint32_t ob[D / 2];  // the row in bf16 pairs
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      tmem_ld32_nw(tO + 32 * c, o);
+      tmem_wait_ld();
+      reg_fence32(o);
+      const float* of = reinterpret_cast<const float*>(o);
+#pragma unroll
+      for (int t = 0; t < 16; ++t) ob[16 * c + t] = pack_bf16x2(of[2 * t] * inv, of[2 * t + 1] * inv);
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.o_empty());
+    if (row_exists) {
+      // padded rows (inv = 0) are written as zeros; O is finite there since
+      // every value row such a row could meet is finite or zeroed
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c)
+        orow[c] = row_valid ? make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3])
+                            : make_uint4(0, 0, 0, 0);
+    }
+    tr.ev(7);
+  }
+  tr.done();
+}
+
+constexpr int kBandThreads = 256;
+
+template <int D>
+__global__ void __launch_bounds__(kBandThreads, BandCfg<D>::kCtaPerSm)
+    band_tc_kernel(const __grid_constant__ BandParams p) {
+  using C = BandCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  BandSmem<D> sm;
+  {
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    sm.base = smem_raw + pad;
+    sm.sbase = raw + pad;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(sm.q_full(b), 1);
+      mbar_init(sm.q_empty(b), 1);
+    }
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(sm.k_full(s), 1);
+      mbar_init(sm.k_empty(s), 1);
+      mbar_init(sm.v_full(s), 1);
+      mbar_init(sm.v_empty(s), 1);
+      mbar_init(sm.vt_full(s), 1);
+      mbar_init(sm.vt_empty(s), 1);
+    }
+    mbar_init(sm.v_land(), 1);
+    for (int b = 0; b < 3; ++b) {
+      mbar_init(sm.s_full(b), 1);
+      mbar_init(sm.p_full(b), 4);  // the four softmax warps
+    }
+    mbar_init(sm.pv_done(0), 1);
+    mbar_init(sm.pv_done(1), 1);
+    mbar_init(sm.o_empty(), 4);
+    mbar_init(sm.fin(), 1);
+    *sm.abort_flag() = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  for (int i = threadIdx.x; i < p.nseg; i += blockDim.x) sm.segs()[i] = p.seg[i];
+  if (warp == 0) {
+    tmem_alloc(smem_u32(sm.tmem_holder()), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sm.tmem_holder();
+
+  if (warp >= 4) {
+    band_softmax<D>(p, sm, tmem, warp & 3, lane);
+  } else if (warp == 0) {
+    band_mma<D>(p, sm, tmem);
+  } else if (warp == 1) {
+    band_producer<D, false>(p, sm, lane);
+  } else if (warp == 2) {
+    band_producer<D, true>(p, sm, lane);
+  } else {
+    band_transposer<D>(p, sm, lane);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D>
+static lf_status launch_band_tc_d(const BandParams& p, int grid, cudaStream_t s) {
+  using C = BandCfg<D>;
+  static bool attr_set = false;  // per process; the attribute is per function
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(band_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) {
+      set_error("cudaFuncSetAttribute(band kernel): %s", cudaGetErrorString(e));
+      return LF_ERR_CUDA;
+    }
+    attr_set = true;
+  }
+  band_tc_kernel<D><<<grid, kBandThreads, C::kSmem, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error("band kernel launch: %s", cudaGetErrorString(e));
+    return LF_ERR_CUDA;
+  }
+  count_launch();
+  return LF_OK;
+}
+
+// D = 64 only (D = 128 runs the pair kernel of band_pair.cuh).
+inline lf_status launch(const BandParams& p, int grid, cudaStream_t s) { return launch_band_tc_d<64>(p, grid, s); }
+
+}  // namespace ringk
+}  // namespace lf

@@ -12,11 +12,26 @@
 #include <vector>
 
 #include "lf_internal.cuh"
-#include "band_tc.cuh"
+#include "band_ring.cuh"
+#include "band_pair.cuh"
 #include "band_simt.cuh"
 #include "global_rows.cuh"
 
 namespace lf {
+
+// ------------------------------------------------------------------ band kernel choice
+// D = 64: the ring kernel (one 128-row tile per CTA, two CTAs per SM, 64-key
+// entries); D = 128: the pair kernel (two tiles per CTA sharing 128-key
+// entries, one CTA per SM).
+lf_status launch_band_tc(const BandParams& p, int d, int grid, cudaStream_t s) {
+  if (d == 64) return ringk::launch(p, grid, s);
+  if (d == 128) return pairk::launch(p, grid, s);
+  set_error("band kernel: unsupported head dimension %d", d);
+  return LF_ERR_UNSUPPORTED;
+}
+int band_ctas_per_sm(int d) { return d == 64 ? ringk::BandCfg<64>::kCtaPerSm : 1; }
+int band_entry_keys(int d) { return d == 64 ? ringk::BandCfg<64>::kE : 128; }
+int band_rows_per_item(int d) { return d == 64 ? 128 : 256; }
 
 static thread_local char t_msg[512] = "";
 static thread_local cudaEvent_t t_band_start = nullptr, t_band_stop = nullptr;
@@ -52,9 +67,9 @@ static EncodeTiledFn encode_fn() {
 }
 
 // [d, rows, planes] bf16 view with row stride `row_stride` elements, plane
-// stride `plane_stride` elements; boxes of [64, 128, 1] with 128-byte swizzle.
+// stride `plane_stride` elements; boxes of [64, box_rows, 1] with 128-byte swizzle.
 static lf_status make_map(CUtensorMap* m, const void* base, int d, int64_t rows, int64_t planes,
-                          int64_t row_stride, int64_t plane_stride) {
+                          int64_t row_stride, int64_t plane_stride, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) {
     set_error("cuTensorMapEncodeTiled is not available from the driver");
@@ -62,7 +77,7 @@ static lf_status make_map(CUtensorMap* m, const void* base, int d, int64_t rows,
   }
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)planes};
   cuuint64_t strides[2] = {(cuuint64_t)row_stride * 2, (cuuint64_t)plane_stride * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -318,11 +333,12 @@ static lf_status global_merges(const Problem& P, const float* ws) {
 
 // ------------------------------------------------------------------ bf16 band planning
 // Every (head, residue) class with at least one row is a segment; its work
-// items are pairs of 128-row tiles.  Segments are generated in order straight
+// items are its 128-row tiles (D = 64) or pairs of them (D = 128).  Segments are generated in order straight
 // into the parameter block `p` (no heap use), one launch per kMaxSeg segments
 // or kMaxSets (dilation, residue) tensor-map sets.
 static lf_status run_band_bf16(const Problem& P, int b0, int nbat, BandParams& p) {
-  const int grid_cap = sm_count();
+  const int grid_cap = sm_count() * band_ctas_per_sm(P.d);
+  const int rows_per_item = band_rows_per_item(P.d);
   const size_t off = (size_t)b0 * P.H * P.n * P.d;
   const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(P.q) + off;
   const __nv_bfloat16* k = reinterpret_cast<const __nv_bfloat16*>(P.k) + off;
@@ -357,10 +373,10 @@ static lf_status run_band_bf16(const Problem& P, int b0, int nbat, BandParams& p
       bs.r = r;
       bs.delta = delta;
       bs.n_r = n_r;
-      bs.pairs = (n_r + 255) / 256;
+      bs.items = (n_r + rows_per_item - 1) / rows_per_item;
       bs.set = set;
       bs.begin = items_per_b;
-      items_per_b += bs.pairs;
+      items_per_b += bs.items;
       ++r;
     }
     if (nseg == 0) break;
@@ -370,9 +386,10 @@ static lf_status run_band_bf16(const Problem& P, int b0, int nbat, BandParams& p
       const int64_t rs = (int64_t)delta * P.d, ps = (int64_t)P.n * P.d;
       const size_t ro = (size_t)rr * P.d;
       lf_status st;
-      if ((st = make_map(&p.tq[t], q + ro, P.d, n_r, planes, rs, ps)) != LF_OK) return st;
-      if ((st = make_map(&p.tk[t], k + ro, P.d, n_r, planes, rs, ps)) != LF_OK) return st;
-      if ((st = make_map(&p.tv[t], v + ro, P.d, n_r, planes, rs, ps)) != LF_OK) return st;
+      const int ek = band_entry_keys(P.d);
+      if ((st = make_map(&p.tq[t], q + ro, P.d, n_r, planes, rs, ps, 128)) != LF_OK) return st;
+      if ((st = make_map(&p.tk[t], k + ro, P.d, n_r, planes, rs, ps, ek)) != LF_OK) return st;
+      if ((st = make_map(&p.tv[t], v + ro, P.d, n_r, planes, rs, ps, ek)) != LF_OK) return st;
     }
     p.k = k;
     p.v = v;

@@ -39,10 +39,10 @@ __device__ int g_trace_n[kTraceTracks];
 
 // ----------------------------------------------------------------- band kernel params
 // A segment is one (head, residue class) of the dilated window: rows
-// i = r + delta*m for m in [0, n_r).  Its work items are pairs of
-// consecutive 128-row tiles of m (256 rows).
+// i = r + delta*m for m in [0, n_r).  Its work items are its 128-row tiles
+// (D = 64) or pairs of consecutive tiles (D = 128).
 struct BandSeg {
-  int32_t h, r, delta, n_r, pairs, set, begin, pad_;
+  int32_t h, r, delta, n_r, items, set, begin, pad_;
 };
 
 struct BandParams {
@@ -85,6 +85,9 @@ struct LaunchCtx {
 
 // All return LF_OK or an error status and set the thread's message.
 lf_status launch_band_tc(const BandParams& p, int d, int grid, cudaStream_t s);
+int band_ctas_per_sm(int d);  // resident band-kernel CTAs per SM
+int band_entry_keys(int d);   // keys per K/V entry (the TMA box height)
+int band_rows_per_item(int d);  // query rows per band work item
 lf_status launch_band_simt_f32(const SimtParams& p, const float* q, const float* k, const float* v,
                                float* out, cudaStream_t s);
 template <typename T>
