@@ -49,6 +49,10 @@
 namespace lf {
 namespace ringk {
 
+// Global positions kept in shared memory (the rest, if any, are read from
+// the kernel parameters).
+constexpr int kGSmem = 1024;
+
 // D = 64: two CTAs per SM (so that two softmax warps share each SM
 // sub-partition and hide each other's latencies), 64-key entries, 256 TMEM
 // columns each.  D = 128: one CTA per SM, 128-key entries, all 512 columns.
@@ -68,12 +72,21 @@ struct BandCfg {
   static constexpr int kOffV = kOffK + kKSt * kTile;
   static constexpr int kOffVT = kOffV + kVSt * kTile;
   static constexpr int kOffBar = kOffVT + kTSt * kTile;
-  // q_full[2], q_empty[2], k_full[4], k_empty[4], v_full[4], v_empty[4],
-  // vt_full[4], vt_empty[4], v_land, s_full[3], p_full[3], pv_done[0], o_empty, fin, pv_done[1]
-  static constexpr int kNumBar = 2 + 2 + 4 * 6 + 1 + 3 + 3 + 1 + 1 + 1 + 1;
+  // q_full[2], q_empty[2], k_full[4], (unused)[4], v_full[4], v_empty[4],
+  // vt_full[4], pv_done[4], v_land, s_full[3], p_full[3], (unused), o_empty, fin
+  static constexpr int kNumBar = 2 + 2 + 4 * 6 + 1 + 3 + 3 + 1 + 1 + 1;
   static_assert(kKSt <= 4 && kVSt <= 4 && kTSt <= 4 && kQBuf <= 2 && kSBuf <= 3, "barrier arrays");
+  // A K slot is free once the S product that read it is done, and a V^T slot
+  // once its P.V product is done: the S and P.V completions are those of the
+  // K and V^T slots only while the rings are as deep as s_full and pv_done.
+  static_assert(D != 64 || (kKSt == kSBuf && kTSt == 4), "K ring = S buffers, V^T ring = pv_done barriers");
   static constexpr int kOffMisc = kOffBar + kNumBar * 8;
-  static constexpr int kSmem = kOffMisc + 16 + kMaxSeg * (int)sizeof(BandSeg) + 1024;  // + slack to align the base
+  // after the barriers: TMEM address and abort flag (16 bytes), the segment
+  // table, the batch rows' padding and the first kGSmem global positions
+  static constexpr int kOffSeg = kOffMisc + 16;
+  static constexpr int kOffPad = kOffSeg + kMaxSeg * (int)sizeof(BandSeg);
+  static constexpr int kOffGidx = kOffPad + kMaxBatch * 4;
+  static constexpr int kSmem = kOffGidx + kGSmem * 4 + 1024;  // + slack to align the base
   static constexpr int kTmemCols = (D == 64) ? 256 : 512;
   static constexpr uint32_t kColO = kSBuf * kE;     // S buffers at kE * b, then O (D columns)
   static_assert(kColO + D <= kTmemCols, "TMEM budget");
@@ -82,6 +95,18 @@ struct BandCfg {
 
 // Everything the roles need to know about one work item.  Computed the same
 // way by every role from the item number alone.
+// The launch's lookup tables, copied to shared memory at kernel start (a
+// data-dependent read of the kernel parameters would miss the constant cache).
+struct Tables {
+  const BandSeg* seg;
+  const int32_t* pad;   // [B] padding of each batch row
+  const int32_t* gidx;  // [min(G, kGSmem)] global positions
+};
+
+__device__ __forceinline__ int gidx_at(const BandParams& p, const Tables& tb, int i) {
+  return i < kGSmem ? tb.gidx[i] : p.gidx[i];
+}
+
 struct TileItem {
   int b, h, r, delta, n_r, set, m0, Lb, Lm, bh;
   bool act;     // the tile has at least one valid row
@@ -91,20 +116,19 @@ struct TileItem {
   int nE;       // entries: nU band entries, then ceil(gcnt / kE) global entries
 };
 
-__device__ __forceinline__ int upper_bound_gidx(const BandParams& p, int lim) {
+__device__ __forceinline__ int upper_bound_gidx(const BandParams& p, const Tables& tb, int lim) {
   // number of global positions <= lim (gidx is strictly increasing)
   int lo = 0, hi = p.G;
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
-    if (p.gidx[mid] <= lim) lo = mid + 1; else hi = mid;
+    if (gidx_at(p, tb, mid) <= lim) lo = mid + 1; else hi = mid;
   }
   return lo;
 }
 
-// `segs`: the launch's segment table, copied to shared memory at kernel start
-// (a search over the kernel parameters would miss the constant cache).
 template <int kE>
-__device__ __forceinline__ TileItem decode_tile(const BandParams& p, const BandSeg* segs, int item) {
+__device__ __forceinline__ TileItem decode_tile(const BandParams& p, const Tables& tb, int item) {
+  const BandSeg* segs = tb.seg;
   TileItem it;
   it.b = item / p.items_per_b;
   const int rem = item - it.b * p.items_per_b;
@@ -121,7 +145,7 @@ __device__ __forceinline__ TileItem decode_tile(const BandParams& p, const BandS
   it.set = sg.set;
   it.m0 = (rem - sg.begin) * 128;
   it.bh = it.b * p.H + it.h;
-  it.Lb = p.n - p.pad[it.b];
+  it.Lb = p.n - tb.pad[it.b];
   const int Lm = (it.Lb > it.r) ? (it.Lb - it.r + it.delta - 1) / it.delta : 0;
   it.Lm = min(Lm, it.n_r);
   it.act = it.m0 < it.Lm;
@@ -137,7 +161,7 @@ __device__ __forceinline__ TileItem decode_tile(const BandParams& p, const BandS
   it.nU = (it.khi - it.klo) / kE + 1;
   int glim = it.Lb - 1;
   if (p.causal) glim = min(glim, it.r + it.delta * qlast);
-  it.gcnt = (p.G > 0) ? upper_bound_gidx(p, glim) : 0;
+  it.gcnt = (p.G > 0) ? upper_bound_gidx(p, tb, glim) : 0;
   it.nE = it.nU + (it.gcnt + kE - 1) / kE;
   return it;
 }
@@ -163,23 +187,27 @@ struct BandSmem {
   __device__ __forceinline__ uint32_t q_full(int b) const { return bar(0 + b); }
   __device__ __forceinline__ uint32_t q_empty(int b) const { return bar(2 + b); }
   __device__ __forceinline__ uint32_t k_full(int s) const { return bar(4 + s); }
-  __device__ __forceinline__ uint32_t k_empty(int s) const { return bar(8 + s); }
   __device__ __forceinline__ uint32_t v_full(int s) const { return bar(12 + s); }
   __device__ __forceinline__ uint32_t v_empty(int s) const { return bar(16 + s); }
   __device__ __forceinline__ uint32_t vt_full(int s) const { return bar(20 + s); }
-  __device__ __forceinline__ uint32_t vt_empty(int s) const { return bar(24 + s); }
   __device__ __forceinline__ uint32_t v_land() const { return bar(28); }
   __device__ __forceinline__ uint32_t s_full(int b) const { return bar(29 + b); }
   __device__ __forceinline__ uint32_t p_full(int b) const { return bar(32 + b); }
-  // completion of the P.V of entry k arrives on pv_done(k & 1): the softmax
-  // takes them in order up to one entry behind, and with two barriers neither
-  // runs more than one phase ahead of it
-  __device__ __forceinline__ uint32_t pv_done(uint32_t k) const { return (k & 1) ? bar(38) : bar(35); }
+  // Completion of the P.V of entry k arrives on pv_done(k & 3); it also frees
+  // V^T slot k % 4.  The softmax waits only for the completions it needs (the
+  // previous entry's before it rescales O, the last one before the epilogue);
+  // the transposer waits for the one four entries back.  A waiter for entry k
+  // knows that the P.V of entry k - 4 is done and that of k + 4 cannot be, so
+  // the barrier is in the phase of entry k.
+  __device__ __forceinline__ uint32_t pv_done(uint32_t k) const { return bar(24 + (k & 3)); }
   __device__ __forceinline__ uint32_t o_empty() const { return bar(36); }
   __device__ __forceinline__ uint32_t fin() const { return bar(37); }
   __device__ __forceinline__ uint32_t* tmem_holder() const { return reinterpret_cast<uint32_t*>(base + C::kOffMisc); }
   __device__ __forceinline__ volatile int* abort_flag() const { return reinterpret_cast<volatile int*>(base + C::kOffMisc + 4); }
-  __device__ __forceinline__ BandSeg* segs() const { return reinterpret_cast<BandSeg*>(base + C::kOffMisc + 16); }
+  __device__ __forceinline__ BandSeg* segs() const { return reinterpret_cast<BandSeg*>(base + C::kOffSeg); }
+  __device__ __forceinline__ int32_t* pad() const { return reinterpret_cast<int32_t*>(base + C::kOffPad); }
+  __device__ __forceinline__ int32_t* gidx() const { return reinterpret_cast<int32_t*>(base + C::kOffGidx); }
+  __device__ __forceinline__ Tables tables() const { return Tables{segs(), pad(), gidx()}; }
 };
 
 // 16-byte chunk `ch` of row `row` inside a [rows, D] bf16 tile stored as D/64
@@ -204,6 +232,7 @@ __device__ void band_producer(const BandParams& p, const BandSmem<D>& sm, int la
   using C = BandCfg<D>;
   constexpr int kSt = kIsV ? C::kVSt : C::kKSt;
   volatile int* abort = sm.abort_flag();
+  const Tables tb = sm.tables();
   uint32_t kv = 0, q_it = 0, land = 0;
   int land_pending = -1;  // v_land phase of a zeroing load not yet seen to land
   int last_fill[kSt], last_q[C::kQBuf];
@@ -214,37 +243,84 @@ __device__ void band_producer(const BandParams& p, const BandSmem<D>& sm, int la
   bool ok = true;
   Tracer tr;
   if (blockIdx.x == 0 && lane == 0) tr.track = kIsV ? 5 : 3;
+  Prof pf;
+
+  // Query tiles run one item ahead: the next active item's Q is issued as
+  // soon as its buffer is free (polled between the K loads of the current
+  // item), so that its latency hides behind a whole item.
+  int q_item = blockIdx.x;  // the next item whose Q is to be issued
+  bool q_have = false;      // ... and it exists (is active)
+  TileItem qt;              // its description
+  auto q_seek = [&]() {
+    q_have = false;
+    for (; q_item < p.total_items; q_item += gridDim.x) {
+      qt = decode_tile<C::kE>(p, tb, q_item);
+      if (qt.act) { q_have = true; return; }
+    }
+  };
+  // Issues the pending Q if its buffer is free (waiting for that if `block`);
+  // false on abort.
+  auto q_issue = [&](bool block) -> bool {
+    const int qb = q_it % C::kQBuf;
+    const uint32_t par = ((q_it / C::kQBuf) & 1) ^ 1;
+    if (block) {
+      if (!warp_wait(sm.q_empty(qb), par, abort, kRoleProducer)) return false;
+    } else if (!__all_sync(0xffffffffu, mbar_test_wait(sm.q_empty(qb), par))) {
+      return true;
+    }
+    if (lane == 0) {
+      mbar_arrive_expect_tx(sm.q_full(qb), C::kTileQ);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_3d(sm.q(qb) + c * 16384, &p.tq[qt.set], c * 64, qt.m0, qt.bh, sm.q_full(qb));
+    }
+    last_q[qb] = (int)q_it;
+    ++q_it;
+    q_item += gridDim.x;
+    q_seek();
+    return true;
+  };
+  if (!kIsV) q_seek();
+  uint32_t n_act = 0;  // active items started
 
   for (int item = blockIdx.x; ok && item < p.total_items; item += gridDim.x) {
-    const TileItem it = decode_tile<C::kE>(p, sm.segs(), item);
+    const TileItem it = decode_tile<C::kE>(p, tb, item);
     if (!it.act) continue;
-
-    if (!kIsV) {
-      const int qb = q_it % C::kQBuf;
-      if (!warp_wait(sm.q_empty(qb), ((q_it / C::kQBuf) & 1) ^ 1, abort, kRoleProducer)) { ok = false; break; }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(sm.q_full(qb), C::kTileQ);
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sm.q(qb) + c * 16384, &p.tq[it.set], c * 64, it.m0, it.bh, sm.q_full(qb));
-      }
-      last_q[qb] = (int)q_it;
-      ++q_it;
-    }
+    if (!kIsV && q_it == n_act && !q_issue(true)) { ok = false; break; }  // this item's Q
+    ++n_act;
 
     const __nv_bfloat16* src = (kIsV ? p.v : p.k) + (size_t)it.bh * p.n * D;
     const CUtensorMap* map = kIsV ? &p.tv[it.set] : &p.tk[it.set];
     constexpr int CH = D / 8;  // 16-byte chunks per row
 
     for (int e = 0; e < it.nE; ++e, ++kv) {
+      if (!kIsV && q_it == n_act && q_have && !q_issue(false)) { ok = false; break; }  // the next item's Q
       const int slot = kv % kSt;
       const uint32_t full = kIsV ? sm.v_full(slot) : sm.k_full(slot);
-      const uint32_t empty = kIsV ? sm.v_empty(slot) : sm.k_empty(slot);
+      // a K slot is free when the S product of the entry kKSt back (same S buffer) is done
+      const uint32_t empty = kIsV ? sm.v_empty(slot) : sm.s_full(slot);
       const uint32_t dst = kIsV ? sm.v(slot) : sm.k(slot);
       uint8_t* dst_ptr = kIsV ? sm.v_ptr(slot) : sm.k_ptr(slot);
+      // A global entry is gathered row by row with plain loads; the first
+      // kPre 16-byte chunks of every lane are read before the wait for the
+      // slot, so that their latency hides behind it.
+      constexpr int kPre = 4;
+      uint4 pre[kPre];
+      if (e >= it.nU) {
+        const int gt = e - it.nU;
+        const int cnt = global_count<C::kE>(it, e);
+#pragma unroll
+        for (int j = 0; j < kPre; ++j) {
+          const int idx = lane + 32 * j, row = idx / CH, ch = idx - (idx / CH) * CH;
+          pre[j] = make_uint4(0, 0, 0, 0);
+          if (row < cnt) pre[j] = __ldg(reinterpret_cast<const uint4*>(src + (size_t)gidx_at(p, tb, C::kE * gt + row) * D) + ch);
+        }
+      }
       tr.ev(30);
+      pf.lap(0);
       if (!warp_wait(empty, ((kv / kSt) & 1) ^ 1, abort, kRoleProducer)) { ok = false; break; }
       tr.ev(31);
+      pf.lap(1);
       if (e < it.nU) {
         const int y = it.U0 + C::kE * e;
         // value rows past the last key any row of the tile attends (padding,
@@ -282,11 +358,16 @@ __device__ void band_producer(const BandParams& p, const BandSmem<D>& sm, int la
         // rows of the global tokens visible to the tile, zeros after
         const int gt = e - it.nU;
         const int cnt = global_count<C::kE>(it, e);
-        const int ng = (cnt + 15) & ~15;
-        for (int idx = lane; idx < ng * CH; idx += 32) {
+        const int ng = (cnt + 15) & ~15;  // at least 16 rows: 32 * kPre chunks when D = 64
+#pragma unroll
+        for (int j = 0; j < kPre; ++j) {
+          const int idx = lane + 32 * j, row = idx / CH, ch = idx - (idx / CH) * CH;
+          if (idx < ng * CH) *reinterpret_cast<uint4*>(dst_ptr + sw128_offset(row, ch, C::kE)) = pre[j];
+        }
+        for (int idx = lane + 32 * kPre; idx < ng * CH; idx += 32) {
           const int row = idx / CH, ch = idx - (idx / CH) * CH;
           uint4 x = make_uint4(0, 0, 0, 0);
-          if (row < cnt) x = __ldg(reinterpret_cast<const uint4*>(src + (size_t)p.gidx[C::kE * gt + row] * D) + ch);
+          if (row < cnt) x = __ldg(reinterpret_cast<const uint4*>(src + (size_t)gidx_at(p, tb, C::kE * gt + row) * D) + ch);
           *reinterpret_cast<uint4*>(dst_ptr + sw128_offset(row, ch, C::kE)) = x;
         }
         fence_proxy_async_smem();
@@ -295,9 +376,11 @@ __device__ void band_producer(const BandParams& p, const BandSmem<D>& sm, int la
         last_fill[slot] = -1;  // completed synchronously
       }
       tr.ev(32);
+      pf.lap(2);
     }
   }
   tr.done();
+  pf.flush(kIsV ? 7 : 6, lane == 0);
   // Let every TMA copy this warp issued land before the CTA can exit.
   int dummy = 0;
 #pragma unroll
@@ -325,15 +408,20 @@ __device__ void band_transposer(const BandParams& p, const BandSmem<D>& sm, int 
   const int m = lane >> 3, r = lane & 7;  // this lane addresses row r of matrix m
   Tracer tr;
   if (blockIdx.x == 0 && lane == 0) tr.track = 4;
+  Prof pf;
   for (int item = blockIdx.x; ok && item < p.total_items; item += gridDim.x) {
-    const TileItem it = decode_tile<C::kE>(p, sm.segs(), item);
+    const TileItem it = decode_tile<C::kE>(p, sm.tables(), item);
     if (!it.act) continue;
     for (int e = 0; e < it.nE; ++e, ++kv) {
       const int vs = kv % C::kVSt, ts = kv % C::kTSt;
       tr.ev(40);
+      pf.lap(0);
       if (!warp_wait(sm.v_full(vs), (kv / C::kVSt) & 1, abort, kRoleTranspose)) { ok = false; break; }
-      if (!warp_wait(sm.vt_empty(ts), ((kv / C::kTSt) & 1) ^ 1, abort, kRoleTranspose)) { ok = false; break; }
+      pf.lap(1);
+      // V^T slot ts is free once the P.V of entry kv - kTSt is done
+      if (!warp_wait(sm.pv_done(kv), ((kv / C::kTSt) & 1) ^ 1, abort, kRoleTranspose)) { ok = false; break; }
       tr.ev(41);
+      pf.lap(2);
       const uint32_t src = sm.v(vs), dst = sm.vt(ts);
 #pragma unroll 2
       for (int ki = 0; ki < C::kE / 8; ++ki) {  // 8-key groups
@@ -348,6 +436,7 @@ __device__ void band_transposer(const BandParams& p, const BandSmem<D>& sm, int 
           stmatrix_x4(dblk + dr * 128 + (((ki & 7) ^ (dr & 7)) << 4), x0, x1, x2, x3);
         }
       }
+      pf.lap(3);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -355,9 +444,11 @@ __device__ void band_transposer(const BandParams& p, const BandSmem<D>& sm, int 
         mbar_arrive(sm.vt_full(ts));
       }
       tr.ev(43);
+      pf.lap(4);
     }
   }
   tr.done();
+  pf.flush(5, lane == 0);
 }
 
 // ------------------------------------------------------------------ MMA issuer (one warp)
@@ -375,10 +466,10 @@ struct EntryCursor {
 };
 
 template <int kE>
-__device__ __forceinline__ void cursor_seek(const BandParams& p, const BandSeg* segs, EntryCursor& c) {
+__device__ __forceinline__ void cursor_seek(const BandParams& p, const Tables& tb, EntryCursor& c) {
   // first active item at or after c.item
   while (c.item < p.total_items) {
-    c.it = decode_tile<kE>(p, segs, c.item);
+    c.it = decode_tile<kE>(p, tb, c.item);
     if (c.it.act) return;
     c.item += gridDim.x;
   }
@@ -386,25 +477,25 @@ __device__ __forceinline__ void cursor_seek(const BandParams& p, const BandSeg* 
 }
 
 template <int kE>
-__device__ __forceinline__ void cursor_start(const BandParams& p, const BandSeg* segs, EntryCursor& c) {
+__device__ __forceinline__ void cursor_start(const BandParams& p, const Tables& tb, EntryCursor& c) {
   c.item = blockIdx.x;
   c.e = 0;
   c.g = 0;
   c.kv = 0;
   c.n_items = 0;
   c.valid = true;
-  cursor_seek<kE>(p, segs, c);
+  cursor_seek<kE>(p, tb, c);
 }
 
 template <int kE>
-__device__ __forceinline__ void cursor_next(const BandParams& p, const BandSeg* segs, EntryCursor& c) {
+__device__ __forceinline__ void cursor_next(const BandParams& p, const Tables& tb, EntryCursor& c) {
   ++c.g;
   if (++c.e < c.it.nE) return;
   c.kv += c.it.nE;
   ++c.n_items;
   c.e = 0;
   c.item += gridDim.x;
-  cursor_seek<kE>(p, segs, c);
+  cursor_seek<kE>(p, tb, c);
 }
 
 template <int D>
@@ -419,27 +510,32 @@ __device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tm
   const uint64_t kdesc0 = smem_desc_sw128(sm.k(0), 16, 1024);
   const uint64_t vdesc0 = smem_desc_sw128(sm.vt(0), 16, 1024);
   const uint32_t ot = tmem + C::kColO;
+  const Tables tb = sm.tables();
   uint32_t o_cnt = 0;
   bool ok = true;
   Tracer tr;
   if (blockIdx.x == 0 && (threadIdx.x & 31) == 0) tr.track = 2;
+  Prof pf;
 
   EntryCursor cs, cp;  // S cursor (ahead), P.V cursor
-  cursor_start<C::kE>(p, sm.segs(), cs);
-  cursor_start<C::kE>(p, sm.segs(), cp);
+  cursor_start<C::kE>(p, tb, cs);
+  cursor_start<C::kE>(p, tb, cp);
 
   // S of the entry under cs into buffer cs.g % kSBuf
   auto issue_s = [&]() -> bool {
     const TileItem& it = cs.it;
     const int qb = cs.n_items % C::kQBuf;
+    pf.lap(7);
     if (cs.e == 0) {
       if (!warp_wait(sm.q_full(qb), (cs.n_items / C::kQBuf) & 1, abort, kRoleMma)) return false;
     }
+    pf.lap(1);
     const uint32_t f = cs.kv + cs.e;
     const int ks = f % C::kKSt;
     tr.ev(10);
     if (!warp_wait(sm.k_full(ks), (f / C::kKSt) & 1, abort, kRoleMma)) return false;
     tr.ev(11);
+    pf.lap(2);
     tc_fence_after();
     const uint32_t idesc =
         (cs.e < it.nU) ? idesc_sband : idesc_bf16_f32(128, (global_count<C::kE>(it, cs.e) + 15) & ~15, 0);
@@ -456,11 +552,11 @@ __device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tm
         const uint32_t koff = ((kk >> 2) * (C::kE * 128) + (kk & 3) * 32) >> 4;
         mma_bf16_ss(dt, qd + qoff, kd + koff, idesc, kk > 0);
       }
-      mma_commit(sm.s_full(buf));
-      mma_commit(sm.k_empty(ks));
+      mma_commit(sm.s_full(buf));  // also frees K slot ks (= buf)
       if (last) mma_commit(sm.q_empty(qb));  // the item's last S: Q may be replaced
     }
     __syncwarp();
+    pf.lap(3);
     return true;
   };
 
@@ -471,13 +567,17 @@ __device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tm
     const int ts = f % C::kTSt;
     const uint32_t buf = cp.g % C::kSBuf;
     tr.ev(12);
+    pf.lap(7);
     if (!warp_wait(sm.vt_full(ts), (f / C::kTSt) & 1, abort, kRoleMma)) return false;
+    pf.lap(4);
     if (!warp_wait(sm.p_full(buf), (cp.g / C::kSBuf) & 1, abort, kRoleMma)) return false;
+    pf.lap(5);
     tr.ev(13);
     if (cp.e == 0) {  // O is overwritten: the previous item's epilogue must have read it
       if (!warp_wait(sm.o_empty(), (o_cnt & 1) ^ 1, abort, kRoleMma)) return false;
       ++o_cnt;
     }
+    pf.lap(6);
     tc_fence_after();
     const int ksteps = (cp.e < it.nU) ? C::kE / 16 : ((global_count<C::kE>(it, cp.e) + 15) >> 4);
     const uint32_t pt = tmem + C::kE * buf;  // P over the first kE/2 columns of the buffer
@@ -496,29 +596,31 @@ __device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tm
           mma_bf16_ts(ot, pt + kk * 8, vd + off, idesc_pv, kk > 0 ? 1u : acc0);
         }
       }
-      mma_commit(sm.pv_done(cp.g));
-      mma_commit(sm.vt_empty(ts));
+      mma_commit(sm.pv_done(cp.g));  // also frees V^T slot ts
     }
     __syncwarp();
     tr.ev(14);
+    pf.lap(8);
     return true;
   };
 
   while (ok && cs.valid && cs.g < (uint32_t)C::kSBuf) {
     ok = issue_s();
-    cursor_next<C::kE>(p, sm.segs(), cs);
+    cursor_next<C::kE>(p, tb, cs);
   }
   while (ok && cp.valid) {
     ok = issue_pv();
     if (!ok) break;
-    cursor_next<C::kE>(p, sm.segs(), cp);
+    cursor_next<C::kE>(p, tb, cp);
     // the S buffer just read by that P.V is free: refill up to kSBuf ahead
     while (ok && cs.valid && cs.g < cp.g + C::kSBuf) {
       ok = issue_s();
-      cursor_next<C::kE>(p, sm.segs(), cs);
+      cursor_next<C::kE>(p, tb, cs);
     }
   }
   tr.done();
+  pf.lap(7);
+  pf.flush(4, (threadIdx.x & 31) == 0);
   // Wait until every MMA this warp issued has finished before TMEM is freed.
   if (elect_one()) mma_commit(sm.fin());
   __syncwarp();
@@ -545,15 +647,15 @@ __device__ __forceinline__ uint32_t bit_range(int lo, int hi) {
 // Global entry e, chunk c: bit t set where this row attends global column
 // 32c + t (a global key already in the row's band is counted there, once).
 template <int kE>
-__device__ __forceinline__ uint32_t global_keep(const BandParams& p, const TileItem& it, int e, int c,
-                                                int m_q, bool row_valid) {
+__device__ __forceinline__ uint32_t global_keep(const BandParams& p, const Tables& tb, const TileItem& it,
+                                                int e, int c, int m_q, bool row_valid) {
   const int gt = e - it.nU;
   const int tend = max(0, min(32, global_count<kE>(it, e) - 32 * c));
   const int i_q = it.r + it.delta * m_q;
   uint32_t k = 0;
 #pragma unroll 1
   for (int t = 0; t < tend; ++t) {
-    const int g = p.gidx[kE * gt + 32 * c + t];
+    const int g = gidx_at(p, tb, kE * gt + 32 * c + t);
     const int mg = residue_coord(g, it.r, it.delta);
     const bool in_band = (m_q - mg <= p.half) && (mg - m_q <= p.right);
     k |= (uint32_t)((!p.causal || g <= i_q) && !in_band) << t;
@@ -561,69 +663,73 @@ __device__ __forceinline__ uint32_t global_keep(const BandParams& p, const TileI
   return row_valid ? k : 0u;
 }
 
-// Maximum over the kept columns of a 32-column chunk of raw scores.
-__device__ __forceinline__ float chunk_max(const uint32_t (&x)[32], uint32_t keep, uint32_t whole) {
-  const float NEG_INF = -__int_as_float(0x7f800000);
-  float v[32];
-  if (whole) {
+// Columns of a 64-column entry whose keep bit is clear become -inf (bit t of
+// keep0 is column t, bit t of keep1 column 32 + t).
+__device__ __forceinline__ void mask64(uint32_t (&x)[64], uint32_t keep0, uint32_t keep1) {
+  const uint32_t kNegInf = 0xff800000u;
 #pragma unroll
-    for (int t = 0; t < 32; ++t) v[t] = __uint_as_float(x[t]);
-  } else {
-#pragma unroll
-    for (int t = 0; t < 32; ++t) v[t] = ((keep >> t) & 1u) ? __uint_as_float(x[t]) : NEG_INF;
+  for (int t = 0; t < 32; ++t) {
+    x[t] = ((keep0 >> t) & 1u) ? x[t] : kNegInf;
+    x[32 + t] = ((keep1 >> t) & 1u) ? x[32 + t] : kNegInf;
   }
-  float a = max3f(v[0], v[1], v[2]), b = max3f(v[3], v[4], v[5]), c = max3f(v[6], v[7], v[8]),
-        d = max3f(v[9], v[10], v[11]);
-#pragma unroll
-  for (int t = 12; t < 28; t += 8) {
-    a = max3f(a, v[t], v[t + 1]);
-    b = max3f(b, v[t + 2], v[t + 3]);
-    c = max3f(c, v[t + 4], v[t + 5]);
-    d = max3f(d, v[t + 6], v[t + 7]);
-  }
-  return fmaxf(max3f(a, b, v[28]), max3f(c, d, max3f(v[29], v[30], v[31])));
 }
 
-// P for a 32-column chunk: p = exp2(s * sl2 - m) on the kept columns, 0
-// elsewhere, packed to bf16 pairs; returns the two partial row sums.
-__device__ __forceinline__ float2 chunk_exp(const uint32_t (&x)[32], uint32_t keep, uint32_t whole,
-                                            float sl2, float mneg, uint32_t (&pk)[16]) {
-  const float NEG_INF = -__int_as_float(0x7f800000);
+// Maximum of 64 raw scores (four independent max3 chains).
+__device__ __forceinline__ float max64(const uint32_t (&x)[64]) {
+#define LF_V(i) __uint_as_float(x[i])
+  float a = max3f(LF_V(0), LF_V(1), LF_V(2)), b = max3f(LF_V(3), LF_V(4), LF_V(5)),
+        c = max3f(LF_V(6), LF_V(7), LF_V(8)), d = max3f(LF_V(9), LF_V(10), LF_V(11));
+#pragma unroll
+  for (int t = 12; t < 60; t += 8) {
+    a = max3f(a, LF_V(t), LF_V(t + 1));
+    b = max3f(b, LF_V(t + 2), LF_V(t + 3));
+    c = max3f(c, LF_V(t + 4), LF_V(t + 5));
+    d = max3f(d, LF_V(t + 6), LF_V(t + 7));
+  }
+  a = max3f(a, LF_V(60), LF_V(61));
+  b = max3f(b, LF_V(62), LF_V(63));
+#undef LF_V
+  return fmaxf(max3f(a, b, c), d);
+}
+
+// P for 32 columns of an entry: p = exp2(s * sl2 - m), packed to bf16 pairs
+// (pk[t] holds columns 2t, 2t + 1); returns the sum of the p values.
+// Masked columns hold -inf and give p = 0.
+__device__ __forceinline__ float exp32(const uint32_t* x, float sl2, float mneg, uint32_t (&pk)[16]) {
   const float2 sc2 = make_float2(sl2, sl2), of2 = make_float2(mneg, mneg);
   float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
 #pragma unroll
   for (int t = 0; t < 16; ++t) {
-    float s0 = __uint_as_float(x[2 * t]), s1 = __uint_as_float(x[2 * t + 1]);
-    if (!whole) {
-      s0 = ((keep >> (2 * t)) & 1u) ? s0 : NEG_INF;
-      s1 = ((keep >> (2 * t + 1)) & 1u) ? s1 : NEG_INF;
-    }
-    const float2 y = __ffma2_rn(make_float2(s0, s1), sc2, of2);
+    const float2 y = __ffma2_rn(make_float2(__uint_as_float(x[2 * t]), __uint_as_float(x[2 * t + 1])), sc2, of2);
     const float p0 = ex2_approx(y.x), p1 = ex2_approx(y.y);
     if (t & 1) sb = __fadd2_rn(sb, make_float2(p0, p1));
     else sa = __fadd2_rn(sa, make_float2(p0, p1));
     pk[t] = pack_bf16x2(p0, p1);
   }
-  return __fadd2_rn(sa, sb);
+  const float2 s = __fadd2_rn(sa, sb);
+  return s.x + s.y;
 }
 
 // Softmax and epilogue (one query row per thread; warp quarter wq of TMEM lanes).
 template <int D>
 __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_t tmem, int wq, int lane) {
   using C = BandCfg<D>;
+  static_assert(C::kE == 64, "the softmax holds one 64-column entry in registers");
   volatile int* abort = sm.abort_flag();
+  const Tables tb = sm.tables();
   const int row = wq * 32 + lane;
   const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
   const uint32_t tO = tmem + lane_base + C::kColO;
   const float NEG_INF = -__int_as_float(0x7f800000);
   const float sl2 = p.sl2;
-  uint32_t g = 0, pv_cnt = 0;
+  uint32_t g = 0;
   bool ok = true;
   Tracer tr;
   if (blockIdx.x == 0 && wq == 0 && lane == 0) tr.track = 0;
+  Prof pf;
 
   for (int item = blockIdx.x; ok && item < p.total_items; item += gridDim.x) {
-    const TileItem it = decode_tile<C::kE>(p, sm.segs(), item);
+    const TileItem it = decode_tile<C::kE>(p, sm.tables(), item);
     tr.ev(0);
     const int m_q = it.m0 + row;
     const bool row_exists = m_q < it.n_r;
@@ -637,65 +743,58 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
       continue;
     }
     float m_run = NEG_INF, l_run = 0.f;
+    pf.lap(0);
 
     for (int e = 0; e < it.nE; ++e, ++g) {
-      // ---- keep c: bit t set where this row attends column 32c + t
-      uint32_t keep0, keep1, keep2, keep3;
-      uint32_t onm, fullm;
+      // ---- keep: bit t of keep0 (keep1) set where this row attends column t (32 + t)
+      // mode 0: no row of the warp attends a column of the entry; 1: every
+      // row attends every column; 2: masked
+      uint32_t keep0 = ~0u, keep1 = ~0u;
+      int mode;
       const int kb_w = it.U0 + C::kE * e;
       const int mw = it.m0 + 32 * wq;  // first row of this warp
       if (e < it.nU && mw + 31 < it.Lm && kb_w >= mw + 31 - p.half &&
           kb_w + C::kE - 1 <= min(mw + p.right, it.Lm - 1)) {
-        // every row of the warp attends the whole entry
-        keep0 = keep1 = keep2 = keep3 = ~0u;
-        onm = fullm = (1u << (C::kE / 32)) - 1u;
+        mode = 1;
       } else {
-      if (e < it.nU) {
-        const int clo = m_q - p.half - kb_w;
-        int chi = min(min(m_q + p.right, it.Lm - 1) - kb_w, C::kE - 1);
-        if (!row_valid) chi = clo - 1;
-        keep0 = bit_range(clo, chi);
-        keep1 = bit_range(clo - 32, chi - 32);
-        keep2 = bit_range(clo - 64, chi - 64);
-        keep3 = bit_range(clo - 96, chi - 96);
-      } else {
-        keep0 = global_keep<C::kE>(p, it, e, 0, m_q, row_valid);
-        keep1 = global_keep<C::kE>(p, it, e, 1, m_q, row_valid);
-        keep2 = C::kE > 64 ? global_keep<C::kE>(p, it, e, 2, m_q, row_valid) : 0u;
-        keep3 = C::kE > 64 ? global_keep<C::kE>(p, it, e, 3, m_q, row_valid) : 0u;
-      }
-      // chunks some lane of the warp needs, and chunks every lane needs whole
-      onm = (__any_sync(0xffffffffu, keep0 != 0u) ? 1u : 0u) |
-            (__any_sync(0xffffffffu, keep1 != 0u) ? 2u : 0u) |
-            (__any_sync(0xffffffffu, keep2 != 0u) ? 4u : 0u) |
-            (__any_sync(0xffffffffu, keep3 != 0u) ? 8u : 0u);
-      fullm = (__all_sync(0xffffffffu, keep0 == ~0u) ? 1u : 0u) |
-              (__all_sync(0xffffffffu, keep1 == ~0u) ? 2u : 0u) |
-              (__all_sync(0xffffffffu, keep2 == ~0u) ? 4u : 0u) |
-              (__all_sync(0xffffffffu, keep3 == ~0u) ? 8u : 0u);
+        if (e < it.nU) {
+          const int clo = m_q - p.half - kb_w;
+          int chi = min(min(m_q + p.right, it.Lm - 1) - kb_w, C::kE - 1);
+          if (!row_valid) chi = clo - 1;
+          keep0 = bit_range(clo, chi);
+          keep1 = bit_range(clo - 32, chi - 32);
+        } else {
+          keep0 = global_keep<C::kE>(p, tb, it, e, 0, m_q, row_valid);
+          keep1 = global_keep<C::kE>(p, tb, it, e, 1, m_q, row_valid);
+        }
+        const bool any = __any_sync(0xffffffffu, (keep0 | keep1) != 0u);
+        const bool all = __all_sync(0xffffffffu, (keep0 & keep1) == ~0u);
+        mode = !any ? 0 : (all ? 1 : 2);
       }
 
       const uint32_t buf = g % C::kSBuf;
       const uint32_t tS = tmem + lane_base + C::kE * buf;  // S of this entry, then P
       tr.ev(1);
+      pf.lap(1);
       if (!warp_wait(sm.s_full(buf), (g / C::kSBuf) & 1, abort, kRoleSoftmax)) { ok = false; break; }
       tr.ev(2);
+      pf.lap(2);
       tc_fence_after();
 
-      // ---- pass 1: row maximum of the raw scores (the scale is positive),
-      // one 32-column chunk at a time (TMEM reads are cheap; the loop body
-      // stays small for the instruction cache)
+      // ---- the entry's 64 raw scores stay in registers for both passes
+      uint32_t x[64];
       float mx = NEG_INF;
-#pragma unroll 1
-      for (int c = 0; c < C::kE / 32; ++c) {
-        if (!((onm >> c) & 1u)) continue;
-        uint32_t x[32];
-        tmem_ld32_nw(tS + 32 * c, x);
+      if (mode != 0) {
+        tmem_ld32_nw(tS, x);
+        tmem_ld32_nw(tS + 32, x + 32);
         tmem_wait_ld();
         reg_fence32(x);
-        const uint32_t kc = c == 0 ? keep0 : c == 1 ? keep1 : c == 2 ? keep2 : keep3;
-        mx = fmaxf(mx, chunk_max(x, kc, (fullm >> c) & 1u));
+        reg_fence32(x + 32);
+        pf.lap(3);
+        if (mode == 2) mask64(x, keep0, keep1);
+        mx = max64(x);  // row maximum of the raw scores (the scale is positive)
       }
+      pf.lap(4);
       const float mt = mx * sl2;
       float alpha = 1.f;
       bool resc = false;
@@ -704,70 +803,71 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
         m_run = mt;
         resc = true;
       }
-      // Completions of the P.V products are taken in order, one entry behind
-      // (long done, no stall); a rescale of O also needs the previous entry's.
+      // A rescale of O needs every earlier P.V of the item done; they
+      // complete in order, so the previous entry's completion suffices.  (The
+      // S of this entry was written after the P.V of entry g - 3.)
       const bool any_resc = e > 0 && __any_sync(0xffffffffu, resc);
-      const uint32_t need = any_resc ? g : (g > 0 ? g - 1 : 0);  // P.V products that must be done
-      while (ok && pv_cnt < need) {
-        ok = warp_wait(sm.pv_done(pv_cnt), (pv_cnt >> 1) & 1, abort, kRoleSoftmax);
-        ++pv_cnt;
-      }
-      if (!ok) break;
+      if (any_resc && !warp_wait(sm.pv_done(g - 1), ((g - 1) >> 2) & 1, abort, kRoleSoftmax)) { ok = false; break; }
+      pf.lap(5);
       if (any_resc) {
         tc_fence_after();
-        {
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32_nw(tO + 32 * c, o);
-            tmem_wait_ld();
-            reg_fence32(o);
-            float2* of = reinterpret_cast<float2*>(o);
-            const float2 a2 = make_float2(alpha, alpha);
+        for (int c = 0; c < D / 16; ++c) {
+          uint32_t o[16];
+          tmem_ld16_nw(tO + 16 * c, o);
+          tmem_wait_ld();
+          reg_fence16(o);
+          float2* of = reinterpret_cast<float2*>(o);
+          const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-            for (int t = 0; t < 16; ++t) of[t] = __fmul2_rn(of[t], a2);
-            tmem_st16_nw(tO + 32 * c, o);
-            tmem_st16_nw(tO + 32 * c + 16, o + 16);
-          }
+          for (int t = 0; t < 8; ++t) of[t] = __fmul2_rn(of[t], a2);
+          tmem_st16_nw(tO + 16 * c, o);
+        }
+        // the scores are read again rather than held across the rescale
+        if (mode != 0) {
+          tmem_ld32_nw(tS, x);
+          tmem_ld32_nw(tS + 32, x + 32);
+          tmem_wait_ld();
+          reg_fence32(x);
+          reg_fence32(x + 32);
+          if (mode == 2) mask64(x, keep0, keep1);
         }
       }
       tr.ev(3);
-      // ---- pass 2: P = exp2(s * scale - m) chunk by chunk; P chunk c goes to
-      // columns [16c, 16c + 16) of the buffer, whose scores (chunk c/2) are read
-      const float mneg = (m_run == NEG_INF) ? 0.f : -m_run;
-      float2 sum2 = make_float2(0.f, 0.f);
-#pragma unroll 1
-      for (int c = 0; c < C::kE / 32; ++c) {
+      pf.lap(6);
+      // ---- P = exp2(s * scale - m) over the entry's first 32 columns
+      // (bf16 pairs), aliasing the scores already read
+      if (mode != 0) {
+        const float mneg = (m_run == NEG_INF) ? 0.f : -m_run;
         uint32_t pk[16];
-        if ((onm >> c) & 1u) {
-          uint32_t x[32];
-          tmem_ld32_nw(tS + 32 * c, x);
-          tmem_wait_ld();
-          reg_fence32(x);
-          const uint32_t kc = c == 0 ? keep0 : c == 1 ? keep1 : c == 2 ? keep2 : keep3;
-          sum2 = __fadd2_rn(sum2, chunk_exp(x, kc, (fullm >> c) & 1u, sl2, mneg, pk));
-        } else {
+        float l = exp32(x, sl2, mneg, pk);
+        tmem_st16_nw(tS, pk);
+        l += exp32(x + 32, sl2, mneg, pk);
+        tmem_st16_nw(tS + 16, pk);
+        l_run = l_run * alpha + l;
+      } else {
+        uint32_t pk[16];
 #pragma unroll
-          for (int t = 0; t < 16; ++t) pk[t] = 0u;
-        }
-        tmem_st16_nw(tS + 16 * c, pk);
+        for (int t = 0; t < 16; ++t) pk[t] = 0u;
+        tmem_st16_nw(tS, pk);
+        tmem_st16_nw(tS + 16, pk);
+        l_run = l_run * alpha;
       }
-      l_run = l_run * alpha + (sum2.x + sum2.y);
+      pf.lap(7);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(sm.p_full(buf));
       tr.ev(4);
+      pf.lap(8);
     }
     if (!ok) break;
 
     // ---- epilogue: O / l -> bf16 (32 columns at a time) -> global
     tr.ev(5);
-    while (ok && pv_cnt < g) {  // every P.V of the item (entries before g)
-      ok = warp_wait(sm.pv_done(pv_cnt), (pv_cnt >> 1) & 1, abort, kRoleSoftmax);
-      ++pv_cnt;
-    }
-    if (!ok) break;
+    // every P.V of the item: the last one's completion implies the others'
+    if (!warp_wait(sm.pv_done(g - 1), ((g - 1) >> 2) & 1, abort, kRoleSoftmax)) { ok = false; break; }
+    pf.lap(9);
     tc_fence_after();
     const float inv = (row_valid && l_run > 0.f) ? 1.0f / l_run : 0.f;
     uint32_t ob[D / 2];  // the row in bf16 pairs
@@ -793,8 +893,10 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
                             : make_uint4(0, 0, 0, 0);
     }
     tr.ev(7);
+    pf.lap(10);
   }
   tr.done();
+  pf.flush(wq, lane == 0);
 }
 
 constexpr int kBandThreads = 256;
@@ -820,19 +922,16 @@ __global__ void __launch_bounds__(kBandThreads, BandCfg<D>::kCtaPerSm)
     }
     for (int s = 0; s < 4; ++s) {
       mbar_init(sm.k_full(s), 1);
-      mbar_init(sm.k_empty(s), 1);
       mbar_init(sm.v_full(s), 1);
       mbar_init(sm.v_empty(s), 1);
       mbar_init(sm.vt_full(s), 1);
-      mbar_init(sm.vt_empty(s), 1);
+      mbar_init(sm.pv_done(s), 1);
     }
     mbar_init(sm.v_land(), 1);
     for (int b = 0; b < 3; ++b) {
       mbar_init(sm.s_full(b), 1);
       mbar_init(sm.p_full(b), 4);  // the four softmax warps
     }
-    mbar_init(sm.pv_done(0), 1);
-    mbar_init(sm.pv_done(1), 1);
     mbar_init(sm.o_empty(), 4);
     mbar_init(sm.fin(), 1);
     *sm.abort_flag() = 0;
@@ -840,6 +939,8 @@ __global__ void __launch_bounds__(kBandThreads, BandCfg<D>::kCtaPerSm)
     fence_proxy_async_smem();
   }
   for (int i = threadIdx.x; i < p.nseg; i += blockDim.x) sm.segs()[i] = p.seg[i];
+  for (int i = threadIdx.x; i < p.B; i += blockDim.x) sm.pad()[i] = p.pad[i];
+  for (int i = threadIdx.x; i < min(p.G, kGSmem); i += blockDim.x) sm.gidx()[i] = p.gidx[i];
   if (warp == 0) {
     tmem_alloc(smem_u32(sm.tmem_holder()), C::kTmemCols);
     tmem_relinquish();

@@ -678,6 +678,17 @@ int lf_trace_dump(unsigned long long* dst, int* counts) {
 }
 #endif
 
+#ifdef LF_PROF
+// Diagnostic builds only: copies and clears the phase counters, dst[8][12].
+int lf_prof_dump(unsigned long long* dst) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+  if (cudaMemcpyFromSymbol(dst, lf::g_prof, sizeof(lf::g_prof)) != cudaSuccess) return -1;
+  static const unsigned long long zeros[lf::kProfSlots][lf::kProfPhases] = {};
+  if (cudaMemcpyToSymbol(lf::g_prof, zeros, sizeof(zeros)) != cudaSuccess) return -1;
+  return 0;
+}
+#endif
+
 }  // extern "C"
 
 // The allocation-free variant of lf_attn_fwd (same translation unit).

@@ -37,6 +37,15 @@ __device__ unsigned long long g_trace[kTraceTracks][kTraceLen];
 __device__ int g_trace_n[kTraceTracks];
 #endif
 
+// ----------------------------------------------------------------- phase counters
+// Built only with -DLF_PROF (a diagnostic build, never the product): each
+// role adds the SM cycles it spent in each phase of its loop into
+// g_prof[slot][phase], summed over all CTAs; read back with lf_prof_dump().
+#ifdef LF_PROF
+constexpr int kProfSlots = 8, kProfPhases = 12;
+__device__ unsigned long long g_prof[kProfSlots][kProfPhases];
+#endif
+
 // ----------------------------------------------------------------- band kernel params
 // A segment is one (head, residue class) of the dilated window: rows
 // i = r + delta*m for m in [0, n_r).  Its work items are its 128-row tiles
@@ -128,6 +137,32 @@ struct Tracer {
 };
 #endif
 
+#ifdef LF_PROF
+struct Prof {
+  uint32_t t, acc[kProfPhases];
+  __device__ __forceinline__ Prof() : t((uint32_t)clock()) {
+#pragma unroll
+    for (int i = 0; i < kProfPhases; ++i) acc[i] = 0;
+  }
+  // cycles since the previous lap go to phase k (k a compile-time constant)
+  __device__ __forceinline__ void lap(int k) {
+    const uint32_t now = (uint32_t)clock();
+    acc[k] += now - t;
+    t = now;
+  }
+  __device__ __forceinline__ void flush(int slot, bool writer) {
+    if (!writer) return;
+#pragma unroll
+    for (int i = 0; i < kProfPhases; ++i) atomicAdd(&g_prof[slot][i], (unsigned long long)acc[i]);
+  }
+};
+#else
+struct Prof {
+  __device__ __forceinline__ void lap(int) {}
+  __device__ __forceinline__ void flush(int, bool) {}
+};
+#endif
+
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
@@ -155,6 +190,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uin
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Non-blocking test of the phase.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
@@ -322,6 +370,28 @@ __device__ __forceinline__ void tmem_ld32_nw(uint32_t taddr, uint32_t* r) {
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr)
       : "memory");
+}
+
+// 32 lanes x 16 columns into r[0..16) without waiting; complete with tmem_wait_ld().
+__device__ __forceinline__ void tmem_ld16_nw(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+// reg_fence32 for 16 registers.
+__device__ __forceinline__ void reg_fence16(uint32_t* r) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_ld() {
