@@ -126,8 +126,10 @@ __device__ __forceinline__ int upper_bound_gidx(const BandParams& p, const Table
   return lo;
 }
 
+// Not inlined: every role calls it once per item, and one out-of-line copy
+// keeps the per-entry loops small in the instruction cache.
 template <int kE>
-__device__ __forceinline__ TileItem decode_tile(const BandParams& p, const Tables& tb, int item) {
+__device__ __noinline__ TileItem decode_tile(const BandParams& p, const Tables& tb, int item) {
   const BandSeg* segs = tb.seg;
   TileItem it;
   it.b = item / p.items_per_b;
@@ -635,6 +637,12 @@ __device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tm
 // rescaled rarely; P values stay below 2^kLazy.
 constexpr float kLazy = 8.0f;
 
+__device__ __forceinline__ int floor_div_i(int a, int b) {  // b > 0
+  const int q = a / b;
+  return (a % b != 0 && a < 0) ? q - 1 : q;
+}
+__device__ __forceinline__ int ceil_div_i(int a, int b) { return -floor_div_i(-a, b); }
+
 // Bits [lo, hi] of a 32-bit word (empty when hi < lo); lo, hi may lie outside [0, 31].
 __device__ __forceinline__ uint32_t bit_range(int lo, int hi) {
   lo = max(lo, 0);
@@ -743,6 +751,29 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
       continue;
     }
     float m_run = NEG_INF, l_run = 0.f;
+    // Band entries e in [e_all0, e_all1] are attended whole by every row of
+    // this warp, those outside [e_any0, e_any1] by none of them (the rows'
+    // windows together span keys [mw - half, min(mw_last + right, Lm - 1)]).
+    int e_all0, e_all1, e_any0, e_any1;
+    {
+      const int mw = it.m0 + 32 * wq;  // first row of this warp
+      const int mw_last = min(mw + 31, it.Lm - 1);
+      const int hi_w = min(mw + p.right, it.Lm - 1);  // last key the warp's first row attends
+      if (mw + 31 < it.Lm) {
+        e_all0 = ceil_div_i(mw + 31 - p.half - it.U0, C::kE);
+        e_all1 = floor_div_i(hi_w - (C::kE - 1) - it.U0, C::kE);
+      } else {
+        e_all0 = 1;
+        e_all1 = 0;
+      }
+      if (mw < it.Lm) {
+        e_any0 = ceil_div_i(mw - p.half - (C::kE - 1) - it.U0, C::kE);
+        e_any1 = floor_div_i(min(mw_last + p.right, it.Lm - 1) - it.U0, C::kE);
+      } else {
+        e_any0 = 1;
+        e_any1 = 0;
+      }
+    }
     pf.lap(0);
 
     for (int e = 0; e < it.nE; ++e, ++g) {
@@ -751,22 +782,19 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
       // row attends every column; 2: masked
       uint32_t keep0 = ~0u, keep1 = ~0u;
       int mode;
-      const int kb_w = it.U0 + C::kE * e;
-      const int mw = it.m0 + 32 * wq;  // first row of this warp
-      if (e < it.nU && mw + 31 < it.Lm && kb_w >= mw + 31 - p.half &&
-          kb_w + C::kE - 1 <= min(mw + p.right, it.Lm - 1)) {
-        mode = 1;
-      } else {
-        if (e < it.nU) {
-          const int clo = m_q - p.half - kb_w;
-          int chi = min(min(m_q + p.right, it.Lm - 1) - kb_w, C::kE - 1);
+      if (e < it.nU) {
+        mode = (e >= e_all0 && e <= e_all1) ? 1 : (e >= e_any0 && e <= e_any1) ? 2 : 0;
+        if (mode == 2) {
+          const int kb = it.U0 + C::kE * e;
+          const int clo = m_q - p.half - kb;
+          int chi = min(min(m_q + p.right, it.Lm - 1) - kb, C::kE - 1);
           if (!row_valid) chi = clo - 1;
           keep0 = bit_range(clo, chi);
           keep1 = bit_range(clo - 32, chi - 32);
-        } else {
-          keep0 = global_keep<C::kE>(p, tb, it, e, 0, m_q, row_valid);
-          keep1 = global_keep<C::kE>(p, tb, it, e, 1, m_q, row_valid);
         }
+      } else {
+        keep0 = global_keep<C::kE>(p, tb, it, e, 0, m_q, row_valid);
+        keep1 = global_keep<C::kE>(p, tb, it, e, 1, m_q, row_valid);
         const bool any = __any_sync(0xffffffffu, (keep0 | keep1) != 0u);
         const bool all = __all_sync(0xffffffffu, (keep0 & keep1) == ~0u);
         mode = !any ? 0 : (all ? 1 : 2);
@@ -803,38 +831,9 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
         m_run = mt;
         resc = true;
       }
-      // A rescale of O needs every earlier P.V of the item done; they
-      // complete in order, so the previous entry's completion suffices.  (The
-      // S of this entry was written after the P.V of entry g - 3.)
       const bool any_resc = e > 0 && __any_sync(0xffffffffu, resc);
-      if (any_resc && !warp_wait(sm.pv_done(g - 1), ((g - 1) >> 2) & 1, abort, kRoleSoftmax)) { ok = false; break; }
       pf.lap(5);
-      if (any_resc) {
-        tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < D / 16; ++c) {
-          uint32_t o[16];
-          tmem_ld16_nw(tO + 16 * c, o);
-          tmem_wait_ld();
-          reg_fence16(o);
-          float2* of = reinterpret_cast<float2*>(o);
-          const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-          for (int t = 0; t < 8; ++t) of[t] = __fmul2_rn(of[t], a2);
-          tmem_st16_nw(tO + 16 * c, o);
-        }
-        // the scores are read again rather than held across the rescale
-        if (mode != 0) {
-          tmem_ld32_nw(tS, x);
-          tmem_ld32_nw(tS + 32, x + 32);
-          tmem_wait_ld();
-          reg_fence32(x);
-          reg_fence32(x + 32);
-          if (mode == 2) mask64(x, keep0, keep1);
-        }
-      }
       tr.ev(3);
-      pf.lap(6);
       // ---- P = exp2(s * scale - m) over the entry's first 32 columns
       // (bf16 pairs), aliasing the scores already read
       if (mode != 0) {
@@ -854,6 +853,27 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
         l_run = l_run * alpha;
       }
       pf.lap(7);
+      // ---- O *= alpha before the P.V of this entry adds to it; that needs
+      // every earlier P.V of the item done, and they complete in order, so
+      // the previous entry's completion suffices.  (The S of this entry was
+      // written after the P.V of entry g - 3.)
+      if (any_resc) {
+        if (!warp_wait(sm.pv_done(g - 1), ((g - 1) >> 2) & 1, abort, kRoleSoftmax)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < D / 16; ++c) {
+          uint32_t o[16];
+          tmem_ld16_nw(tO + 16 * c, o);
+          tmem_wait_ld();
+          reg_fence16(o);
+          float2* of = reinterpret_cast<float2*>(o);
+          const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+          for (int t = 0; t < 8; ++t) of[t] = __fmul2_rn(of[t], a2);
+          tmem_st16_nw(tO + 16 * c, o);
+        }
+      }
+      pf.lap(6);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
