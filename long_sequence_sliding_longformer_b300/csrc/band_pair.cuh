@@ -680,10 +680,21 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
     const PairItem it = decode_pair(p, sm.segs(), item);
     tr.ev(0);
     const int m_q = it.m0 + 128 * X + row;
-    const bool row_exists = m_q < it.n_r;
+    // rows at the positions of global tokens are written by the global-row
+    // pass, which may run at the same time: this kernel leaves them alone
+    bool write_row = m_q < it.n_r;
+    if (p.G > 0) {
+      const int m_t = it.m0 + 128 * X;
+      const int i_lo = it.r + it.delta * m_t;
+      const int i_hi = it.r + it.delta * min(m_t + 127, it.n_r - 1);
+      if (m_t < it.n_r && upper_bound_gidx(p, i_hi) > upper_bound_gidx(p, i_lo - 1) && write_row) {
+        const int i_q = it.r + it.delta * m_q;
+        if (upper_bound_gidx(p, i_q) > upper_bound_gidx(p, i_q - 1)) write_row = false;
+      }
+    }
     const bool row_valid = m_q < it.Lm;
     if (it.zero || !(X ? it.act[1] : it.act[0])) {
-      if (row_exists) {
+      if (write_row) {
         uint4* orow = reinterpret_cast<uint4*>(p.out + ((size_t)it.bh * p.n + it.r + (size_t)it.delta * m_q) * D);
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
@@ -860,7 +871,7 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
       for (int t = 0; t < 16; ++t) ob[16 * c + t] = pack_bf16x2(of[2 * t] * inv, of[2 * t + 1] * inv);
     }
     tc_fence_before();
-    if (row_exists) {
+    if (write_row) {
       uint4* orow = reinterpret_cast<uint4*>(p.out + ((size_t)it.bh * p.n + it.r + (size_t)it.delta * m_q) * D);
       // padded rows (inv = 0) are written as zeros; O is finite there since
       // every value row such a row could meet is finite or zeroed

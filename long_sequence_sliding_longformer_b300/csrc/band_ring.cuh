@@ -740,11 +740,21 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
     const TileItem it = decode_tile<C::kE>(p, sm.tables(), item);
     tr.ev(0);
     const int m_q = it.m0 + row;
-    const bool row_exists = m_q < it.n_r;
+    // rows at the positions of global tokens are written by the global-row
+    // pass, which may run at the same time: this kernel leaves them alone
+    bool write_row = m_q < it.n_r;
+    if (p.G > 0) {
+      const int i_lo = it.r + it.delta * it.m0;
+      const int i_hi = it.r + it.delta * min(it.m0 + 127, it.n_r - 1);
+      if (upper_bound_gidx(p, tb, i_hi) > upper_bound_gidx(p, tb, i_lo - 1) && write_row) {
+        const int i_q = it.r + it.delta * m_q;
+        if (upper_bound_gidx(p, tb, i_q) > upper_bound_gidx(p, tb, i_q - 1)) write_row = false;
+      }
+    }
     const bool row_valid = m_q < it.Lm;
     uint4* orow = reinterpret_cast<uint4*>(p.out + ((size_t)it.bh * p.n + it.r + (size_t)it.delta * m_q) * D);
     if (!it.act) {
-      if (row_exists) {
+      if (write_row) {
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
       }
@@ -904,7 +914,7 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(sm.o_empty());
-    if (row_exists) {
+    if (write_row) {
       // padded rows (inv = 0) are written as zeros; O is finite there since
       // every value row such a row could meet is finite or zeroed
 #pragma unroll

@@ -5,13 +5,16 @@
 // its own projections: softmax(qg[g] . kg[j] / sqrt(d)) averaged over vg[j].
 // These few rows are long (n keys each), so the keys are split across CTAs:
 //
-//   global_partial_kernel  grid (key chunks, query blocks, B*H).  Each CTA
-//       scores up to 8 global queries against its chunk of keys, keeps a
-//       running (max, sum, weighted value sum) over its sub-chunks of 128 keys
-//       and writes that partial state to a scratch buffer.
-//   global_merge_kernel    grid (G, B*H).  Merges the partials of one row in
+//   partial pass  grid (key chunks, query blocks, B*H).  Each CTA scores a
+//       block of global queries against its chunk of keys, keeps a running
+//       (max, sum, weighted value sum) and writes that partial state to a
+//       scratch buffer.
+//   merge         done by the last CTA of each (query block, B*H) pair to
+//       finish (a counter per pair): it merges the partials of its rows in
 //       increasing chunk order (a fixed order: results are deterministic),
-//       normalises and writes the row of `out` at the token's position.
+//       normalises and writes the rows of `out` at the tokens' positions.
+//       The band kernels leave those rows alone, so the whole pass may run
+//       beside them.
 //
 // Scores are kept in the exp2 domain (scaled by log2(e)/sqrt(d)).
 #pragma once
@@ -40,11 +43,55 @@ template <>
 __device__ __forceinline__ void from_f<__nv_bfloat16>(__nv_bfloat16* dst, float x) { *dst = __float2bfloat16_rn(x); }
 
 // Scratch layout: per (bh, chunk, g): [m, l, acc[0..d)] as fp32, d + 2 floats.
+//
+// Called by every thread of a partial-pass CTA once its partial state is
+// written.  The last CTA of query block `qblk` of row set `bh` to get here
+// (counters[bh * nqb + qblk] counts them; zero before the pass) merges the
+// chunks of rows g0 .. g0 + gq - 1 and writes them to `out`.
+template <typename T>
+__device__ void merge_if_last(const PatternParams& p, const float* ws, T* __restrict__ out,
+                              unsigned* counters, int nchunks, int nqb, int qblk, int g0, int gq,
+                              int64_t bh) {
+  __shared__ unsigned s_last;
+  __threadfence();  // this CTA's partial state is visible before it is counted
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(&counters[bh * nqb + qblk], 1u) == (unsigned)nchunks - 1u;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();  // and every other CTA's is visible to this one
+  const int D = p.d;
+  const int b = (int)(bh / p.H);
+  const int L = p.n - p.pad[b];
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  const int64_t cstride = (int64_t)p.G * (D + 2);
+  for (int idx = threadIdx.x; idx < gq * D; idx += blockDim.x) {
+    const int g = idx / D, c = idx - (idx / D) * D;
+    const float* base = ws + ((bh * nchunks) * p.G + g0 + g) * (D + 2);
+    float M = NEG_INF;
+#pragma unroll 8
+    for (int ch = 0; ch < nchunks; ++ch) M = fmaxf(M, __ldcg(base + ch * cstride));
+    float l = 0.f, a = 0.f;
+    if (M != NEG_INF) {
+#pragma unroll 4
+      for (int ch = 0; ch < nchunks; ++ch) {
+        const float* e = base + ch * cstride;
+        const float me = __ldcg(e), le = __ldcg(e + 1), ae = __ldcg(e + 2 + c);
+        if (me == NEG_INF) continue;  // nothing attended in this chunk: skip, never scale by 0
+        const float f = ex2_approx(me - M);
+        l = fmaf(le, f, l);
+        a = fmaf(ae, f, a);
+      }
+    }
+    const int pos = p.gidx[g0 + g];
+    from_f<T>(out + (bh * p.n + pos) * D + c, (pos < L && l > 0.f) ? a / l : 0.f);
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kGThreads)
 global_partial_kernel(const __grid_constant__ PatternParams p, const T* __restrict__ qg,
                       const T* __restrict__ kg, const T* __restrict__ vg, float* __restrict__ ws,
-                      int nchunks, int chunk) {
+                      T* __restrict__ out, unsigned* counters, int nchunks, int chunk) {
   __shared__ float qs[kGQ][128];
   __shared__ float sc[kGQ][kGSub];
   __shared__ float red[kGThreads / 32][kGQ][128];
@@ -187,6 +234,7 @@ global_partial_kernel(const __grid_constant__ PatternParams p, const T* __restri
     else val = run_acc[g][c - 2];
     ws[((bh * nchunks + c_idx) * p.G + g0 + g) * (D + 2) + c] = val;
   }
+  merge_if_last<T>(p, ws, out, counters, nchunks, gridDim.y, blockIdx.y, g0, gq, bh);
 }
 
 // bf16 streaming variant for a few global queries (NQ <= 8 per CTA).  Each
@@ -202,7 +250,8 @@ global_partial_stream_kernel(const __grid_constant__ PatternParams p,
                              const __nv_bfloat16* __restrict__ qg,
                              const __nv_bfloat16* __restrict__ kg,
                              const __nv_bfloat16* __restrict__ vg, float* __restrict__ ws,
-                             int nchunks, int chunk) {
+                             __nv_bfloat16* __restrict__ out, unsigned* counters, int nchunks,
+                             int chunk) {
   constexpr int CH = D / 8;       // 16-byte chunks per row
   constexpr int KPW = 32 / CH;    // key rows per warp step
   __shared__ float red[kGsWarps][NQ][D + 2];
@@ -352,133 +401,67 @@ global_partial_stream_kernel(const __grid_constant__ PatternParams p,
     }
     ws[((bh * nchunks + c_idx) * p.G + g0 + g) * (D + 2) + col] = val;
   }
-}
-
-// kMergeGroups groups of 128 threads (thread = output column) split the
-// chunks round-robin; each keeps its own running sums, and the groups are
-// added in a fixed order at the end (deterministic).  The chunk loop keeps
-// four independent loads in flight: the kernel is latency-bound.
-constexpr int kMergeGroups = 4;
-
-template <typename T>
-__global__ void __launch_bounds__(128 * kMergeGroups)
-global_merge_kernel(const __grid_constant__ PatternParams p, const float* __restrict__ ws,
-                    T* __restrict__ out, int nchunks) {
-  __shared__ float red_m[4 * kMergeGroups];
-  __shared__ float part_l[kMergeGroups], part_a[kMergeGroups][128];
-  const int g = blockIdx.x;
-  const int64_t bh = blockIdx.y;
-  const int b = (int)(bh / p.H);
-  const int D = p.d;
-  const int L = p.n - p.pad[b];
-  const int pos = p.gidx[g];
-  const float NEG_INF = -__int_as_float(0x7f800000);
-  T* orow = out + (bh * p.n + pos) * D;
-  const int tid = threadIdx.x, c = tid & 127, grp = tid >> 7;
-  const float* base = ws + ((bh * nchunks) * p.G + g) * (D + 2);
-  const int64_t cstride = (int64_t)p.G * (D + 2);
-  // maximum over the chunks, all threads at once
-  float M = NEG_INF;
-  for (int ch = tid; ch < nchunks; ch += 128 * kMergeGroups) M = fmaxf(M, base[ch * cstride]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if ((tid & 31) == 0) red_m[tid >> 5] = M;
-  __syncthreads();
-  M = red_m[0];
-#pragma unroll
-  for (int w = 1; w < 4 * kMergeGroups; ++w) M = fmaxf(M, red_m[w]);
-  float l = 0.f, a = 0.f;
-  if (M != NEG_INF && c < D) {
-    int ch = grp;
-    for (; ch + 3 * kMergeGroups < nchunks; ch += 4 * kMergeGroups) {
-      float me[4], le[4], ae[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float* e = base + (int64_t)(ch + u * kMergeGroups) * cstride;
-        me[u] = e[0];
-        le[u] = e[1];
-        ae[u] = e[2 + c];
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (me[u] == NEG_INF) continue;  // nothing attended in this chunk: skip, never scale by 0
-        const float f = ex2_approx(me[u] - M);
-        l = fmaf(le[u], f, l);
-        a = fmaf(ae[u], f, a);
-      }
-    }
-    for (; ch < nchunks; ch += kMergeGroups) {
-      const float* e = base + (int64_t)ch * cstride;
-      const float me = e[0];
-      if (me == NEG_INF) continue;
-      const float f = ex2_approx(me - M);
-      l = fmaf(e[1], f, l);
-      a = fmaf(e[2 + c], f, a);
-    }
-  }
-  part_a[grp][c] = a;
-  if (c == 0) part_l[grp] = l;
-  __syncthreads();
-  if (grp != 0 || c >= D) return;
-  if (pos >= L) {
-    from_f<T>(orow + c, 0.f);
-    return;
-  }
-  float lt = part_l[0], at = part_a[0][c];
-#pragma unroll
-  for (int q = 1; q < kMergeGroups; ++q) {
-    lt += part_l[q];
-    at += part_a[q][c];
-  }
-  from_f<T>(orow + c, lt > 0.f ? at / lt : 0.f);
+  merge_if_last<__nv_bfloat16>(p, ws, out, counters, nchunks, gridDim.x, blockIdx.x, g0, gq, bh);
 }
 
 // Query-block size of the streaming kernel for a given number of global tokens.
 inline int stream_nq(int G) { return G >= 8 ? 8 : (G >= 4 ? 4 : (G >= 2 ? 2 : 1)); }
 
 template <typename T>
-inline bool launch_partial_stream(const PatternParams&, const T*, const T*, const T*, float*, int,
-                                  int, cudaStream_t) {
+inline bool launch_partial_stream(const PatternParams&, const T*, const T*, const T*, float*, T*,
+                                  unsigned*, int, int, cudaStream_t) {
   return false;  // fp32 inputs use the generic kernel
 }
 
 template <int D>
 inline void launch_stream_d(const PatternParams& p, const __nv_bfloat16* qg, const __nv_bfloat16* kg,
-                            const __nv_bfloat16* vg, float* ws, int nchunks, int chunk,
-                            cudaStream_t s) {
+                            const __nv_bfloat16* vg, float* ws, __nv_bfloat16* out,
+                            unsigned* counters, int nchunks, int chunk, cudaStream_t s) {
   const int nq = stream_nq(p.G);
   dim3 grid((p.G + nq - 1) / nq, nchunks, (unsigned)((int64_t)p.B * p.H));
   switch (nq) {
-    case 1: global_partial_stream_kernel<D, 1><<<grid, kGsWarps * 32, 0, s>>>(p, qg, kg, vg, ws, nchunks, chunk); break;
-    case 2: global_partial_stream_kernel<D, 2><<<grid, kGsWarps * 32, 0, s>>>(p, qg, kg, vg, ws, nchunks, chunk); break;
-    case 4: global_partial_stream_kernel<D, 4><<<grid, kGsWarps * 32, 0, s>>>(p, qg, kg, vg, ws, nchunks, chunk); break;
-    default: global_partial_stream_kernel<D, 8><<<grid, kGsWarps * 32, 0, s>>>(p, qg, kg, vg, ws, nchunks, chunk); break;
+    case 1: global_partial_stream_kernel<D, 1><<<grid, kGsWarps * 32, 0, s>>>(p, qg, kg, vg, ws, out, counters, nchunks, chunk); break;
+    case 2: global_partial_stream_kernel<D, 2><<<grid, kGsWarps * 32, 0, s>>>(p, qg, kg, vg, ws, out, counters, nchunks, chunk); break;
+    case 4: global_partial_stream_kernel<D, 4><<<grid, kGsWarps * 32, 0, s>>>(p, qg, kg, vg, ws, out, counters, nchunks, chunk); break;
+    default: global_partial_stream_kernel<D, 8><<<grid, kGsWarps * 32, 0, s>>>(p, qg, kg, vg, ws, out, counters, nchunks, chunk); break;
   }
 }
 
 template <>
 inline bool launch_partial_stream<__nv_bfloat16>(const PatternParams& p, const __nv_bfloat16* qg,
                                                  const __nv_bfloat16* kg, const __nv_bfloat16* vg,
-                                                 float* ws, int nchunks, int chunk, cudaStream_t s) {
-  if (p.d == 64) launch_stream_d<64>(p, qg, kg, vg, ws, nchunks, chunk, s);
-  else if (p.d == 128) launch_stream_d<128>(p, qg, kg, vg, ws, nchunks, chunk, s);
+                                                 float* ws, __nv_bfloat16* out, unsigned* counters,
+                                                 int nchunks, int chunk, cudaStream_t s) {
+  if (p.d == 64) launch_stream_d<64>(p, qg, kg, vg, ws, out, counters, nchunks, chunk, s);
+  else if (p.d == 128) launch_stream_d<128>(p, qg, kg, vg, ws, out, counters, nchunks, chunk, s);
   else return false;
   return true;
 }
 
+// Counters the global-row pass needs for B*H rows sets of G global tokens
+// (one per query block; at most one per token).
+inline size_t global_counters(int64_t bh, int G) { return (size_t)bh * (size_t)G; }
+
+// The whole global-row pass on stream s: clears the merge counters, then the
+// partial kernel (whose last CTAs merge and write the rows of `out`).
 template <typename T>
-lf_status launch_global_partial(const PatternParams& p, const T* qg, const T* kg, const T* vg,
-                                float* ws, int nchunks, int chunk, cudaStream_t s) {
+lf_status launch_global_rows(const PatternParams& p, const T* qg, const T* kg, const T* vg, T* out,
+                             float* ws, unsigned* counters, int nchunks, int chunk, cudaStream_t s) {
   const int64_t bhs = (int64_t)p.B * p.H;
   if (bhs > 65535 || nchunks > 65535) {
     set_error("global-row kernels: B*H = %lld or %d key chunks exceed the grid limit", (long long)bhs, nchunks);
     return LF_ERR_UNSUPPORTED;
   }
-  if (!launch_partial_stream(p, qg, kg, vg, ws, nchunks, chunk, s)) {
-    dim3 g1(nchunks, (p.G + kGQ - 1) / kGQ, (unsigned)bhs);
-    global_partial_kernel<T><<<g1, kGThreads, 0, s>>>(p, qg, kg, vg, ws, nchunks, chunk);
+  cudaError_t e = cudaMemsetAsync(counters, 0, global_counters(bhs, p.G) * sizeof(unsigned), s);
+  if (e != cudaSuccess) {
+    set_error("clearing the global-row counters: %s", cudaGetErrorString(e));
+    return LF_ERR_CUDA;
   }
-  cudaError_t e = cudaGetLastError();
+  if (!launch_partial_stream(p, qg, kg, vg, ws, out, counters, nchunks, chunk, s)) {
+    dim3 g1(nchunks, (p.G + kGQ - 1) / kGQ, (unsigned)bhs);
+    global_partial_kernel<T><<<g1, kGThreads, 0, s>>>(p, qg, kg, vg, ws, out, counters, nchunks, chunk);
+  }
+  e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("global partial kernel launch: %s", cudaGetErrorString(e));
     return LF_ERR_CUDA;
@@ -487,32 +470,12 @@ lf_status launch_global_partial(const PatternParams& p, const T* qg, const T* kg
   return LF_OK;
 }
 
-template <typename T>
-lf_status launch_global_merge(const PatternParams& p, const float* ws, T* out, int nchunks,
-                              cudaStream_t s) {
-  dim3 g2(p.G, (unsigned)((int64_t)p.B * p.H));
-  global_merge_kernel<T><<<g2, 128 * kMergeGroups, 0, s>>>(p, ws, out, nchunks);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) {
-    set_error("global merge kernel launch: %s", cudaGetErrorString(e));
-    return LF_ERR_CUDA;
-  }
-  count_launch();
-  return LF_OK;
-}
-
-template <typename T>
-lf_status launch_global_rows(const PatternParams& p, const T* qg, const T* kg, const T* vg, T* out,
-                             float* ws, int nchunks, int chunk, cudaStream_t s) {
-  lf_status st = launch_global_partial<T>(p, qg, kg, vg, ws, nchunks, chunk, s);
-  if (st != LF_OK) return st;
-  return launch_global_merge<T>(p, ws, out, nchunks, s);
-}
-
 template lf_status launch_global_rows<float>(const PatternParams&, const float*, const float*,
-                                             const float*, float*, float*, int, int, cudaStream_t);
+                                             const float*, float*, float*, unsigned*, int, int,
+                                             cudaStream_t);
 template lf_status launch_global_rows<__nv_bfloat16>(const PatternParams&, const __nv_bfloat16*,
                                                      const __nv_bfloat16*, const __nv_bfloat16*,
-                                                     __nv_bfloat16*, float*, int, int, cudaStream_t);
+                                                     __nv_bfloat16*, float*, unsigned*, int, int,
+                                                     cudaStream_t);
 
 }  // namespace lf

@@ -283,16 +283,18 @@ static AuxStream* aux_stream() {
   return &a;
 }
 
-// Enqueues the global rows' partial pass on `ps` (after `fork` if set) and
-// records how to merge; the merge runs later on the caller's stream.
-struct GlobalPass {
-  float* ws = nullptr;
-  size_t floats = 0;
-};
-
+// Enqueues the global-row pass (partials and the merge by their last CTAs)
+// on stream `ps`.  Scratch: the partial states of every batch chunk, then
+// their merge counters.
 template <typename T>
-static lf_status global_partials(const Problem& P, float* ws, cudaStream_t ps) {
-  size_t off_ws = 0;
+static lf_status global_pass(const Problem& P, float* ws, cudaStream_t ps) {
+  size_t off_ws = 0, total = 0;
+  for (int b0 = 0; b0 < P.B; b0 += kMaxBatch) {
+    size_t nf = 0;
+    global_chunk(P, std::min(kMaxBatch, P.B - b0), &nf);
+    total += nf;
+  }
+  unsigned* counters = reinterpret_cast<unsigned*>(ws + total);
   for (int b0 = 0; b0 < P.B; b0 += kMaxBatch) {
     const int nb = std::min(kMaxBatch, P.B - b0);
     size_t nf = 0;
@@ -302,31 +304,14 @@ static lf_status global_partials(const Problem& P, float* ws, cudaStream_t ps) {
     fill_pattern(pp, P, b0, nb);
     const size_t off = (size_t)b0 * P.H * P.n * P.d;
     const size_t goff = (size_t)b0 * P.H * P.G * P.d;
-    lf_status st = launch_global_partial<T>(pp, reinterpret_cast<const T*>(P.qg) + goff,
-                                            reinterpret_cast<const T*>(P.kg) + off,
-                                            reinterpret_cast<const T*>(P.vg) + off, ws + off_ws,
-                                            nchunks, (int)chunk, ps);
+    lf_status st = launch_global_rows<T>(pp, reinterpret_cast<const T*>(P.qg) + goff,
+                                         reinterpret_cast<const T*>(P.kg) + off,
+                                         reinterpret_cast<const T*>(P.vg) + off,
+                                         reinterpret_cast<T*>(P.out) + off, ws + off_ws, counters,
+                                         nchunks, (int)chunk, ps);
     if (st != LF_OK) return st;
     off_ws += nf;
-  }
-  return LF_OK;
-}
-
-template <typename T>
-static lf_status global_merges(const Problem& P, const float* ws) {
-  size_t off_ws = 0;
-  for (int b0 = 0; b0 < P.B; b0 += kMaxBatch) {
-    const int nb = std::min(kMaxBatch, P.B - b0);
-    size_t nf = 0;
-    const int64_t chunk = global_chunk(P, nb, &nf);
-    const int nchunks = (int)((P.n + chunk - 1) / chunk);
-    PatternParams pp;
-    fill_pattern(pp, P, b0, nb);
-    const size_t off = (size_t)b0 * P.H * P.n * P.d;
-    lf_status st = launch_global_merge<T>(pp, ws + off_ws, reinterpret_cast<T*>(P.out) + off, nchunks,
-                                          P.stream);
-    if (st != LF_OK) return st;
-    off_ws += nf;
+    counters += global_counters((int64_t)nb * P.H, P.G);
   }
   return LF_OK;
 }
@@ -473,39 +458,33 @@ static lf_status wait_event(cudaStream_t s, cudaEvent_t e) {
 template <typename T>
 static lf_status forward_t(const Problem& P, bool bf16) {
   lf_status st;
-  // ---- global rows: scratch, then the partial pass on a second stream
+  // ---- global rows: scratch and a fork point for the side stream
   float* ws = nullptr;
   AuxStream* aux = nullptr;
   if (P.G > 0) {
     size_t total = 0;
     for (int b0 = 0; b0 < P.B; b0 += kMaxBatch) {
+      const int nb = std::min(kMaxBatch, P.B - b0);
       size_t nf = 0;
-      global_chunk(P, std::min(kMaxBatch, P.B - b0), &nf);
-      total += nf;
+      global_chunk(P, nb, &nf);
+      total += nf * sizeof(float) + global_counters((int64_t)nb * P.H, P.G) * sizeof(unsigned);
     }
-    cudaError_t e = cudaMallocAsync((void**)&ws, total * sizeof(float), P.stream);
+    cudaError_t e = cudaMallocAsync((void**)&ws, total, P.stream);
     if (e != cudaSuccess) {
       cudaGetLastError();
-      set_error("scratch allocation of %zu bytes failed: %s", total * sizeof(float), cudaGetErrorString(e));
+      set_error("scratch allocation of %zu bytes failed: %s", total, cudaGetErrorString(e));
       return LF_ERR_NO_MEMORY;
     }
-    aux = aux_stream();
-    cudaStream_t ps = P.stream;
-    if (aux && record(aux->fork, P.stream) == LF_OK && wait_event(aux->s, aux->fork) == LF_OK) ps = aux->s;
-    else aux = nullptr;
-    st = global_partials<T>(P, ws, ps);
-    if (aux) {
-      // join even on failure so nothing on the side stream outlives the scratch
-      lf_status j = record(aux->join, aux->s);
-      if (j == LF_OK) j = wait_event(P.stream, aux->join);
-      if (st == LF_OK) st = j;
-    }
-    if (st != LF_OK) {
-      cudaFreeAsync(ws, P.stream);
-      return st;
+    // bf16: the band kernels leave the global tokens' rows to this pass, which
+    // can then run beside them; fp32: it runs after the band kernel
+    if (bf16) {
+      aux = aux_stream();
+      if (!(aux && record(aux->fork, P.stream) == LF_OK && wait_event(aux->s, aux->fork) == LF_OK)) aux = nullptr;
     }
   }
-  // ---- band kernel on the caller's stream
+  // ---- band kernel on the caller's stream, launched first so that it takes
+  // the whole GPU; the global-row pass (side stream) then fills the SMs its
+  // last CTAs leave idle
   st = LF_OK;
   if (t_band_start) st = record_timing(t_band_start, P.stream);
   for (int b0 = 0; st == LF_OK && b0 < P.B; b0 += kMaxBatch) {
@@ -524,9 +503,16 @@ static lf_status forward_t(const Problem& P, bool bf16) {
     }
   }
   if (st == LF_OK && t_band_stop) st = record_timing(t_band_stop, P.stream);
-  // ---- merge (after the band kernel, which also wrote the global tokens' rows)
   if (P.G > 0) {
-    if (st == LF_OK) st = global_merges<T>(P, ws);
+    // the global rows beside the band kernel, or after it on the caller's stream
+    lf_status gp = (st == LF_OK) ? global_pass<T>(P, ws, aux ? aux->s : P.stream) : LF_OK;
+    if (aux) {
+      // join even on failure so nothing on the side stream outlives the scratch
+      lf_status j = record(aux->join, aux->s);
+      if (j == LF_OK) j = wait_event(P.stream, aux->join);
+      if (gp == LF_OK) gp = j;
+    }
+    if (st == LF_OK) st = gp;
     cudaError_t fe = cudaFreeAsync(ws, P.stream);
     if (st == LF_OK && fe != cudaSuccess) {
       set_error("scratch free failed: %s", cudaGetErrorString(fe));

@@ -101,7 +101,7 @@ lf_status launch_band_simt_f32(const SimtParams& p, const float* q, const float*
                                float* out, cudaStream_t s);
 template <typename T>
 lf_status launch_global_rows(const PatternParams& p, const T* qg, const T* kg, const T* vg, T* out,
-                             float* ws, int nchunks, int chunk, cudaStream_t s);
+                             float* ws, unsigned* counters, int nchunks, int chunk, cudaStream_t s);
 
 void set_error(const char* fmt, ...);
 void count_launch(int k = 1);

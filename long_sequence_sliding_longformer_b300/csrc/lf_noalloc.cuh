@@ -15,8 +15,8 @@
 // is loaded holds it until the process exits.  Its device address is looked
 // up once per device, on the first call made with that device current.
 // All calls share the array and it keeps whatever the last call left there;
-// the partial kernel writes every entry the merge kernel later reads, so
-// nothing needs clearing.  Two calls whose kernels overlap on the GPU (for
+// the partial kernel writes every partial state the merge later reads, and
+// the merge counters are cleared by each call.  Two calls whose kernels overlap on the GPU (for
 // example on two streams at once) race on the array.
 //
 // Included at the end of lf_attn.cu (the library's single translation unit).
@@ -71,7 +71,8 @@ static int64_t static_scratch_chunk(const Problem& P, int nbat) {
   while (chunk * 2 <= P.n && bh * qblocks * ((P.n + chunk * 2 - 1) / (chunk * 2)) >= 4 * sm_count())
     chunk *= 2;
   auto bytes = [&](int64_t c) {
-    return (size_t)(bh * ((P.n + c - 1) / c) * P.G * (P.d + 2)) * sizeof(float);
+    return (size_t)(bh * ((P.n + c - 1) / c) * P.G * (P.d + 2)) * sizeof(float) +
+           global_counters(bh, P.G) * sizeof(unsigned);
   };
   while (bytes(chunk) > kStaticScratchBytes && chunk < P.n) chunk *= 2;
   if (chunk > P.n) chunk = P.n;
@@ -88,8 +89,9 @@ static lf_status forward_noalloc(const Problem& P) {
     for (int b0 = 0; b0 < P.B; b0 += kMaxBatch) {
       const int nb = std::min(kMaxBatch, P.B - b0);
       if (static_scratch_chunk(P, nb) == 0) {
-        const size_t need = (size_t)nb * P.H * P.G * (P.d + 2) * sizeof(float);
-        set_error("global rows need at least %zu bytes of scratch (B*H*n_global*(d+2) floats); "
+        const size_t need = (size_t)nb * P.H * P.G * ((P.d + 2) * sizeof(float) + sizeof(unsigned));
+        set_error("global rows need at least %zu bytes of scratch (B*H*n_global*(d+2) floats and "
+                  "B*H*n_global counters); "
                   "the static scratch holds %zu bytes",
                   need, kStaticScratchBytes);
         return LF_ERR_UNSUPPORTED;
@@ -120,11 +122,13 @@ static lf_status forward_noalloc(const Problem& P) {
     const int nchunks = (int)((P.n + chunk - 1) / chunk);
     const size_t off = (size_t)b0 * P.H * P.n * P.d;
     const size_t goff = (size_t)b0 * P.H * P.G * P.d;
+    // partial states, then the merge counters
+    unsigned* counters = reinterpret_cast<unsigned*>(ws + (size_t)nb * P.H * nchunks * P.G * (P.d + 2));
     st = launch_global_rows<__nv_bfloat16>(
         pp, reinterpret_cast<const __nv_bfloat16*>(P.qg) + goff,
         reinterpret_cast<const __nv_bfloat16*>(P.kg) + off,
         reinterpret_cast<const __nv_bfloat16*>(P.vg) + off,
-        reinterpret_cast<__nv_bfloat16*>(P.out) + off, ws, nchunks, (int)chunk, P.stream);
+        reinterpret_cast<__nv_bfloat16*>(P.out) + off, ws, counters, nchunks, (int)chunk, P.stream);
     if (st != LF_OK) return st;
   }
   return LF_OK;
