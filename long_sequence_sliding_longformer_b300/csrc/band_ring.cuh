@@ -523,102 +523,109 @@ __device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tm
   cursor_start<C::kE>(p, tb, cs);
   cursor_start<C::kE>(p, tb, cp);
 
-  // S of the entry under cs into buffer cs.g % kSBuf
-  auto issue_s = [&]() -> bool {
+  // S of the entry under cs into buffer cs.g % kSBuf (the MMAs; the caller
+  // has waited for Q and K and runs this on one elected lane)
+  auto mma_s = [&]() {
     const TileItem& it = cs.it;
     const int qb = cs.n_items % C::kQBuf;
-    pf.lap(7);
-    if (cs.e == 0) {
-      if (!warp_wait(sm.q_full(qb), (cs.n_items / C::kQBuf) & 1, abort, kRoleMma)) return false;
-    }
-    pf.lap(1);
     const uint32_t f = cs.kv + cs.e;
     const int ks = f % C::kKSt;
-    tr.ev(10);
-    if (!warp_wait(sm.k_full(ks), (f / C::kKSt) & 1, abort, kRoleMma)) return false;
-    tr.ev(11);
-    pf.lap(2);
-    tc_fence_after();
     const uint32_t idesc =
         (cs.e < it.nU) ? idesc_sband : idesc_bf16_f32(128, (global_count<C::kE>(it, cs.e) + 15) & ~15, 0);
     const uint64_t qd = qdesc0 + qb * kTileQ16;
     const uint64_t kd = kdesc0 + ks * kTile16;
     const uint32_t buf = cs.g % C::kSBuf;
     const uint32_t dt = tmem + C::kE * buf;
-    const bool last = cs.e + 1 == it.nE;
-    if (elect_one()) {
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        // 16 columns of D: 32 bytes within a 64-column block of 128-byte rows
-        const uint32_t qoff = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-        const uint32_t koff = ((kk >> 2) * (C::kE * 128) + (kk & 3) * 32) >> 4;
-        mma_bf16_ss(dt, qd + qoff, kd + koff, idesc, kk > 0);
-      }
-      mma_commit(sm.s_full(buf));  // also frees K slot ks (= buf)
-      if (last) mma_commit(sm.q_empty(qb));  // the item's last S: Q may be replaced
+    for (int kk = 0; kk < D / 16; ++kk) {
+      // 16 columns of D: 32 bytes within a 64-column block of 128-byte rows
+      const uint32_t qoff = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+      const uint32_t koff = ((kk >> 2) * (C::kE * 128) + (kk & 3) * 32) >> 4;
+      mma_bf16_ss(dt, qd + qoff, kd + koff, idesc, kk > 0);
     }
-    __syncwarp();
-    pf.lap(3);
-    return true;
+    mma_commit(sm.s_full(buf));  // also frees K slot ks (= buf)
+    if (cs.e + 1 == it.nE) mma_commit(sm.q_empty(qb));  // the item's last S: Q may be replaced
   };
-
-  // P.V of the entry under cp, P from buffer cp.g % kSBuf
-  auto issue_pv = [&]() -> bool {
+  // waits (by the whole warp) for what the S of the entry under cs reads
+  auto wait_s = [&]() -> bool {
+    const int qb = cs.n_items % C::kQBuf;
+    const uint32_t f = cs.kv + cs.e;
+    if (cs.e == 0 && !warp_wait(sm.q_full(qb), (cs.n_items / C::kQBuf) & 1, abort, kRoleMma)) return false;
+    return warp_wait(sm.k_full(f % C::kKSt), (f / C::kKSt) & 1, abort, kRoleMma);
+  };
+  // P.V of the entry under cp, P from buffer cp.g % kSBuf (one elected lane)
+  auto mma_pv = [&]() {
     const TileItem& it = cp.it;
     const uint32_t f = cp.kv + cp.e;
     const int ts = f % C::kTSt;
     const uint32_t buf = cp.g % C::kSBuf;
-    tr.ev(12);
-    pf.lap(7);
-    if (!warp_wait(sm.vt_full(ts), (f / C::kTSt) & 1, abort, kRoleMma)) return false;
-    pf.lap(4);
-    if (!warp_wait(sm.p_full(buf), (cp.g / C::kSBuf) & 1, abort, kRoleMma)) return false;
-    pf.lap(5);
-    tr.ev(13);
-    if (cp.e == 0) {  // O is overwritten: the previous item's epilogue must have read it
-      if (!warp_wait(sm.o_empty(), (o_cnt & 1) ^ 1, abort, kRoleMma)) return false;
-      ++o_cnt;
-    }
-    pf.lap(6);
-    tc_fence_after();
     const int ksteps = (cp.e < it.nU) ? C::kE / 16 : ((global_count<C::kE>(it, cp.e) + 15) >> 4);
     const uint32_t pt = tmem + C::kE * buf;  // P over the first kE/2 columns of the buffer
     const uint64_t vd = vdesc0 + ts * kTile16;
     const uint32_t acc0 = cp.e > 0 ? 1u : 0u;
-    if (elect_one()) {
-      if (ksteps == C::kE / 16) {
+    if (ksteps == C::kE / 16) {
 #pragma unroll
-        for (int kk = 0; kk < C::kE / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * (D * 128) + (kk & 3) * 32) >> 4;
-          mma_bf16_ts(ot, pt + kk * 8, vd + off, idesc_pv, kk > 0 ? 1u : acc0);
-        }
-      } else {
-        for (int kk = 0; kk < ksteps; ++kk) {
-          const uint32_t off = ((kk >> 2) * (D * 128) + (kk & 3) * 32) >> 4;
-          mma_bf16_ts(ot, pt + kk * 8, vd + off, idesc_pv, kk > 0 ? 1u : acc0);
-        }
+      for (int kk = 0; kk < C::kE / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * (D * 128) + (kk & 3) * 32) >> 4;
+        mma_bf16_ts(ot, pt + kk * 8, vd + off, idesc_pv, kk > 0 ? 1u : acc0);
       }
-      mma_commit(sm.pv_done(cp.g));  // also frees V^T slot ts
+    } else {
+      for (int kk = 0; kk < ksteps; ++kk) {
+        const uint32_t off = ((kk >> 2) * (D * 128) + (kk & 3) * 32) >> 4;
+        mma_bf16_ts(ot, pt + kk * 8, vd + off, idesc_pv, kk > 0 ? 1u : acc0);
+      }
+    }
+    mma_commit(sm.pv_done(cp.g));  // also frees V^T slot ts
+  };
+
+  // the first kSBuf S products
+  while (ok && cs.valid && cs.g < (uint32_t)C::kSBuf) {
+    ok = wait_s();
+    if (!ok) break;
+    tc_fence_after();
+    if (elect_one()) mma_s();
+    __syncwarp();
+    cursor_next<C::kE>(p, tb, cs);
+  }
+  // then per entry: the P.V of the entry under cp and the S of the one kSBuf
+  // ahead (cs), which goes into the buffer that P.V reads (so after it).
+  // Everything the pair needs is tested at once; only if something is not
+  // ready yet are the bounded waits taken one by one.
+  while (ok && cp.valid) {
+    tr.ev(12);
+    pf.lap(7);
+    const bool has_s = cs.valid;
+    const uint32_t fp = cp.kv + cp.e, fs = cs.kv + cs.e;
+    const int qb = cs.n_items % C::kQBuf;
+    // (tests are reads: the ones not needed this time are made anyway and
+    // ignored, so that all five are in flight together)
+    const bool r_vt = mbar_test_wait(sm.vt_full(fp % C::kTSt), (fp / C::kTSt) & 1);
+    const bool r_p = mbar_test_wait(sm.p_full(cp.g % C::kSBuf), (cp.g / C::kSBuf) & 1);
+    const bool r_o = mbar_test_wait(sm.o_empty(), (o_cnt & 1) ^ 1);
+    const bool r_k = mbar_test_wait(sm.k_full(fs % C::kKSt), (fs / C::kKSt) & 1);
+    const bool r_q = mbar_test_wait(sm.q_full(qb), (cs.n_items / C::kQBuf) & 1);
+    const bool ready = r_vt && r_p && (r_o || cp.e != 0) && (!has_s || (r_k && (r_q || cs.e != 0)));
+    if (!__all_sync(0xffffffffu, ready)) {
+      ok = warp_wait(sm.vt_full(fp % C::kTSt), (fp / C::kTSt) & 1, abort, kRoleMma) &&
+           warp_wait(sm.p_full(cp.g % C::kSBuf), (cp.g / C::kSBuf) & 1, abort, kRoleMma);
+      // O is overwritten by the first P.V of an item: the previous item's epilogue must have read it
+      if (ok && cp.e == 0) ok = warp_wait(sm.o_empty(), (o_cnt & 1) ^ 1, abort, kRoleMma);
+      if (ok && has_s) ok = wait_s();
+      if (!ok) break;
+    }
+    if (cp.e == 0) ++o_cnt;
+    tr.ev(13);
+    pf.lap(5);
+    tc_fence_after();
+    if (elect_one()) {
+      mma_pv();
+      if (has_s) mma_s();
     }
     __syncwarp();
     tr.ev(14);
     pf.lap(8);
-    return true;
-  };
-
-  while (ok && cs.valid && cs.g < (uint32_t)C::kSBuf) {
-    ok = issue_s();
-    cursor_next<C::kE>(p, tb, cs);
-  }
-  while (ok && cp.valid) {
-    ok = issue_pv();
-    if (!ok) break;
     cursor_next<C::kE>(p, tb, cp);
-    // the S buffer just read by that P.V is free: refill up to kSBuf ahead
-    while (ok && cs.valid && cs.g < cp.g + C::kSBuf) {
-      ok = issue_s();
-      cursor_next<C::kE>(p, tb, cs);
-    }
+    if (has_s) cursor_next<C::kE>(p, tb, cs);
   }
   tr.done();
   pf.lap(7);
