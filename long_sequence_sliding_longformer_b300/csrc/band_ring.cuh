@@ -523,8 +523,8 @@ __device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tm
   cursor_start<C::kE>(p, tb, cs);
   cursor_start<C::kE>(p, tb, cp);
 
-  // S of the entry under cs into buffer cs.g % kSBuf (the MMAs; the caller
-  // has waited for Q and K and runs this on one elected lane)
+  // S of the entry under cs into buffer cs.g % kSBuf (the MMAs, issued by an
+  // elected lane of the converged warp; the caller has waited for Q and K)
   auto mma_s = [&]() {
     const TileItem& it = cs.it;
     const int qb = cs.n_items % C::kQBuf;
@@ -541,10 +541,10 @@ __device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tm
       // 16 columns of D: 32 bytes within a 64-column block of 128-byte rows
       const uint32_t qoff = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
       const uint32_t koff = ((kk >> 2) * (C::kE * 128) + (kk & 3) * 32) >> 4;
-      mma_bf16_ss(dt, qd + qoff, kd + koff, idesc, kk > 0);
+      mma_bf16_ss_w(dt, qd + qoff, kd + koff, idesc, kk > 0);
     }
-    mma_commit(sm.s_full(buf));  // also frees K slot ks (= buf)
-    if (cs.e + 1 == it.nE) mma_commit(sm.q_empty(qb));  // the item's last S: Q may be replaced
+    mma_commit_w(sm.s_full(buf));  // also frees K slot ks (= buf)
+    if (cs.e + 1 == it.nE) mma_commit_w(sm.q_empty(qb));  // the item's last S: Q may be replaced
   };
   // waits (by the whole warp) for what the S of the entry under cs reads
   auto wait_s = [&]() -> bool {
@@ -553,7 +553,7 @@ __device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tm
     if (cs.e == 0 && !warp_wait(sm.q_full(qb), (cs.n_items / C::kQBuf) & 1, abort, kRoleMma)) return false;
     return warp_wait(sm.k_full(f % C::kKSt), (f / C::kKSt) & 1, abort, kRoleMma);
   };
-  // P.V of the entry under cp, P from buffer cp.g % kSBuf (one elected lane)
+  // P.V of the entry under cp, P from buffer cp.g % kSBuf (elected lane)
   auto mma_pv = [&]() {
     const TileItem& it = cp.it;
     const uint32_t f = cp.kv + cp.e;
@@ -567,15 +567,15 @@ __device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tm
 #pragma unroll
       for (int kk = 0; kk < C::kE / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * (D * 128) + (kk & 3) * 32) >> 4;
-        mma_bf16_ts(ot, pt + kk * 8, vd + off, idesc_pv, kk > 0 ? 1u : acc0);
+        mma_bf16_ts_w(ot, pt + kk * 8, vd + off, idesc_pv, kk > 0 ? 1u : acc0);
       }
     } else {
       for (int kk = 0; kk < ksteps; ++kk) {
         const uint32_t off = ((kk >> 2) * (D * 128) + (kk & 3) * 32) >> 4;
-        mma_bf16_ts(ot, pt + kk * 8, vd + off, idesc_pv, kk > 0 ? 1u : acc0);
+        mma_bf16_ts_w(ot, pt + kk * 8, vd + off, idesc_pv, kk > 0 ? 1u : acc0);
       }
     }
-    mma_commit(sm.pv_done(cp.g));  // also frees V^T slot ts
+    mma_commit_w(sm.pv_done(cp.g));  // also frees V^T slot ts
   };
 
   // the first kSBuf S products
@@ -583,8 +583,7 @@ __device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tm
     ok = wait_s();
     if (!ok) break;
     tc_fence_after();
-    if (elect_one()) mma_s();
-    __syncwarp();
+    mma_s();
     cursor_next<C::kE>(p, tb, cs);
   }
   // then per entry: the P.V of the entry under cp and the S of the one kSBuf
@@ -605,23 +604,31 @@ __device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tm
     const bool r_k = mbar_test_wait(sm.k_full(fs % C::kKSt), (fs / C::kKSt) & 1);
     const bool r_q = mbar_test_wait(sm.q_full(qb), (cs.n_items / C::kQBuf) & 1);
     const bool ready = r_vt && r_p && (r_o || cp.e != 0) && (!has_s || (r_k && (r_q || cs.e != 0)));
-    if (!__all_sync(0xffffffffu, ready)) {
+    if (__all_sync(0xffffffffu, ready)) {
+      tr.ev(13);
+      pf.lap(5);
+      tc_fence_after();
+      mma_pv();
+      if (has_s) mma_s();
+    } else {
+      // the P.V goes as soon as its own inputs are there (the epilogue of
+      // an item waits for its last P.V), then the S
       ok = warp_wait(sm.vt_full(fp % C::kTSt), (fp / C::kTSt) & 1, abort, kRoleMma) &&
            warp_wait(sm.p_full(cp.g % C::kSBuf), (cp.g / C::kSBuf) & 1, abort, kRoleMma);
       // O is overwritten by the first P.V of an item: the previous item's epilogue must have read it
       if (ok && cp.e == 0) ok = warp_wait(sm.o_empty(), (o_cnt & 1) ^ 1, abort, kRoleMma);
-      if (ok && has_s) ok = wait_s();
       if (!ok) break;
+      tr.ev(13);
+      pf.lap(5);
+      tc_fence_after();
+      mma_pv();
+      if (has_s) {
+        if (!wait_s()) { ok = false; break; }
+        tc_fence_after();
+        mma_s();
+      }
     }
     if (cp.e == 0) ++o_cnt;
-    tr.ev(13);
-    pf.lap(5);
-    tc_fence_after();
-    if (elect_one()) {
-      mma_pv();
-      if (has_s) mma_s();
-    }
-    __syncwarp();
     tr.ev(14);
     pf.lap(8);
     cursor_next<C::kE>(p, tb, cp);
