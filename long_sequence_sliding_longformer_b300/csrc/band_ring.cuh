@@ -56,13 +56,17 @@ constexpr int kGSmem = 1024;
 // D = 64: two CTAs per SM (so that two softmax warps share each SM
 // sub-partition and hide each other's latencies), 64-key entries, 256 TMEM
 // columns each.  D = 128: one CTA per SM, 128-key entries, all 512 columns.
+#ifndef LF_RING_E
+#define LF_RING_E 64  // keys per entry at D = 64
+#endif
 template <int D>
 struct BandCfg {
-  static constexpr int kE = (D == 64) ? 64 : 128;   // keys per entry
-  static constexpr int kCtaPerSm = (D == 64) ? 2 : 1;
+  static constexpr bool kWide = (D == 128) || (LF_RING_E == 128);  // 128-key entries, one CTA per SM
+  static constexpr int kE = kWide ? 128 : 64;       // keys per entry
+  static constexpr int kCtaPerSm = kWide ? 1 : 2;
   static constexpr int kQBuf = 2;                  // Q tiles (the next item's Q loads early)
   static constexpr int kKSt = (D == 64) ? 3 : 2;   // K slots
-  static constexpr int kVSt = (D == 64) ? 2 : 1;   // V slots (as loaded: [keys, D])
+  static constexpr int kVSt = (D == 64) ? (kWide ? 3 : 2) : 1;  // V slots (as loaded: [keys, D])
   static constexpr int kTSt = (D == 64) ? 4 : 2;   // V^T slots ([D, keys], the P.V operand)
   static constexpr int kSBuf = 3;                  // S buffers in TMEM
   static constexpr int kTileQ = 128 * D * 2;       // bytes of one [128, D] bf16 query tile
@@ -87,7 +91,7 @@ struct BandCfg {
   static constexpr int kOffPad = kOffSeg + kMaxSeg * (int)sizeof(BandSeg);
   static constexpr int kOffGidx = kOffPad + kMaxBatch * 4;
   static constexpr int kSmem = kOffGidx + kGSmem * 4 + 1024;  // + slack to align the base
-  static constexpr int kTmemCols = (D == 64) ? 256 : 512;
+  static constexpr int kTmemCols = kWide ? 512 : 256;
   static constexpr uint32_t kColO = kSBuf * kE;     // S buffers at kE * b, then O (D columns)
   static_assert(kColO + D <= kTmemCols, "TMEM budget");
   static_assert(kCtaPerSm == 1 || 2 * (kSmem + 1024) <= 233472, "two CTAs per SM must fit");
@@ -685,19 +689,15 @@ __device__ __forceinline__ uint32_t global_keep(const BandParams& p, const Table
   return row_valid ? k : 0u;
 }
 
-// Columns of a 64-column entry whose keep bit is clear become -inf (bit t of
-// keep0 is column t, bit t of keep1 column 32 + t).
-__device__ __forceinline__ void mask64(uint32_t (&x)[64], uint32_t keep0, uint32_t keep1) {
+// Columns of a 32-column chunk whose keep bit is clear become -inf.
+__device__ __forceinline__ void mask32(uint32_t* x, uint32_t keep) {
   const uint32_t kNegInf = 0xff800000u;
 #pragma unroll
-  for (int t = 0; t < 32; ++t) {
-    x[t] = ((keep0 >> t) & 1u) ? x[t] : kNegInf;
-    x[32 + t] = ((keep1 >> t) & 1u) ? x[32 + t] : kNegInf;
-  }
+  for (int t = 0; t < 32; ++t) x[t] = ((keep >> t) & 1u) ? x[t] : kNegInf;
 }
 
 // Maximum of 64 raw scores (four independent max3 chains).
-__device__ __forceinline__ float max64(const uint32_t (&x)[64]) {
+__device__ __forceinline__ float max64(const uint32_t* x) {
 #define LF_V(i) __uint_as_float(x[i])
   float a = max3f(LF_V(0), LF_V(1), LF_V(2)), b = max3f(LF_V(3), LF_V(4), LF_V(5)),
         c = max3f(LF_V(6), LF_V(7), LF_V(8)), d = max3f(LF_V(9), LF_V(10), LF_V(11));
@@ -736,7 +736,8 @@ __device__ __forceinline__ float exp32(const uint32_t* x, float sl2, float mneg,
 template <int D>
 __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_t tmem, int wq, int lane) {
   using C = BandCfg<D>;
-  static_assert(C::kE == 64, "the softmax holds one 64-column entry in registers");
+  static_assert(C::kE == 64 || C::kE == 128, "the softmax holds one entry in registers");
+  constexpr int NC = C::kE / 32;  // 32-column chunks per entry
   volatile int* abort = sm.abort_flag();
   const Tables tb = sm.tables();
   const int row = wq * 32 + lane;
@@ -801,10 +802,12 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
     pf.lap(0);
 
     for (int e = 0; e < it.nE; ++e, ++g) {
-      // ---- keep: bit t of keep0 (keep1) set where this row attends column t (32 + t)
+      // ---- keep[c]: bit t set where this row attends column 32c + t
       // mode 0: no row of the warp attends a column of the entry; 1: every
       // row attends every column; 2: masked
-      uint32_t keep0 = ~0u, keep1 = ~0u;
+      uint32_t keep[NC];
+#pragma unroll
+      for (int c = 0; c < NC; ++c) keep[c] = ~0u;
       int mode;
       if (e < it.nU) {
         mode = (e >= e_all0 && e <= e_all1) ? 1 : (e >= e_any0 && e <= e_any1) ? 2 : 0;
@@ -813,14 +816,19 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
           const int clo = m_q - p.half - kb;
           int chi = min(min(m_q + p.right, it.Lm - 1) - kb, C::kE - 1);
           if (!row_valid) chi = clo - 1;
-          keep0 = bit_range(clo, chi);
-          keep1 = bit_range(clo - 32, chi - 32);
+#pragma unroll
+          for (int c = 0; c < NC; ++c) keep[c] = bit_range(clo - 32 * c, chi - 32 * c);
         }
       } else {
-        keep0 = global_keep<C::kE>(p, tb, it, e, 0, m_q, row_valid);
-        keep1 = global_keep<C::kE>(p, tb, it, e, 1, m_q, row_valid);
-        const bool any = __any_sync(0xffffffffu, (keep0 | keep1) != 0u);
-        const bool all = __all_sync(0xffffffffu, (keep0 & keep1) == ~0u);
+        uint32_t any_bits = 0u, all_bits = ~0u;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          keep[c] = global_keep<C::kE>(p, tb, it, e, c, m_q, row_valid);
+          any_bits |= keep[c];
+          all_bits &= keep[c];
+        }
+        const bool any = __any_sync(0xffffffffu, any_bits != 0u);
+        const bool all = __all_sync(0xffffffffu, all_bits == ~0u);
         mode = !any ? 0 : (all ? 1 : 2);
       }
 
@@ -833,18 +841,22 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
       pf.lap(2);
       tc_fence_after();
 
-      // ---- the entry's 64 raw scores stay in registers for both passes
-      uint32_t x[64];
+      // ---- the entry's raw scores stay in registers for both passes
+      uint32_t x[C::kE];
       float mx = NEG_INF;
       if (mode != 0) {
-        tmem_ld32_nw(tS, x);
-        tmem_ld32_nw(tS + 32, x + 32);
+#pragma unroll
+        for (int c = 0; c < NC; ++c) tmem_ld32_nw(tS + 32 * c, x + 32 * c);
         tmem_wait_ld();
-        reg_fence32(x);
-        reg_fence32(x + 32);
+#pragma unroll
+        for (int c = 0; c < NC; ++c) reg_fence32(x + 32 * c);
         pf.lap(3);
-        if (mode == 2) mask64(x, keep0, keep1);
+        if (mode == 2) {
+#pragma unroll
+          for (int c = 0; c < NC; ++c) mask32(x + 32 * c, keep[c]);
+        }
         mx = max64(x);  // row maximum of the raw scores (the scale is positive)
+        if (NC == 4) mx = fmaxf(mx, max64(x + 64));
       }
       pf.lap(4);
       const float mt = mx * sl2;
@@ -863,17 +875,19 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
       if (mode != 0) {
         const float mneg = (m_run == NEG_INF) ? 0.f : -m_run;
         uint32_t pk[16];
-        float l = exp32(x, sl2, mneg, pk);
-        tmem_st16_nw(tS, pk);
-        l += exp32(x + 32, sl2, mneg, pk);
-        tmem_st16_nw(tS + 16, pk);
+        float l = 0.f;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          l += exp32(x + 32 * c, sl2, mneg, pk);
+          tmem_st16_nw(tS + 16 * c, pk);  // P chunk c over columns [16c, 16c + 16) (already read)
+        }
         l_run = l_run * alpha + l;
       } else {
         uint32_t pk[16];
 #pragma unroll
         for (int t = 0; t < 16; ++t) pk[t] = 0u;
-        tmem_st16_nw(tS, pk);
-        tmem_st16_nw(tS + 16, pk);
+#pragma unroll
+        for (int c = 0; c < NC; ++c) tmem_st16_nw(tS + 16 * c, pk);
         l_run = l_run * alpha;
       }
       pf.lap(7);

@@ -64,22 +64,39 @@ __device__ void merge_if_last(const PatternParams& p, const float* ws, T* __rest
   const int L = p.n - p.pad[b];
   const float NEG_INF = -__int_as_float(0x7f800000);
   const int64_t cstride = (int64_t)p.G * (D + 2);
+  // each thread one (row, column); the chunks are read 16 at a time (all
+  // loads of a block in flight together) and added in chunk order
+  constexpr int kBlk = 16;
   for (int idx = threadIdx.x; idx < gq * D; idx += blockDim.x) {
     const int g = idx / D, c = idx - (idx / D) * D;
     const float* base = ws + ((bh * nchunks) * p.G + g0 + g) * (D + 2);
     float M = NEG_INF;
-#pragma unroll 8
-    for (int ch = 0; ch < nchunks; ++ch) M = fmaxf(M, __ldcg(base + ch * cstride));
+    for (int ch0 = 0; ch0 < nchunks; ch0 += kBlk) {
+      float mv[kBlk];
+#pragma unroll
+      for (int u = 0; u < kBlk; ++u) mv[u] = (ch0 + u < nchunks) ? __ldcg(base + (ch0 + u) * cstride) : NEG_INF;
+#pragma unroll
+      for (int u = 0; u < kBlk; ++u) M = fmaxf(M, mv[u]);
+    }
     float l = 0.f, a = 0.f;
     if (M != NEG_INF) {
-#pragma unroll 4
-      for (int ch = 0; ch < nchunks; ++ch) {
-        const float* e = base + ch * cstride;
-        const float me = __ldcg(e), le = __ldcg(e + 1), ae = __ldcg(e + 2 + c);
-        if (me == NEG_INF) continue;  // nothing attended in this chunk: skip, never scale by 0
-        const float f = ex2_approx(me - M);
-        l = fmaf(le, f, l);
-        a = fmaf(ae, f, a);
+      for (int ch0 = 0; ch0 < nchunks; ch0 += kBlk) {
+        float mv[kBlk], lv[kBlk], av[kBlk];
+#pragma unroll
+        for (int u = 0; u < kBlk; ++u) {
+          const bool in = ch0 + u < nchunks;
+          const float* e = base + (ch0 + u) * cstride;
+          mv[u] = in ? __ldcg(e) : NEG_INF;
+          lv[u] = in ? __ldcg(e + 1) : 0.f;
+          av[u] = in ? __ldcg(e + 2 + c) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kBlk; ++u) {
+          if (mv[u] == NEG_INF) continue;  // nothing attended in this chunk: skip, never scale by 0
+          const float f = ex2_approx(mv[u] - M);
+          l = fmaf(lv[u], f, l);
+          a = fmaf(av[u], f, a);
+        }
       }
     }
     const int pos = p.gidx[g0 + g];
@@ -295,7 +312,7 @@ global_partial_stream_kernel(const __grid_constant__ PatternParams p,
   const int k_end = min(k_begin + chunk, L);
   const uint4* kb = reinterpret_cast<const uint4*>(kg + bh * (int64_t)p.n * D);
   const uint4* vb = reinterpret_cast<const uint4*>(vg + bh * (int64_t)p.n * D);
-  constexpr int U = 4;  // key steps in flight per warp
+  constexpr int U = NQ <= 2 ? 8 : 4;  // key steps in flight per warp
   constexpr int STEP = kGsWarps * KPW;
   for (int j00 = k_begin + warp * KPW; j00 < k_end; j00 += U * STEP) {
    uint4 kxs[U], vxs[U];
