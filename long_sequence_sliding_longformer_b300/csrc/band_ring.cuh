@@ -152,6 +152,24 @@ __device__ __noinline__ TileItem decode_tile(const BandParams& p, const Tables& 
   it.m0 = (rem - sg.begin) * 128;
   it.bh = it.b * p.H + it.h;
   it.Lb = p.n - tb.pad[it.b];
+  if (p.gmode) {
+    // query rows m: global tokens m0 .. m0 + 127 (of nrow_g); keys: [0, Lb)
+    it.Lm = it.Lb;
+    it.act = it.m0 < p.nrow_g && it.Lb > 0;
+    it.gcnt = 0;
+    if (!it.act) {
+      it.nE = it.nU = 0;
+      it.U0 = it.klo = it.khi = 0;
+      return it;
+    }
+    const int qlast = min(it.m0 + 127, p.nrow_g - 1);
+    it.klo = 0;
+    it.khi = p.causal ? min(it.Lb - 1, gidx_at(p, tb, qlast)) : it.Lb - 1;
+    it.U0 = 0;
+    it.nU = it.khi / kE + 1;
+    it.nE = it.nU;
+    return it;
+  }
   const int Lm = (it.Lb > it.r) ? (it.Lb - it.r + it.delta - 1) / it.delta : 0;
   it.Lm = min(Lm, it.n_r);
   it.act = it.m0 < it.Lm;
@@ -757,7 +775,8 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
     const int m_q = it.m0 + row;
     // rows at the positions of global tokens are written by the global-row
     // pass, which may run at the same time: this kernel leaves them alone
-    bool write_row = m_q < it.n_r;
+    bool write_row = p.gmode ? m_q < p.nrow_g : m_q < it.n_r;
+    const int g_pos = (p.gmode && write_row) ? gidx_at(p, tb, m_q) : 0;  // global-row mode: the token's position
     if (p.G > 0) {
       const int i_lo = it.r + it.delta * it.m0;
       const int i_hi = it.r + it.delta * min(it.m0 + 127, it.n_r - 1);
@@ -766,8 +785,9 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
         if (upper_bound_gidx(p, tb, i_q) > upper_bound_gidx(p, tb, i_q - 1)) write_row = false;
       }
     }
-    const bool row_valid = m_q < it.Lm;
-    uint4* orow = reinterpret_cast<uint4*>(p.out + ((size_t)it.bh * p.n + it.r + (size_t)it.delta * m_q) * D);
+    const bool row_valid = p.gmode ? (write_row && g_pos < it.Lb) : m_q < it.Lm;
+    uint4* orow = reinterpret_cast<uint4*>(
+        p.out + ((size_t)it.bh * p.n + (p.gmode ? (size_t)g_pos : it.r + (size_t)it.delta * m_q)) * D);
     if (!it.act) {
       if (write_row) {
 #pragma unroll
@@ -809,7 +829,21 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
 #pragma unroll
       for (int c = 0; c < NC; ++c) keep[c] = ~0u;
       int mode;
-      if (e < it.nU) {
+      if (p.gmode) {
+        // every key in [0, Lb), up to the token itself when causal
+        const int kb = C::kE * e;
+        const int chi = row_valid ? (p.causal ? min(g_pos, it.Lb - 1) : it.Lb - 1) - kb : -1;
+        uint32_t any_bits = 0u, all_bits = ~0u;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          keep[c] = bit_range(-kb - 32 * c, chi - 32 * c);
+          any_bits |= keep[c];
+          all_bits &= keep[c];
+        }
+        const bool any = __any_sync(0xffffffffu, any_bits != 0u);
+        const bool all = __all_sync(0xffffffffu, all_bits == ~0u);
+        mode = !any ? 0 : (all ? 1 : 2);
+      } else if (e < it.nU) {
         mode = (e >= e_all0 && e <= e_all1) ? 1 : (e >= e_any0 && e <= e_any1) ? 2 : 0;
         if (mode == 2) {
           const int kb = it.U0 + C::kE * e;
@@ -998,7 +1032,7 @@ __global__ void __launch_bounds__(kBandThreads, BandCfg<D>::kCtaPerSm)
   }
   for (int i = threadIdx.x; i < p.nseg; i += blockDim.x) sm.segs()[i] = p.seg[i];
   for (int i = threadIdx.x; i < p.B; i += blockDim.x) sm.pad()[i] = p.pad[i];
-  for (int i = threadIdx.x; i < min(p.G, kGSmem); i += blockDim.x) sm.gidx()[i] = p.gidx[i];
+  for (int i = threadIdx.x; i < min(max(p.G, p.nrow_g), kGSmem); i += blockDim.x) sm.gidx()[i] = p.gidx[i];
   if (warp == 0) {
     tmem_alloc(smem_u32(sm.tmem_holder()), C::kTmemCols);
     tmem_relinquish();

@@ -316,6 +316,74 @@ static lf_status global_pass(const Problem& P, float* ws, cudaStream_t ps) {
   return LF_OK;
 }
 
+// ------------------------------------------------------------------ global rows on the tensor cores
+// With many global tokens (d = 64, G >= kGlobalBandMin) their rows run through
+// the band kernel in its global-row mode: per (batch row, head) the query
+// rows are the G global tokens (128 per work item, from qg), the keys and
+// values are kg and vg over the row's valid length.  No scratch is needed.
+constexpr int kGlobalBandMin = 16;
+
+static bool global_rows_on_band_kernel(const Problem& P, bool bf16) {
+  return bf16 && P.d == 64 && P.G >= kGlobalBandMin;
+}
+
+static lf_status run_global_band_bf16(const Problem& P, int b0, int nbat, BandParams& p,
+                                      cudaStream_t s) {
+  const int grid_cap = sm_count() * band_ctas_per_sm(P.d);
+  const size_t off = (size_t)b0 * P.H * P.n * P.d;
+  const __nv_bfloat16* qg = reinterpret_cast<const __nv_bfloat16*>(P.qg) + (size_t)b0 * P.H * P.G * P.d;
+  const __nv_bfloat16* kg = reinterpret_cast<const __nv_bfloat16*>(P.kg) + off;
+  const __nv_bfloat16* vg = reinterpret_cast<const __nv_bfloat16*>(P.vg) + off;
+  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(P.out) + off;
+  const int64_t planes = (int64_t)nbat * P.H;
+  const int qtiles = (P.G + 127) / 128;
+  for (int h0 = 0; h0 < P.H; h0 += kMaxSeg) {
+    memset(&p, 0, sizeof p);
+    const int nh = std::min(kMaxSeg, P.H - h0);
+    for (int j = 0; j < nh; ++j) {
+      BandSeg& bs = p.seg[j];
+      bs.h = h0 + j;
+      bs.r = 0;
+      bs.delta = 1;
+      bs.n_r = P.n;
+      bs.items = qtiles;
+      bs.set = 0;
+      bs.begin = j * qtiles;
+    }
+    lf_status st;
+    const int ek = band_entry_keys(P.d);
+    if ((st = make_map(&p.tq[0], qg, P.d, P.G, planes, P.d, (int64_t)P.G * P.d, 128)) != LF_OK) return st;
+    if ((st = make_map(&p.tk[0], kg, P.d, P.n, planes, P.d, (int64_t)P.n * P.d, ek)) != LF_OK) return st;
+    if ((st = make_map(&p.tv[0], vg, P.d, P.n, planes, P.d, (int64_t)P.n * P.d, ek)) != LF_OK) return st;
+    p.k = kg;
+    p.v = vg;
+    p.out = out;
+    p.B = nbat;
+    p.H = P.H;
+    p.n = P.n;
+    p.half = P.n;  // every key is in reach
+    p.right = P.n;
+    p.causal = P.causal;
+    p.G = 0;
+    p.gmode = 1;
+    p.nrow_g = P.G;
+    p.nseg = nh;
+    p.items_per_b = nh * qtiles;  // this launch's heads only
+    const int64_t total = (int64_t)p.items_per_b * nbat;
+    if (total > 0x7fffffff) {
+      set_error("too many global-row work items (%lld)", (long long)total);
+      return LF_ERR_UNSUPPORTED;
+    }
+    p.total_items = (int32_t)total;
+    p.sl2 = (float)(1.4426950408889634 / std::sqrt((double)P.d));
+    for (int b = 0; b < nbat; ++b) p.pad[b] = P.pad ? P.pad[b0 + b] : 0;
+    for (int g = 0; g < P.G; ++g) p.gidx[g] = P.gidx[g];
+    const int grid = (int)std::min<int64_t>(total, grid_cap);
+    if (grid > 0 && (st = launch_band_tc(p, P.d, grid, s)) != LF_OK) return st;
+  }
+  return LF_OK;
+}
+
 // ------------------------------------------------------------------ bf16 band planning
 // Every (head, residue) class with at least one row is a segment; its work
 // items are its 128-row tiles (D = 64) or pairs of them (D = 128).  Segments are generated in order straight
@@ -455,13 +523,23 @@ static lf_status wait_event(cudaStream_t s, cudaEvent_t e) {
   return LF_OK;
 }
 
+// The parameter block of the bf16 band launches (~25 KB: kept off the stack;
+// each launch copies it, so one per host thread serves every launch).
+static BandParams* band_params() {
+  static thread_local BandParams* bp = nullptr;
+  if (!bp) bp = new (std::nothrow) BandParams;
+  if (!bp) set_error("host allocation of the band parameter block failed");
+  return bp;
+}
+
 template <typename T>
 static lf_status forward_t(const Problem& P, bool bf16) {
   lf_status st;
-  // ---- global rows: scratch and a fork point for the side stream
+  const bool g_band = P.G > 0 && global_rows_on_band_kernel(P, bf16);
+  // ---- global rows: scratch (streaming pass only) and a fork point for the side stream
   float* ws = nullptr;
   AuxStream* aux = nullptr;
-  if (P.G > 0) {
+  if (P.G > 0 && !g_band) {
     size_t total = 0;
     for (int b0 = 0; b0 < P.B; b0 += kMaxBatch) {
       const int nb = std::min(kMaxBatch, P.B - b0);
@@ -475,12 +553,12 @@ static lf_status forward_t(const Problem& P, bool bf16) {
       set_error("scratch allocation of %zu bytes failed: %s", total, cudaGetErrorString(e));
       return LF_ERR_NO_MEMORY;
     }
-    // bf16: the band kernels leave the global tokens' rows to this pass, which
-    // can then run beside them; fp32: it runs after the band kernel
-    if (bf16) {
-      aux = aux_stream();
-      if (!(aux && record(aux->fork, P.stream) == LF_OK && wait_event(aux->s, aux->fork) == LF_OK)) aux = nullptr;
-    }
+  }
+  // bf16: the band kernels leave the global tokens' rows to the global-row
+  // pass, which can then run beside them; fp32: it runs after the band kernel
+  if (P.G > 0 && bf16) {
+    aux = aux_stream();
+    if (!(aux && record(aux->fork, P.stream) == LF_OK && wait_event(aux->s, aux->fork) == LF_OK)) aux = nullptr;
   }
   // ---- band kernel on the caller's stream, launched first so that it takes
   // the whole GPU; the global-row pass (side stream) then fills the SMs its
@@ -490,14 +568,8 @@ static lf_status forward_t(const Problem& P, bool bf16) {
   for (int b0 = 0; st == LF_OK && b0 < P.B; b0 += kMaxBatch) {
     const int nb = std::min(kMaxBatch, P.B - b0);
     if (bf16) {
-      static thread_local BandParams* bp = nullptr;  // ~25 KB: keep it off the stack
-      if (!bp) bp = new (std::nothrow) BandParams;
-      if (!bp) {
-        set_error("host allocation of the band parameter block failed");
-        st = LF_ERR_NO_MEMORY;
-      } else {
-        st = run_band_bf16(P, b0, nb, *bp);
-      }
+      BandParams* bp = band_params();
+      st = bp ? run_band_bf16(P, b0, nb, *bp) : LF_ERR_NO_MEMORY;
     } else {
       st = run_band_f32(P, b0, nb);
     }
@@ -505,7 +577,16 @@ static lf_status forward_t(const Problem& P, bool bf16) {
   if (st == LF_OK && t_band_stop) st = record_timing(t_band_stop, P.stream);
   if (P.G > 0) {
     // the global rows beside the band kernel, or after it on the caller's stream
-    lf_status gp = (st == LF_OK) ? global_pass<T>(P, ws, aux ? aux->s : P.stream) : LF_OK;
+    cudaStream_t gs = aux ? aux->s : P.stream;
+    lf_status gp = LF_OK;
+    if (st == LF_OK && g_band) {
+      for (int b0 = 0; gp == LF_OK && b0 < P.B; b0 += kMaxBatch) {
+        BandParams* bp = band_params();
+        gp = bp ? run_global_band_bf16(P, b0, std::min(kMaxBatch, P.B - b0), *bp, gs) : LF_ERR_NO_MEMORY;
+      }
+    } else if (st == LF_OK) {
+      gp = global_pass<T>(P, ws, gs);
+    }
     if (aux) {
       // join even on failure so nothing on the side stream outlives the scratch
       lf_status j = record(aux->join, aux->s);
@@ -513,10 +594,12 @@ static lf_status forward_t(const Problem& P, bool bf16) {
       if (gp == LF_OK) gp = j;
     }
     if (st == LF_OK) st = gp;
-    cudaError_t fe = cudaFreeAsync(ws, P.stream);
-    if (st == LF_OK && fe != cudaSuccess) {
-      set_error("scratch free failed: %s", cudaGetErrorString(fe));
-      st = LF_ERR_CUDA;
+    if (ws) {
+      cudaError_t fe = cudaFreeAsync(ws, P.stream);
+      if (st == LF_OK && fe != cudaSuccess) {
+        set_error("scratch free failed: %s", cudaGetErrorString(fe));
+        st = LF_ERR_CUDA;
+      }
     }
   }
   return st;

@@ -65,6 +65,12 @@ struct BandParams {
   int32_t half, right;     // window reach in steps: look-back half, look-ahead right
   int32_t causal, G, nseg, items_per_b, total_items;
   float sl2;               // log2(e) / sqrt(d)
+  // Global-row mode (d = 64 kernel only): the query rows are the global
+  // tokens (tq over qg, nrow_g of them per plane, at positions gidx), the
+  // keys and values are kg and vg, every key below the row's valid length
+  // (and at or before the token when causal) is attended, and the rows are
+  // written at the tokens' positions.  G is then 0 (no global entries).
+  int32_t gmode, nrow_g;
   int32_t pad[kMaxBatch];
   BandSeg seg[kMaxSeg];
   int32_t gidx[kMaxGlobal];

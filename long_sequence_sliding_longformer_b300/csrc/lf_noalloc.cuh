@@ -84,8 +84,10 @@ static lf_status forward_noalloc(const Problem& P) {
   lf_status st = validate(P, true);
   if (st != LF_OK) return st;
   if ((int64_t)P.B * P.H * P.n == 0) return LF_OK;
+  // rows of many global tokens run on the band kernel and need no scratch
+  const bool g_band = P.G > 0 && global_rows_on_band_kernel(P, true);
   // size check before anything touches the device
-  if (P.G > 0) {
+  if (P.G > 0 && !g_band) {
     for (int b0 = 0; b0 < P.B; b0 += kMaxBatch) {
       const int nb = std::min(kMaxBatch, P.B - b0);
       if (static_scratch_chunk(P, nb) == 0) {
@@ -103,7 +105,7 @@ static lf_status forward_noalloc(const Problem& P) {
     return LF_ERR_CUDA;
   }
   float* ws = nullptr;
-  if (P.G > 0 && (st = static_scratch_for_current_device(&ws)) != LF_OK) return st;
+  if (P.G > 0 && !g_band && (st = static_scratch_for_current_device(&ws)) != LF_OK) return st;
   cudaGetLastError();
   if (t_band_start && (st = record_timing(t_band_start, P.stream)) != LF_OK) return st;
   for (int b0 = 0; b0 < P.B; b0 += kMaxBatch) {
@@ -113,6 +115,13 @@ static lf_status forward_noalloc(const Problem& P) {
   }
   if (t_band_stop && (st = record_timing(t_band_stop, P.stream)) != LF_OK) return st;
   if (P.G == 0) return LF_OK;
+  if (g_band) {
+    for (int b0 = 0; b0 < P.B; b0 += kMaxBatch) {
+      BandParams bp;  // on the stack: no heap use on this path
+      if ((st = run_global_band_bf16(P, b0, std::min(kMaxBatch, P.B - b0), bp, P.stream)) != LF_OK) return st;
+    }
+    return LF_OK;
+  }
   // batch chunks run one after another on the stream, so they can share the array
   for (int b0 = 0; b0 < P.B; b0 += kMaxBatch) {
     const int nb = std::min(kMaxBatch, P.B - b0);

@@ -151,6 +151,19 @@ def test_bf16_many_residue_classes(dil):
     check(wl, run(wl, inp), oracle.wl_fwd(wl, inp))
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_global_rows_on_band_kernel(causal):
+    """d = 64 with many global tokens: their rows run through the band kernel's
+    global-row mode (queries from qg, keys kg/vg over the row's valid length).
+    Two query tiles of global tokens, some of them in a padded region."""
+    gidx = tuple(sorted(set(range(0, 600, 4)) | {599}))  # 151 tokens
+    wl = workloads.custom("gband", "bf16", 2, 3, 600, 64, 64, (1, 2, 3), causal, gidx, (0, 170), seed=21)
+    inp = workloads.make_inputs(wl, "cuda")
+    out = run(wl, inp)
+    check(wl, out, oracle.wl_fwd(wl, inp))
+    assert torch.all(out[1, :, 600 - 170:] == 0)
+
+
 def test_bf16_many_globals():
     wl = workloads.custom("glob", "bf16", 1, 2, 1500, 64, 32, (1, 2), False, tuple(range(0, 1500, 5)),
                           (0,), seed=4)
