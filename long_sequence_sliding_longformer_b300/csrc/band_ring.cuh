@@ -132,7 +132,7 @@ __device__ __forceinline__ int upper_bound_gidx(const BandParams& p, const Table
 
 // Not inlined: every role calls it once per item, and one out-of-line copy
 // keeps the per-entry loops small in the instruction cache.
-template <int kE>
+template <int kE, bool kG>
 __device__ __noinline__ TileItem decode_tile(const BandParams& p, const Tables& tb, int item) {
   const BandSeg* segs = tb.seg;
   TileItem it;
@@ -152,7 +152,7 @@ __device__ __noinline__ TileItem decode_tile(const BandParams& p, const Tables& 
   it.m0 = (rem - sg.begin) * 128;
   it.bh = it.b * p.H + it.h;
   it.Lb = p.n - tb.pad[it.b];
-  if (p.gmode) {
+  if (kG) {
     // query rows m: global tokens m0 .. m0 + 127 (of nrow_g); keys: [0, Lb)
     it.Lm = it.Lb;
     it.act = it.m0 < p.nrow_g && it.Lb > 0;
@@ -251,7 +251,7 @@ __device__ __forceinline__ int residue_coord(int g, int r, int delta) {
 // ------------------------------------------------------------------ producers
 // kIsV = false loads Q and the K entries, kIsV = true the V entries, so that a
 // full V ring (waiting for the transposer) never holds back a K.
-template <int D, bool kIsV>
+template <int D, bool kIsV, bool kG>
 __device__ void band_producer(const BandParams& p, const BandSmem<D>& sm, int lane) {
   using C = BandCfg<D>;
   constexpr int kSt = kIsV ? C::kVSt : C::kKSt;
@@ -278,7 +278,7 @@ __device__ void band_producer(const BandParams& p, const BandSmem<D>& sm, int la
   auto q_seek = [&]() {
     q_have = false;
     for (; q_item < p.total_items; q_item += gridDim.x) {
-      qt = decode_tile<C::kE>(p, tb, q_item);
+      qt = decode_tile<C::kE, kG>(p, tb, q_item);
       if (qt.act) { q_have = true; return; }
     }
   };
@@ -308,7 +308,7 @@ __device__ void band_producer(const BandParams& p, const BandSmem<D>& sm, int la
   uint32_t n_act = 0;  // active items started
 
   for (int item = blockIdx.x; ok && item < p.total_items; item += gridDim.x) {
-    const TileItem it = decode_tile<C::kE>(p, tb, item);
+    const TileItem it = decode_tile<C::kE, kG>(p, tb, item);
     if (!it.act) continue;
     if (!kIsV && q_it == n_act && !q_issue(true)) { ok = false; break; }  // this item's Q
     ++n_act;
@@ -423,7 +423,7 @@ __device__ void band_producer(const BandParams& p, const BandSmem<D>& sm, int la
 // [keys, D]; the warp moves every entry into 8x8 blocks of V^T with
 // ldmatrix.trans / stmatrix, both sides 128-byte swizzled: V^T is kE/64
 // blocks of 64 keys, each [D rows, 128 bytes].
-template <int D>
+template <int D, bool kG>
 __device__ void band_transposer(const BandParams& p, const BandSmem<D>& sm, int lane) {
   using C = BandCfg<D>;
   volatile int* abort = sm.abort_flag();
@@ -434,7 +434,7 @@ __device__ void band_transposer(const BandParams& p, const BandSmem<D>& sm, int 
   if (blockIdx.x == 0 && lane == 0) tr.track = 4;
   Prof pf;
   for (int item = blockIdx.x; ok && item < p.total_items; item += gridDim.x) {
-    const TileItem it = decode_tile<C::kE>(p, sm.tables(), item);
+    const TileItem it = decode_tile<C::kE, kG>(p, sm.tables(), item);
     if (!it.act) continue;
     for (int e = 0; e < it.nE; ++e, ++kv) {
       const int vs = kv % C::kVSt, ts = kv % C::kTSt;
@@ -489,18 +489,18 @@ struct EntryCursor {
   bool valid;
 };
 
-template <int kE>
+template <int kE, bool kG>
 __device__ __forceinline__ void cursor_seek(const BandParams& p, const Tables& tb, EntryCursor& c) {
   // first active item at or after c.item
   while (c.item < p.total_items) {
-    c.it = decode_tile<kE>(p, tb, c.item);
+    c.it = decode_tile<kE, kG>(p, tb, c.item);
     if (c.it.act) return;
     c.item += gridDim.x;
   }
   c.valid = false;
 }
 
-template <int kE>
+template <int kE, bool kG>
 __device__ __forceinline__ void cursor_start(const BandParams& p, const Tables& tb, EntryCursor& c) {
   c.item = blockIdx.x;
   c.e = 0;
@@ -508,10 +508,10 @@ __device__ __forceinline__ void cursor_start(const BandParams& p, const Tables& 
   c.kv = 0;
   c.n_items = 0;
   c.valid = true;
-  cursor_seek<kE>(p, tb, c);
+  cursor_seek<kE, kG>(p, tb, c);
 }
 
-template <int kE>
+template <int kE, bool kG>
 __device__ __forceinline__ void cursor_next(const BandParams& p, const Tables& tb, EntryCursor& c) {
   ++c.g;
   if (++c.e < c.it.nE) return;
@@ -519,10 +519,10 @@ __device__ __forceinline__ void cursor_next(const BandParams& p, const Tables& t
   ++c.n_items;
   c.e = 0;
   c.item += gridDim.x;
-  cursor_seek<kE>(p, tb, c);
+  cursor_seek<kE, kG>(p, tb, c);
 }
 
-template <int D>
+template <int D, bool kG>
 __device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tmem) {
   using C = BandCfg<D>;
   constexpr uint32_t kTile16 = C::kTile >> 4;    // a K / V^T slot, in descriptor address units
@@ -542,8 +542,8 @@ __device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tm
   Prof pf;
 
   EntryCursor cs, cp;  // S cursor (ahead), P.V cursor
-  cursor_start<C::kE>(p, tb, cs);
-  cursor_start<C::kE>(p, tb, cp);
+  cursor_start<C::kE, kG>(p, tb, cs);
+  cursor_start<C::kE, kG>(p, tb, cp);
 
   // S of the entry under cs into buffer cs.g % kSBuf (the MMAs, issued by an
   // elected lane of the converged warp; the caller has waited for Q and K)
@@ -606,7 +606,7 @@ __device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tm
     if (!ok) break;
     tc_fence_after();
     mma_s();
-    cursor_next<C::kE>(p, tb, cs);
+    cursor_next<C::kE, kG>(p, tb, cs);
   }
   // then per entry: the P.V of the entry under cp and the S of the one kSBuf
   // ahead (cs), which goes into the buffer that P.V reads (so after it).
@@ -653,8 +653,8 @@ __device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tm
     if (cp.e == 0) ++o_cnt;
     tr.ev(14);
     pf.lap(8);
-    cursor_next<C::kE>(p, tb, cp);
-    if (has_s) cursor_next<C::kE>(p, tb, cs);
+    cursor_next<C::kE, kG>(p, tb, cp);
+    if (has_s) cursor_next<C::kE, kG>(p, tb, cs);
   }
   tr.done();
   pf.lap(7);
@@ -751,7 +751,7 @@ __device__ __forceinline__ float exp32(const uint32_t* x, float sl2, float mneg,
 }
 
 // Softmax and epilogue (one query row per thread; warp quarter wq of TMEM lanes).
-template <int D>
+template <int D, bool kG>
 __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_t tmem, int wq, int lane) {
   using C = BandCfg<D>;
   static_assert(C::kE == 64 || C::kE == 128, "the softmax holds one entry in registers");
@@ -770,13 +770,13 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
   Prof pf;
 
   for (int item = blockIdx.x; ok && item < p.total_items; item += gridDim.x) {
-    const TileItem it = decode_tile<C::kE>(p, sm.tables(), item);
+    const TileItem it = decode_tile<C::kE, kG>(p, sm.tables(), item);
     tr.ev(0);
     const int m_q = it.m0 + row;
     // rows at the positions of global tokens are written by the global-row
     // pass, which may run at the same time: this kernel leaves them alone
-    bool write_row = p.gmode ? m_q < p.nrow_g : m_q < it.n_r;
-    const int g_pos = (p.gmode && write_row) ? gidx_at(p, tb, m_q) : 0;  // global-row mode: the token's position
+    bool write_row = kG ? m_q < p.nrow_g : m_q < it.n_r;
+    const int g_pos = (kG && write_row) ? gidx_at(p, tb, m_q) : 0;  // global-row mode: the token's position
     if (p.G > 0) {
       const int i_lo = it.r + it.delta * it.m0;
       const int i_hi = it.r + it.delta * min(it.m0 + 127, it.n_r - 1);
@@ -785,9 +785,9 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
         if (upper_bound_gidx(p, tb, i_q) > upper_bound_gidx(p, tb, i_q - 1)) write_row = false;
       }
     }
-    const bool row_valid = p.gmode ? (write_row && g_pos < it.Lb) : m_q < it.Lm;
+    const bool row_valid = kG ? (write_row && g_pos < it.Lb) : m_q < it.Lm;
     uint4* orow = reinterpret_cast<uint4*>(
-        p.out + ((size_t)it.bh * p.n + (p.gmode ? (size_t)g_pos : it.r + (size_t)it.delta * m_q)) * D);
+        p.out + ((size_t)it.bh * p.n + (kG ? (size_t)g_pos : it.r + (size_t)it.delta * m_q)) * D);
     if (!it.act) {
       if (write_row) {
 #pragma unroll
@@ -829,7 +829,7 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
 #pragma unroll
       for (int c = 0; c < NC; ++c) keep[c] = ~0u;
       int mode;
-      if (p.gmode) {
+      if (kG) {
         // every key in [0, Lb), up to the token itself when causal
         const int kb = C::kE * e;
         const int chi = row_valid ? (p.causal ? min(g_pos, it.Lb - 1) : it.Lb - 1) - kb : -1;
@@ -993,7 +993,7 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
 
 constexpr int kBandThreads = 256;
 
-template <int D>
+template <int D, bool kG>
 __global__ void __launch_bounds__(kBandThreads, BandCfg<D>::kCtaPerSm)
     band_tc_kernel(const __grid_constant__ BandParams p) {
   using C = BandCfg<D>;
@@ -1043,15 +1043,15 @@ __global__ void __launch_bounds__(kBandThreads, BandCfg<D>::kCtaPerSm)
   const uint32_t tmem = *sm.tmem_holder();
 
   if (warp >= 4) {
-    band_softmax<D>(p, sm, tmem, warp & 3, lane);
+    band_softmax<D, kG>(p, sm, tmem, warp & 3, lane);
   } else if (warp == 0) {
-    band_mma<D>(p, sm, tmem);
+    band_mma<D, kG>(p, sm, tmem);
   } else if (warp == 1) {
-    band_producer<D, false>(p, sm, lane);
+    band_producer<D, false, kG>(p, sm, lane);
   } else if (warp == 2) {
-    band_producer<D, true>(p, sm, lane);
+    band_producer<D, true, kG>(p, sm, lane);
   } else {
-    band_transposer<D>(p, sm, lane);
+    band_transposer<D, kG>(p, sm, lane);
   }
 
   tc_fence_before();
@@ -1062,19 +1062,19 @@ __global__ void __launch_bounds__(kBandThreads, BandCfg<D>::kCtaPerSm)
   }
 }
 
-template <int D>
+template <int D, bool kG>
 static lf_status launch_band_tc_d(const BandParams& p, int grid, cudaStream_t s) {
   using C = BandCfg<D>;
   static bool attr_set = false;  // per process; the attribute is per function
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(band_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(band_tc_kernel<D, kG>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) {
       set_error("cudaFuncSetAttribute(band kernel): %s", cudaGetErrorString(e));
       return LF_ERR_CUDA;
     }
     attr_set = true;
   }
-  band_tc_kernel<D><<<grid, kBandThreads, C::kSmem, s>>>(p);
+  band_tc_kernel<D, kG><<<grid, kBandThreads, C::kSmem, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("band kernel launch: %s", cudaGetErrorString(e));
@@ -1085,7 +1085,11 @@ static lf_status launch_band_tc_d(const BandParams& p, int grid, cudaStream_t s)
 }
 
 // D = 64 only (D = 128 runs the pair kernel of band_pair.cuh).
-inline lf_status launch(const BandParams& p, int grid, cudaStream_t s) { return launch_band_tc_d<64>(p, grid, s); }
+// Global-row mode (p.gmode) is a separate instantiation, so that the band
+// path carries none of its code.
+inline lf_status launch(const BandParams& p, int grid, cudaStream_t s) {
+  return p.gmode ? launch_band_tc_d<64, true>(p, grid, s) : launch_band_tc_d<64, false>(p, grid, s);
+}
 
 }  // namespace ringk
 }  // namespace lf
