@@ -65,6 +65,14 @@ typedef enum {
  * Supported d: 64 and 128.  Computes in fp32 on the tensor cores (bf16
  * operands, fp32 accumulation, fp32 online softmax) and rounds the output
  * to bf16 (round to nearest even).
+ *
+ * Stream-ordered on `stream`.  With n_global > 0 the global tokens' rows run
+ * on a second stream of the library's (one per host thread and device),
+ * forked from and joined back into `stream` with events, beside the band
+ * kernel; the call is still complete when work enqueued on `stream` after it
+ * starts.  Scratch for those rows is allocated stream-ordered on `stream`,
+ * except for d = 64 with n_global >= 16, whose rows run on the tensor cores
+ * without scratch.
  */
 lf_status lf_attn_fwd(const void* q, const void* k, const void* v,
                       const void* qg, const void* kg, const void* vg,
@@ -91,7 +99,8 @@ lf_status lf_attn_fwd_f32(const void* q, const void* k, const void* v,
  * counterpart to this: it is an interface choice, not part of the method.
  *
  * lf_attn_fwd allocates the scratch of its global-row pass (stream-ordered,
- * on every call with n_global > 0).  This variant is for callers that cannot
+ * on every call with n_global > 0 that does not take the scratch-free path
+ * for d = 64 with n_global >= 16).  This variant is for callers that cannot
  * allocate device memory while they run: an engine that reserves its whole
  * memory budget at start-up, code that must not meet an out-of-memory error
  * or allocator latency in the middle of a step, or a host application that
@@ -103,10 +112,12 @@ lf_status lf_attn_fwd_f32(const void* q, const void* k, const void* v,
  * loading the library holds until the process exits.  The first call on each
  * device looks up that array's device address, so make the first call on a
  * device before any stream capture.  Returns LF_ERR_UNSUPPORTED when
- * B*H*n_global*(d+2) fp32 values (per block of 256 batch rows) exceed the
- * array.  All calls share the array and it keeps the last call's contents
- * (every value a call reads is written earlier in that call): calls whose
- * kernels overlap on the GPU, e.g. on two streams at once, race on it.
+ * B*H*n_global*(d+2) fp32 values plus B*H*n_global 32-bit counters (per
+ * block of 256 batch rows) exceed the array (never for d = 64 with
+ * n_global >= 16, which needs no scratch).  Everything runs on `stream`.  All
+ * calls share the array and it keeps the last call's contents (every value a
+ * call reads is written earlier in that call): calls whose kernels overlap
+ * on the GPU, e.g. on two streams at once, race on it.
  */
 lf_status lf_attn_fwd_noalloc(const void* q, const void* k, const void* v,
                               const void* qg, const void* kg, const void* vg,
