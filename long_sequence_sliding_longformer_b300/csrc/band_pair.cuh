@@ -4,8 +4,9 @@
 // Computes the sliding / dilated / causal window part of Longformer attention
 // (velog.io/@lainshower/Longformer, section 3-1 "Sliding Window", "Dilated
 // Sliding Window", section 4.1 for the look-back-only pattern) plus the
-// global tokens' key columns ("Global Attention"), for every row.  Rows of
-// global tokens are overwritten afterwards by the global-row kernels.
+// global tokens' key columns ("Global Attention"), for every row except the
+// rows at global tokens' positions, which the global-row pass writes (it may
+// run at the same time).
 //
 // Dilation is handled by residue classes: with dilation delta, row
 // i = r + delta*m only ever attends rows of the same residue r, and in the

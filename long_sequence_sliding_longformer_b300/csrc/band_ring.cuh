@@ -5,8 +5,11 @@
 // Computes the sliding / dilated / causal window part of Longformer attention
 // (velog.io/@lainshower/Longformer, section 3-1 "Sliding Window", "Dilated
 // Sliding Window", section 4.1 for the look-back-only pattern) plus the
-// global tokens' key columns ("Global Attention"), for every row.  Rows of
-// global tokens are overwritten afterwards by the global-row kernels.
+// global tokens' key columns ("Global Attention"), for every row except the
+// rows at global tokens' positions, which the global-row pass writes (it may
+// run at the same time).  A second instantiation (kG = true) is that pass for
+// many global tokens: the query rows are the global tokens, the keys every
+// valid key (see BandParams::gmode).
 //
 // Dilation is handled by residue classes: with dilation delta, row
 // i = r + delta*m only ever attends rows of the same residue r, and in the
@@ -18,10 +21,11 @@
 // the kE-key "entries" that intersect the tile's windows, then the gathered
 // keys of the global tokens, and accumulates O = softmax(S) V online.
 //
-// Persistent CTAs (two per SM for D = 64, one for D = 128), 8 warps each:
-//   warp 0     allocates TMEM; issues every tcgen05.mma (one elected lane):
-//              S = Q K^T for up to kSBuf entries ahead into a ring of TMEM
-//              buffers, and O += P V once the softmax has written P
+// Persistent CTAs (two per SM; one with 128-key entries, LF_RING_E=128), 8 warps each:
+//   warp 0     allocates TMEM; issues every tcgen05.mma (an elected lane of
+//              the converged warp): per entry g, O += P V of entry g once
+//              the softmax has written P, then S = Q K^T of entry g + kSBuf
+//              into the buffer that P.V read
 //   warp 1     Q/K producer: TMA loads of Q and of the K entries
 //   warp 2     V producer: TMA loads of the V entries (the global tokens'
 //              K/V rows are gathered by the producers with plain loads)
