@@ -164,6 +164,17 @@ def test_bf16_global_rows_on_band_kernel(causal):
     assert torch.all(out[1, :, 600 - 170:] == 0)
 
 
+def test_bf16_more_globals_than_shared_memory_holds():
+    """1100 global tokens: the band kernels keep the first 1024 positions in
+    shared memory and read the rest from the kernel parameters; both the
+    global key columns of the band rows and the global rows (global-row mode
+    at d = 64) cross that boundary."""
+    gidx = tuple(range(0, 2200, 2))
+    wl = workloads.custom("g1100", "bf16", 1, 1, 2200, 64, 64, (1,), False, gidx, None, seed=23)
+    inp = workloads.make_inputs(wl, "cuda")
+    check(wl, run(wl, inp), oracle.wl_fwd(wl, inp))
+
+
 def test_bf16_many_globals():
     wl = workloads.custom("glob", "bf16", 1, 2, 1500, 64, 32, (1, 2), False, tuple(range(0, 1500, 5)),
                           (0,), seed=4)
