@@ -130,7 +130,8 @@ def dist_setup():
     backend = "nccl" if torch.cuda.is_available() else "gloo"
     if torch.cuda.is_available():
         torch.cuda.set_device(local)
-    dist.init_process_group(backend)
+    if not dist.is_initialized():
+        dist.init_process_group(backend)
     return rank, ws, local
 
 
