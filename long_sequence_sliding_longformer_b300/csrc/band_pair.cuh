@@ -981,13 +981,12 @@ __global__ void __launch_bounds__(kBandThreads, 1) band_tc_kernel(const __grid_c
 template <int D>
 static lf_status launch_band_tc_d(const BandParams& p, int grid, cudaStream_t s) {
   using C = BandCfg<D>;
-  static bool attr_set = false;  // per process; the attribute is per function
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(band_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (e != cudaSuccess) {
-      set_error("cudaFuncSetAttribute(band kernel): %s", cudaGetErrorString(e));
-      return LF_ERR_CUDA;
-    }
+  static std::atomic<uint64_t> attr_done{0};
+  static std::atomic<bool> regs_checked{false};
+  lf_status st = smem_attr_once((const void*)band_tc_kernel<D>, C::kSmem, attr_done, "band kernel");
+  if (st != LF_OK) return st;
+  if (!regs_checked.load(std::memory_order_acquire)) {
+    cudaError_t e;
     // The register hand-over between warpgroups needs the launch allocation
     // it was planned for; with fewer registers setmaxnreg.inc could never be
     // satisfied, so refuse to launch rather than wait.
@@ -1002,7 +1001,7 @@ static lf_status launch_band_tc_d(const BandParams& p, int grid, cudaStream_t s)
                 fa.numRegs, kRegsAtLaunchMin, 65536 / kBandThreads);
       return LF_ERR_UNSUPPORTED;
     }
-    attr_set = true;
+    regs_checked.store(true, std::memory_order_release);
   }
   band_tc_kernel<D><<<grid, kBandThreads, C::kSmem, s>>>(p);
   cudaError_t e = cudaGetLastError();

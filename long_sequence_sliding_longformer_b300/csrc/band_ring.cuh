@@ -1069,15 +1069,9 @@ __global__ void __launch_bounds__(kBandThreads, BandCfg<D>::kCtaPerSm)
 template <int D, bool kG>
 static lf_status launch_band_tc_d(const BandParams& p, int grid, cudaStream_t s) {
   using C = BandCfg<D>;
-  static bool attr_set = false;  // per process; the attribute is per function
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(band_tc_kernel<D, kG>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (e != cudaSuccess) {
-      set_error("cudaFuncSetAttribute(band kernel): %s", cudaGetErrorString(e));
-      return LF_ERR_CUDA;
-    }
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  lf_status st = smem_attr_once((const void*)band_tc_kernel<D, kG>, C::kSmem, attr_done, "band kernel");
+  if (st != LF_OK) return st;
   band_tc_kernel<D, kG><<<grid, kBandThreads, C::kSmem, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {

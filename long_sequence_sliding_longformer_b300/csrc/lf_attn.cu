@@ -13,6 +13,7 @@
 
 #include "lf_internal.cuh"
 #include "band_ring.cuh"
+#include "band_duo.cuh"
 #include "band_pair.cuh"
 #include "band_simt.cuh"
 #include "global_rows.cuh"
@@ -20,18 +21,16 @@
 namespace lf {
 
 // ------------------------------------------------------------------ band kernel choice
-// D = 64: the ring kernel (one 128-row tile per CTA, two CTAs per SM, 64-key
-// entries); D = 128: the pair kernel (two tiles per CTA sharing 128-key
-// entries, one CTA per SM).
+// D = 64: the duo kernel (two 128-row tiles per item sharing 128-key loads,
+// one CTA per SM); its global-row mode still runs on the ring kernel (one
+// 128-row tile per CTA, two CTAs per SM, 64-key entries).  D = 128: the pair
+// kernel (two tiles per CTA sharing 128-key entries, one CTA per SM).
 lf_status launch_band_tc(const BandParams& p, int d, int grid, cudaStream_t s) {
-  if (d == 64) return ringk::launch(p, grid, s);
+  if (d == 64) return p.gmode ? ringk::launch(p, grid, s) : duok::launch(p, grid, s);
   if (d == 128) return pairk::launch(p, grid, s);
   set_error("band kernel: unsupported head dimension %d", d);
   return LF_ERR_UNSUPPORTED;
 }
-int band_ctas_per_sm(int d) { return d == 64 ? ringk::BandCfg<64>::kCtaPerSm : 1; }
-int band_entry_keys(int d) { return d == 64 ? ringk::BandCfg<64>::kE : 128; }
-int band_rows_per_item(int d) { return d == 64 ? 128 : 256; }
 
 static thread_local char t_msg[512] = "";
 static thread_local cudaEvent_t t_band_start = nullptr, t_band_stop = nullptr;
@@ -329,7 +328,7 @@ static bool global_rows_on_band_kernel(const Problem& P, bool bf16) {
 
 static lf_status run_global_band_bf16(const Problem& P, int b0, int nbat, BandParams& p,
                                       cudaStream_t s) {
-  const int grid_cap = sm_count() * band_ctas_per_sm(P.d);
+  const int grid_cap = sm_count() * ringk::BandCfg<64>::kCtaPerSm;
   const size_t off = (size_t)b0 * P.H * P.n * P.d;
   const __nv_bfloat16* qg = reinterpret_cast<const __nv_bfloat16*>(P.qg) + (size_t)b0 * P.H * P.G * P.d;
   const __nv_bfloat16* kg = reinterpret_cast<const __nv_bfloat16*>(P.kg) + off;
@@ -351,7 +350,7 @@ static lf_status run_global_band_bf16(const Problem& P, int b0, int nbat, BandPa
       bs.begin = j * qtiles;
     }
     lf_status st;
-    const int ek = band_entry_keys(P.d);
+    const int ek = ringk::BandCfg<64>::kE;
     if ((st = make_map(&p.tq[0], qg, P.d, P.G, planes, P.d, (int64_t)P.G * P.d, 128)) != LF_OK) return st;
     if ((st = make_map(&p.tk[0], kg, P.d, P.n, planes, P.d, (int64_t)P.n * P.d, ek)) != LF_OK) return st;
     if ((st = make_map(&p.tv[0], vg, P.d, P.n, planes, P.d, (int64_t)P.n * P.d, ek)) != LF_OK) return st;
@@ -390,8 +389,13 @@ static lf_status run_global_band_bf16(const Problem& P, int b0, int nbat, BandPa
 // into the parameter block `p` (no heap use), one launch per kMaxSeg segments
 // or kMaxSets (dilation, residue) tensor-map sets.
 static lf_status run_band_bf16(const Problem& P, int b0, int nbat, BandParams& p) {
-  const int grid_cap = sm_count() * band_ctas_per_sm(P.d);
-  const int rows_per_item = band_rows_per_item(P.d);
+  const int grid_cap = sm_count();  // one persistent CTA per SM
+  const int64_t half0 = std::min<int64_t>(P.w / 2, P.n);
+  const int64_t right0 = P.causal ? 0 : half0;
+  // D = 64 pairs tiles when the window reach is a multiple of 16 keys (the
+  // tiles' key ranges then meet on 16-key steps); D = 128 always pairs.
+  const int pair = (P.d == 128) || (half0 % 16 == 0 && right0 % 16 == 0);
+  const int rows_per_item = pair ? 256 : 128;
   const size_t off = (size_t)b0 * P.H * P.n * P.d;
   const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(P.q) + off;
   const __nv_bfloat16* k = reinterpret_cast<const __nv_bfloat16*>(P.k) + off;
@@ -439,7 +443,7 @@ static lf_status run_band_bf16(const Problem& P, int b0, int nbat, BandParams& p
       const int64_t rs = (int64_t)delta * P.d, ps = (int64_t)P.n * P.d;
       const size_t ro = (size_t)rr * P.d;
       lf_status st;
-      const int ek = band_entry_keys(P.d);
+      const int ek = 128;  // keys per K/V load
       if ((st = make_map(&p.tq[t], q + ro, P.d, n_r, planes, rs, ps, 128)) != LF_OK) return st;
       if ((st = make_map(&p.tk[t], k + ro, P.d, n_r, planes, rs, ps, ek)) != LF_OK) return st;
       if ((st = make_map(&p.tv[t], v + ro, P.d, n_r, planes, rs, ps, ek)) != LF_OK) return st;
@@ -454,6 +458,7 @@ static lf_status run_band_bf16(const Problem& P, int b0, int nbat, BandParams& p
     p.right = P.causal ? 0 : (int32_t)half;
     p.causal = P.causal;
     p.G = P.G;
+    p.pair = pair;
     p.nseg = nseg;
     p.items_per_b = items_per_b;
     const int64_t total = (int64_t)items_per_b * nbat;

@@ -11,6 +11,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/lf_attn.h"
 
 namespace lf {
@@ -71,6 +73,8 @@ struct BandParams {
   // (and at or before the token when causal) is attended, and the rows are
   // written at the tokens' positions.  G is then 0 (no global entries).
   int32_t gmode, nrow_g;
+  // Work items are pairs of consecutive 128-row tiles (1) or single tiles (0).
+  int32_t pair;
   int32_t pad[kMaxBatch];
   BandSeg seg[kMaxSeg];
   int32_t gidx[kMaxGlobal];
@@ -100,9 +104,6 @@ struct LaunchCtx {
 
 // All return LF_OK or an error status and set the thread's message.
 lf_status launch_band_tc(const BandParams& p, int d, int grid, cudaStream_t s);
-int band_ctas_per_sm(int d);  // resident band-kernel CTAs per SM
-int band_entry_keys(int d);   // keys per K/V entry (the TMA box height)
-int band_rows_per_item(int d);  // query rows per band work item
 lf_status launch_band_simt_f32(const SimtParams& p, const float* q, const float* k, const float* v,
                                float* out, cudaStream_t s);
 template <typename T>
@@ -111,6 +112,27 @@ lf_status launch_global_rows(const PatternParams& p, const T* qg, const T* kg, c
 
 void set_error(const char* fmt, ...);
 void count_launch(int k = 1);
+
+// Raises `func`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per device (the attribute applies to the device that is
+// current when it is set); `done` holds one bit per device already set.
+inline lf_status smem_attr_once(const void* func, int bytes, std::atomic<uint64_t>& done, const char* name) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    set_error("cudaGetDevice: %s", cudaGetErrorString(e));
+    return LF_ERR_CUDA;
+  }
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return LF_OK;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) {
+    set_error("cudaFuncSetAttribute(%s): %s", name, cudaGetErrorString(e));
+    return LF_ERR_CUDA;
+  }
+  if (bit) done.fetch_or(bit, std::memory_order_release);
+  return LF_OK;
+}
 
 // ----------------------------------------------------------------- device helpers
 #ifdef __CUDACC__
