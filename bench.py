@@ -164,16 +164,32 @@ def useful_work(wl):
     return pairs, flops, gpairs * 4 * wl.d
 
 
+def pct(xs, p):
+    """p-th percentile (nearest rank) of xs."""
+    ys = sorted(xs)
+    return ys[min(len(ys) - 1, max(0, int(round(p / 100.0 * (len(ys) - 1)))))]
+
+
 def band_bytes(wl) -> int:
     """Algorithmic HBM bytes of the band kernel: q, k, v read once, out written
     once, over all rows (8*d bytes per token-head in bf16)."""
     return 4 * wl.B * wl.H * wl.n * wl.d * wl.elem_bytes
 
 
-def cpu_sample(wl, inp, target_s: float = 12.0):
+def cpu_model() -> str:
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def cpu_sample(wl, inp, target_s: float = 12.0, threads: int = 0):
     """Time the oracle on whole (batch, head) slices of the workload until about
-    target_s seconds of work; returns (seconds, useful flops, threads, description)."""
-    import long_sequence_sliding_longformer_b300 as lf
+    target_s seconds of work; returns (seconds, useful flops, threads, description).
+    Useful work is counted by the oracle itself (no product code is loaded)."""
     import numpy as np
     import oracle
     host = workloads.Inputs(*[None if t is None else t.cpu() for t in
@@ -189,24 +205,25 @@ def cpu_sample(wl, inp, target_s: float = 12.0):
         chunk = slices[done:done + take]
         rows = np.concatenate([np.arange(n, dtype=np.int64) + (b * wl.H + h) * n for b, h in chunk])
         t0 = time.perf_counter()
-        oracle.wl_fwd(wl, host, rows=rows)
+        oracle.wl_fwd(wl, host, rows=rows, threads=threads)
         secs += time.perf_counter() - t0
         for b, h in chunk:
             pad = None if wl.pad_len is None else [wl.pad_len[b]]
-            _, f = lf.count_pairs(B=1, H=1, n=n, d=wl.d, w=wl.w, dilation=[wl.dilation[h]],
-                                  causal=wl.causal, pad_len=pad, global_idx=wl.global_idx)
-            flops += f
+            p, _ = oracle.count_pairs(B=1, H=1, n=n, w=wl.w, dilation=[wl.dilation[h]],
+                                      causal=wl.causal, pad_len=pad, global_idx=wl.global_idx)
+            flops += 4.0 * wl.d * p
         done += take
     desc = "%d of %d (batch, head) slices, all %d rows each (every row of the sample)" % (
         done, len(slices), n)
-    return secs, flops, oracle.max_threads(), desc
+    return secs, flops, threads if threads > 0 else oracle.max_threads(), desc
 
 
 def run_reference(args, wl):
     rank, ws, _ = dist_setup()
     if rank != 0:
         return
-    inp = workloads.make_inputs(wl, "cpu")
+    import oracle
+    inp = workloads.make_inputs(wl, "cpu", seed=wl.seed)
     times, flops_tot = [], 0.0
     threads, desc = 0, ""
     per_step_target = max(2.0, 60.0 / max(1, args.steps + args.warmup))
@@ -221,12 +238,12 @@ def run_reference(args, wl):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded N(0,1), CPU generator)",
+        "data": "synthetic (N(0,1), CPU generator seed %d)" % wl.seed,
         "config": dict(wl.describe(), sample="bounded per step"),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                         "sample": desc},
+                         "sample": desc, "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "tokens_per_s": value * 1e12 * tok / useful_work(wl)[1],
+        "tokens_per_s": value * 1e12 * tok / (4.0 * wl.d * oracle.wl_count_pairs(wl)[0]),
     }
     print(json.dumps(line), flush=True)
 
@@ -237,7 +254,11 @@ def run_gpu(args, wl):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     lf.load()
-    inp = workloads.make_inputs(wl, str(dev), seed=wl.seed + rank)
+    # the same CPU generator and seed as the reference arm (rank r: seed + r)
+    inp_host = workloads.make_inputs(wl, "cpu", seed=wl.seed + rank)
+    inp = workloads.Inputs(*[None if t is None else t.to(dev) for t in
+                             (inp_host.q, inp_host.k, inp_host.v, inp_host.qg, inp_host.kg, inp_host.vg)])
+    del inp_host
     out = torch.empty_like(inp.q)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -266,6 +287,7 @@ def run_gpu(args, wl):
         step()
     lf.set_band_events(None, None)
     launches_per_step = lf.launch_count() - launches0
+    band_kernel = lf.last_band_kernel()
     for _ in range(3):
         flush.zero_()
         graph.replay()
@@ -292,6 +314,19 @@ def run_gpu(args, wl):
     step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = max_over_ranks(sum(step_ms), ws, dev)
     ms_per_step = total_ms / K
+
+    # ---- hot L2: the same replay with no flush between steps (inputs that
+    # fit in L2 then stay there); reported beside the flushed number
+    Kh = min(K, 200)
+    evh = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Kh)]
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    for i in range(Kh):
+        evh[i][0].record(stream)
+        graph.replay()
+        evh[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    hot_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evh) / Kh, ws, dev)
 
     # ---- end to end through the public API: pinned host in, host out.  Every
     # step copies its inputs in and its output back; consecutive steps are
@@ -366,17 +401,21 @@ def run_gpu(args, wl):
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
-            "data": "synthetic (seeded N(0,1) on the device)",
+            "data": "synthetic (N(0,1), CPU generator seed %d, copied to the device)" % (wl.seed + rank),
             "config": dict(wl.describe(), parallelism="replicas: one workload per GPU" if ws > 1 else "1 GPU",
                            l2="flushed before every step (256 MiB write)"),
             "tokens_per_s": ws * wl.tokens() / (ms_per_step * 1e-3),
             "frac_of_bf16_peak": value / pk["bf16_tflops"],
             "roofline": {"bound": "tensor", "achieved": band_achieved, "peak": pk["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": band_achieved / pk["bf16_tflops"],
-                         "traffic": traffic, "kernel": "band_tc_kernel",
+                         "traffic": traffic, "kernel": band_kernel,
                          "peak_source": pk["source"] + " (burst)",
                          "hbm_achieved_gbs": hbm_achieved, "hbm_frac": hbm_achieved / pk["hbm_gbs"],
                          "band_ms": band_avg_ms, "band_share_of_step": band_avg_ms / statistics.mean(step_ms)},
+            "step_ms_p10": pct(step_ms, 10), "step_ms_p50": pct(step_ms, 50), "step_ms_p90": pct(step_ms, 90),
+            "band_ms_p10": pct(band_ms, 10), "band_ms_p90": pct(band_ms, 90),
+            "hot_l2": {"ms_per_step": hot_ms, "value": ws * flops / (hot_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                       "steps": Kh, "l2": "not flushed between steps"},
             "e2e": {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": launches,
@@ -388,8 +427,11 @@ def run_gpu(args, wl):
     if rank == 0 and not args.no_cpu_baseline and ws == 1:
         secs, sflops, threads, desc = cpu_sample(wl, inp, target_s=args.cpu_seconds)
         v = sflops / secs / 1e12
+        secs1, sflops1, _, desc1 = cpu_sample(wl, inp, target_s=min(3.0, args.cpu_seconds), threads=1)
         line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                                "sample": desc, "seconds": secs}
+                                "sample": desc, "seconds": secs, "cpu_model": cpu_model(),
+                                "one_thread": {"value": sflops1 / secs1 / 1e12, "seconds": secs1,
+                                               "sample": desc1}}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:

@@ -155,11 +155,30 @@ lf_status lf_attn_set_band_events(cudaEvent_t start, cudaEvent_t stop);
 uint64_t lf_attn_launch_count(void);
 
 /*
+ * Name of the band kernel that the last forward call on this host thread
+ * launched ("band_ring", "band_duo", "band_pair" or "band_simt_f32"; "" before
+ * the first).  A static string: the caller does not free it.
+ */
+const char* lf_attn_last_band_kernel(void);
+
+/*
  * Synchronises the current device and reads the library's device error word
  * (0 = none; otherwise LF_ERR_TIMEOUT in the low byte and the kernel role
  * that gave up in the next byte).  clear != 0 resets it to 0.
  */
 lf_status lf_device_error(uint32_t* code, int32_t clear);
+
+/*
+ * Testing hook for the timeout path.  Sets, for the current device, how long
+ * a kernel's pipeline wait (a role waiting for another role's barrier) may
+ * last before the kernel gives up: it then records LF_ERR_TIMEOUT in the
+ * device error word, every role leaves its loop, the in-flight copies and
+ * MMAs are waited for (those drain waits keep their own 200 ms limit) and
+ * the kernel returns; the call's output is then undefined.  ns = 0 restores
+ * the default of 2 s.  Synchronises the device first.  Returns LF_ERR_CUDA
+ * if the device cannot be reached.
+ */
+lf_status lf_set_wait_limit_ns(uint64_t ns);
 
 #ifdef __cplusplus
 }

@@ -20,7 +20,7 @@ from typing import Optional, Sequence
 
 import torch
 
-__all__ = ["attn", "count_pairs", "set_band_events", "launch_count", "device_error", "LfError",
+__all__ = ["attn", "count_pairs", "set_band_events", "launch_count", "last_band_kernel", "set_wait_limit_ns", "device_error", "LfError",
            "load", "LIB_PATH"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblf_attn.so")
@@ -59,6 +59,8 @@ def load():
     lib.lf_attn_set_band_events.argtypes = [P, P]
     lib.lf_attn_set_band_events.restype = ctypes.c_int
     lib.lf_attn_launch_count.restype = ctypes.c_uint64
+    lib.lf_attn_last_band_kernel.restype = ctypes.c_char_p
+    lib.lf_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.lf_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
     lib.lf_device_error.restype = ctypes.c_int
     _lib = lib
@@ -151,6 +153,16 @@ def set_band_events(start: Optional[torch.cuda.Event], stop: Optional[torch.cuda
 
 def launch_count() -> int:
     return int(load().lf_attn_launch_count())
+
+
+def last_band_kernel() -> str:
+    """Name of the band kernel the last call on this thread launched ("" before any)."""
+    return load().lf_attn_last_band_kernel().decode()
+
+
+def set_wait_limit_ns(ns: int):
+    """Limit of the kernels' pipeline waits on the current device (0: the 2 s default); for tests."""
+    _check(load().lf_set_wait_limit_ns(int(ns)))
 
 
 def device_error(clear: bool = False) -> int:

@@ -372,11 +372,11 @@ __device__ void band_producer(const BandParams& p, const BandSmem<D>& sm, int la
 #pragma unroll
   for (int s = 0; s < kSt; ++s)
     if (last_fill[s] >= 0)
-      mbar_wait(kIsV ? sm.v_full(s) : sm.k_full(s), ((uint32_t)last_fill[s] / kSt) & 1, &dummy, kRoleDrain, 200000000ull);
+      mbar_wait(kIsV ? sm.v_full(s) : sm.k_full(s), ((uint32_t)last_fill[s] / kSt) & 1, &dummy, kRoleDrain, kDrainLimitNs);
 #pragma unroll
   for (int s = 0; s < C::kQBuf; ++s)
-    if (last_q[s] >= 0) mbar_wait(sm.q_full(s), ((uint32_t)last_q[s] / C::kQBuf) & 1, &dummy, kRoleDrain, 200000000ull);
-  if (land_pending >= 0) mbar_wait(sm.v_land(), (uint32_t)land_pending & 1, &dummy, kRoleDrain, 200000000ull);
+    if (last_q[s] >= 0) mbar_wait(sm.q_full(s), ((uint32_t)last_q[s] / C::kQBuf) & 1, &dummy, kRoleDrain, kDrainLimitNs);
+  if (land_pending >= 0) mbar_wait(sm.v_land(), (uint32_t)land_pending & 1, &dummy, kRoleDrain, kDrainLimitNs);
 }
 
 // ------------------------------------------------------------------ MMA issue (per tile)
@@ -889,7 +889,7 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
     if (elect_one()) mma_commit(sm.fin());
     __syncwarp();
     int dummy = 0;
-    mbar_wait(sm.fin(), 0, &dummy, kRoleDrain, 200000000ull);
+    mbar_wait(sm.fin(), 0, &dummy, kRoleDrain, kDrainLimitNs);
     __syncwarp();
   }
 }
@@ -940,6 +940,7 @@ __global__ void __launch_bounds__(kBandThreads, 1) band_tc_kernel(const __grid_c
     }
     mbar_init(sm.fin(), 2);  // one commit per tile's issuing lane
     *sm.abort_flag() = 0;
+    *cta_wait_limit(sm.abort_flag()) = wait_limit_ns();
     for (int i = 0; i < 8; ++i) reinterpret_cast<volatile int*>(sm.segs() + kMaxSeg)[i] = 0;
     fence_barrier_init();
     fence_proxy_async_smem();

@@ -21,7 +21,7 @@
 // the kE-key "entries" that intersect the tile's windows, then the gathered
 // keys of the global tokens, and accumulates O = softmax(S) V online.
 //
-// Persistent CTAs (two per SM; one with 128-key entries, LF_RING_E=128), 8 warps each:
+// Persistent CTAs (two per SM), 8 warps each:
 //   warp 0     allocates TMEM; issues every tcgen05.mma (an elected lane of
 //              the converged warp): per entry g, O += P V of entry g once
 //              the softmax has written P, then S = Q K^T of entry g + kSBuf
@@ -60,12 +60,9 @@ constexpr int kGSmem = 1024;
 // D = 64: two CTAs per SM (so that two softmax warps share each SM
 // sub-partition and hide each other's latencies), 64-key entries, 256 TMEM
 // columns each.  D = 128: one CTA per SM, 128-key entries, all 512 columns.
-#ifndef LF_RING_E
-#define LF_RING_E 64  // keys per entry at D = 64
-#endif
 template <int D>
 struct BandCfg {
-  static constexpr bool kWide = (D == 128) || (LF_RING_E == 128);  // 128-key entries, one CTA per SM
+  static constexpr bool kWide = (D == 128);  // 128-key entries, one CTA per SM
   static constexpr int kE = kWide ? 128 : 64;       // keys per entry
   static constexpr int kCtaPerSm = kWide ? 1 : 2;
   static constexpr int kQBuf = 2;                  // Q tiles (the next item's Q loads early)
@@ -414,11 +411,11 @@ __device__ void band_producer(const BandParams& p, const BandSmem<D>& sm, int la
 #pragma unroll
   for (int s = 0; s < kSt; ++s)
     if (last_fill[s] >= 0)
-      mbar_wait(kIsV ? sm.v_full(s) : sm.k_full(s), ((uint32_t)last_fill[s] / kSt) & 1, &dummy, kRoleDrain, 200000000ull);
+      mbar_wait(kIsV ? sm.v_full(s) : sm.k_full(s), ((uint32_t)last_fill[s] / kSt) & 1, &dummy, kRoleDrain, kDrainLimitNs);
 #pragma unroll
   for (int s = 0; s < C::kQBuf; ++s)
-    if (last_q[s] >= 0) mbar_wait(sm.q_full(s), ((uint32_t)last_q[s] / C::kQBuf) & 1, &dummy, kRoleDrain, 200000000ull);
-  if (land_pending >= 0) mbar_wait(sm.v_land(), (uint32_t)land_pending & 1, &dummy, kRoleDrain, 200000000ull);
+    if (last_q[s] >= 0) mbar_wait(sm.q_full(s), ((uint32_t)last_q[s] / C::kQBuf) & 1, &dummy, kRoleDrain, kDrainLimitNs);
+  if (land_pending >= 0) mbar_wait(sm.v_land(), (uint32_t)land_pending & 1, &dummy, kRoleDrain, kDrainLimitNs);
 }
 
 // ------------------------------------------------------------------ V transposer (one warp)
@@ -667,7 +664,7 @@ __device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tm
   if (elect_one()) mma_commit(sm.fin());
   __syncwarp();
   int dummy = 0;
-  mbar_wait(sm.fin(), 0, &dummy, kRoleDrain, 200000000ull);
+  mbar_wait(sm.fin(), 0, &dummy, kRoleDrain, kDrainLimitNs);
   __syncwarp();
 }
 
@@ -1031,6 +1028,7 @@ __global__ void __launch_bounds__(kBandThreads, BandCfg<D>::kCtaPerSm)
     mbar_init(sm.o_empty(), 4);
     mbar_init(sm.fin(), 1);
     *sm.abort_flag() = 0;
+    *cta_wait_limit(sm.abort_flag()) = wait_limit_ns();
     fence_barrier_init();
     fence_proxy_async_smem();
   }

@@ -21,13 +21,42 @@
 namespace lf {
 
 // ------------------------------------------------------------------ band kernel choice
-// D = 64: the duo kernel (two 128-row tiles per item sharing 128-key loads,
-// one CTA per SM); its global-row mode still runs on the ring kernel (one
-// 128-row tile per CTA, two CTAs per SM, 64-key entries).  D = 128: the pair
-// kernel (two tiles per CTA sharing 128-key entries, one CTA per SM).
+// D = 64 has two tensor-core band kernels: the ring kernel (one 128-row tile
+// per CTA, two CTAs per SM, 64-key entries; also the global-row mode) and the
+// duo kernel (two 128-row tiles per item sharing 96-key loads, one CTA per
+// SM).  D = 128 runs the pair kernel (two tiles per CTA sharing 128-key
+// entries, one CTA per SM).
+enum class BandKernel { ring, duo, pair };
+
+
+static thread_local const char* t_band_kernel = "";
+
+// Host-side fault injection for tests: with the environment variable
+// LF_FAULT set to "alloc" (or "launch") a call reports that its scratch
+// allocation (or its first kernel launch) failed, at that point, before
+// anything of the call has run on the device.
+static bool injected_fault(const char* what) {
+  const char* f = std::getenv("LF_FAULT");
+  return f && std::strcmp(f, what) == 0;
+}
+
 lf_status launch_band_tc(const BandParams& p, int d, int grid, cudaStream_t s) {
-  if (d == 64) return p.gmode ? ringk::launch(p, grid, s) : duok::launch(p, grid, s);
-  if (d == 128) return pairk::launch(p, grid, s);
+  if (injected_fault("launch")) {
+    set_error("band kernel launch: injected failure (LF_FAULT=launch)");
+    return LF_ERR_CUDA;
+  }
+  if (d == 64 && (p.gmode || !p.pair_kernel)) {
+    if (!p.gmode) t_band_kernel = "band_ring";
+    return ringk::launch(p, grid, s);
+  }
+  if (d == 64) {
+    t_band_kernel = "band_duo";
+    return duok::launch(p, grid, s);
+  }
+  if (d == 128) {
+    t_band_kernel = "band_pair";
+    return pairk::launch(p, grid, s);
+  }
   set_error("band kernel: unsupported head dimension %d", d);
   return LF_ERR_UNSUPPORTED;
 }
@@ -267,17 +296,19 @@ static AuxStream* aux_stream() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxAuxDevices) return nullptr;
   AuxStream& a = t_aux[dev];
-  if (!a.s) {
-    if (cudaStreamCreateWithFlags(&a.s, cudaStreamNonBlocking) != cudaSuccess) {
-      cudaGetLastError();
-      a.s = nullptr;
-      return nullptr;
-    }
-    if (cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming) != cudaSuccess) {
-      cudaGetLastError();
-      return nullptr;
-    }
+  if (a.s && a.fork && a.join) return &a;
+  // Build all three or none: a half-built entry is destroyed, so that the
+  // next call starts over instead of using it.
+  bool ok = cudaStreamCreateWithFlags(&a.s, cudaStreamNonBlocking) == cudaSuccess;
+  ok = ok && cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming) == cudaSuccess;
+  ok = ok && cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();  // clear the sticky-free error of the failed create
+    if (a.join) cudaEventDestroy(a.join);
+    if (a.fork) cudaEventDestroy(a.fork);
+    if (a.s) cudaStreamDestroy(a.s);
+    a = AuxStream{};
+    return nullptr;
   }
   return &a;
 }
@@ -388,14 +419,29 @@ static lf_status run_global_band_bf16(const Problem& P, int b0, int nbat, BandPa
 // items are its 128-row tiles (D = 64) or pairs of them (D = 128).  Segments are generated in order straight
 // into the parameter block `p` (no heap use), one launch per kMaxSeg segments
 // or kMaxSets (dilation, residue) tensor-map sets.
+// For D = 64 the choice is measured (whole calls, one B300, L2 flushed):
+// with global tokens and a two-sided window the duo kernel is 3-22% faster
+// (it gathers the global key columns once per 256 rows instead of once per
+// 128); without global tokens, or with a one-sided (causal) window, the ring
+// kernel is 8-35% faster.
+static BandKernel band_kernel_for(const Problem& P) {
+  if (P.d == 128) return BandKernel::pair;
+  return (P.G > 0 && !P.causal) ? BandKernel::duo : BandKernel::ring;
+}
+
 static lf_status run_band_bf16(const Problem& P, int b0, int nbat, BandParams& p) {
-  const int grid_cap = sm_count();  // one persistent CTA per SM
+  const BandKernel kind = band_kernel_for(P);
+  // persistent CTAs: two per SM for the ring kernel, one for the others
+  const int grid_cap = sm_count() * (kind == BandKernel::ring ? ringk::BandCfg<64>::kCtaPerSm : 1);
   const int64_t half0 = std::min<int64_t>(P.w / 2, P.n);
   const int64_t right0 = P.causal ? 0 : half0;
-  // D = 64 pairs tiles when the window reach is a multiple of 16 keys (the
-  // tiles' key ranges then meet on 16-key steps); D = 128 always pairs.
-  const int pair = (P.d == 128) || (half0 % 16 == 0 && right0 % 16 == 0);
+  // The duo kernel pairs tiles when the window reach is a multiple of 16
+  // keys (the tiles' key ranges then meet on 16-key steps); the pair kernel
+  // always pairs, the ring kernel never.
+  const int pair = kind == BandKernel::pair || (kind == BandKernel::duo && half0 % 16 == 0 && right0 % 16 == 0);
   const int rows_per_item = pair ? 256 : 128;
+  // keys per K/V load
+  const int ek = kind == BandKernel::ring ? ringk::BandCfg<64>::kE : kind == BandKernel::duo ? duok::kLK : 128;
   const size_t off = (size_t)b0 * P.H * P.n * P.d;
   const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(P.q) + off;
   const __nv_bfloat16* k = reinterpret_cast<const __nv_bfloat16*>(P.k) + off;
@@ -443,7 +489,6 @@ static lf_status run_band_bf16(const Problem& P, int b0, int nbat, BandParams& p
       const int64_t rs = (int64_t)delta * P.d, ps = (int64_t)P.n * P.d;
       const size_t ro = (size_t)rr * P.d;
       lf_status st;
-      const int ek = 128;  // keys per K/V load
       if ((st = make_map(&p.tq[t], q + ro, P.d, n_r, planes, rs, ps, 128)) != LF_OK) return st;
       if ((st = make_map(&p.tk[t], k + ro, P.d, n_r, planes, rs, ps, ek)) != LF_OK) return st;
       if ((st = make_map(&p.tv[t], v + ro, P.d, n_r, planes, rs, ps, ek)) != LF_OK) return st;
@@ -459,6 +504,7 @@ static lf_status run_band_bf16(const Problem& P, int b0, int nbat, BandParams& p
     p.causal = P.causal;
     p.G = P.G;
     p.pair = pair;
+    p.pair_kernel = kind != BandKernel::ring;
     p.nseg = nseg;
     p.items_per_b = items_per_b;
     const int64_t total = (int64_t)items_per_b * nbat;
@@ -489,6 +535,11 @@ static lf_status run_band_f32(const Problem& P, int b0, int nbat) {
   const size_t off = (size_t)b0 * P.H * P.n * P.d;
   fill_pattern(sp->pat, P, b0, nbat);
   for (int h = 0; h < P.H; ++h) sp->dil[h] = P.dil[h];
+  if (injected_fault("launch")) {
+    set_error("band kernel launch: injected failure (LF_FAULT=launch)");
+    return LF_ERR_CUDA;
+  }
+  t_band_kernel = "band_simt_f32";
   return launch_band_simt_f32(*sp, reinterpret_cast<const float*>(P.q) + off,
                               reinterpret_cast<const float*>(P.k) + off,
                               reinterpret_cast<const float*>(P.v) + off,
@@ -552,7 +603,8 @@ static lf_status forward_t(const Problem& P, bool bf16) {
       global_chunk(P, nb, &nf);
       total += nf * sizeof(float) + global_counters((int64_t)nb * P.H, P.G) * sizeof(unsigned);
     }
-    cudaError_t e = cudaMallocAsync((void**)&ws, total, P.stream);
+    cudaError_t e = injected_fault("alloc") ? cudaErrorMemoryAllocation
+                                            : cudaMallocAsync((void**)&ws, total, P.stream);
     if (e != cudaSuccess) {
       cudaGetLastError();
       set_error("scratch allocation of %zu bytes failed: %s", total, cudaGetErrorString(e));
@@ -563,7 +615,10 @@ static lf_status forward_t(const Problem& P, bool bf16) {
   // pass, which can then run beside them; fp32: it runs after the band kernel
   if (P.G > 0 && bf16) {
     aux = aux_stream();
-    if (!(aux && record(aux->fork, P.stream) == LF_OK && wait_event(aux->s, aux->fork) == LF_OK)) aux = nullptr;
+    if (aux && !(record(aux->fork, P.stream) == LF_OK && wait_event(aux->s, aux->fork) == LF_OK)) {
+      cudaGetLastError();  // a failed fork only serialises the passes: clear it
+      aux = nullptr;
+    }
   }
   // ---- band kernel on the caller's stream, launched first so that it takes
   // the whole GPU; the global-row pass (side stream) then fills the SMs its
@@ -723,6 +778,8 @@ lf_status lf_attn_set_band_events(cudaEvent_t start, cudaEvent_t stop) {
 
 uint64_t lf_attn_launch_count(void) { return lf::g_launches.load(std::memory_order_relaxed); }
 
+const char* lf_attn_last_band_kernel(void) { return lf::t_band_kernel; }
+
 lf_status lf_device_error(uint32_t* code, int32_t clear) {
   if (!code) {
     lf::set_error("code must not be NULL");
@@ -736,6 +793,17 @@ lf_status lf_device_error(uint32_t* code, int32_t clear) {
   }
   if (e != cudaSuccess) {
     lf::set_error("reading the device error word: %s", cudaGetErrorString(e));
+    return LF_ERR_CUDA;
+  }
+  return LF_OK;
+}
+
+lf_status lf_set_wait_limit_ns(uint64_t ns) {
+  const uint64_t v = ns ? ns : lf::kWaitLimitDefaultNs;
+  cudaError_t e = cudaDeviceSynchronize();  // no running kernel reads it halfway
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(lf::g_wait_limit_ns, &v, sizeof v);
+  if (e != cudaSuccess) {
+    lf::set_error("setting the wait limit: %s", cudaGetErrorString(e));
     return LF_ERR_CUDA;
   }
   return LF_OK;

@@ -28,6 +28,11 @@ constexpr int kMaxGlobal = LF_MAX_GLOBAL;
 enum Role : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleDrain = 4, kRoleTranspose = 5 };
 // Defined once here: the library is built as a single translation unit.
 __device__ uint32_t g_device_error = 0;
+// Limit of the pipeline waits, in ns (settable for tests of the timeout
+// path); the drain waits at a kernel's end keep kDrainLimitNs.
+constexpr uint64_t kWaitLimitDefaultNs = 2000000000ull;
+constexpr uint64_t kDrainLimitNs = 200000000ull;
+__device__ uint64_t g_wait_limit_ns = kWaitLimitDefaultNs;
 
 // ----------------------------------------------------------------- timeline trace
 // Built only with -DLF_TRACE (a diagnostic build, never the product): the
@@ -75,6 +80,9 @@ struct BandParams {
   int32_t gmode, nrow_g;
   // Work items are pairs of consecutive 128-row tiles (1) or single tiles (0).
   int32_t pair;
+  // The launch runs a kernel that takes items of two tiles (duo, pair: 1) or
+  // the ring kernel (0).
+  int32_t pair_kernel;
   int32_t pad[kMaxBatch];
   BandSeg seg[kMaxSeg];
   int32_t gidx[kMaxGlobal];
@@ -199,6 +207,10 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive_cnt(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
@@ -207,10 +219,7 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 // Tests the phase; if it is not complete the thread may sleep until it
 // completes or about `hint_ns` pass (so waiting warps do not spin on the
 // issue slots of working ones).
-#ifndef LF_EXP_HINT
-#define LF_EXP_HINT 20000
-#endif
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t hint_ns = LF_EXP_HINT) {
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t hint_ns = 20000) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -235,18 +244,37 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait: gives up after `limit_ns` or when *abort becomes non-zero.
-// On giving up it records the role in the device error word, raises *abort
-// and returns false.
+// The pipeline waits' limit as set on the device.
+__device__ __forceinline__ uint64_t wait_limit_ns() {
+  return *reinterpret_cast<volatile uint64_t*>(&g_wait_limit_ns);
+}
+
+// Every kernel keeps its abort flag (an int at an address 4 mod 8) in shared
+// memory, followed by the CTA's copy of the pipeline-wait limit, which thread
+// 0 reads from wait_limit_ns() once at the kernel's start.
+__device__ __forceinline__ volatile uint64_t* cta_wait_limit(volatile int* abort) {
+  return reinterpret_cast<volatile uint64_t*>(abort + 1);
+}
+
+// Bounded wait: gives up after `limit_ns` (0: the CTA's pipeline limit; then
+// `abort` must be the CTA's abort flag) or when *abort becomes non-zero.  On
+// giving up it records the role in the device error word, raises *abort and
+// returns false.  Polls suspend for up to 20 us each; below a 20 us limit
+// they do not suspend at all and the limit is checked after every poll.
+// Time is counted in SM cycles at two per ns (the global timer can tick as
+// coarsely as 1 us): at least the limit at clocks up to 2 GHz.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          uint32_t role, uint64_t limit_ns = 2000000000ull) {
-  if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = global_timer_ns();
+                                          uint32_t role, uint64_t limit_ns = 0) {
+  if (mbar_test_wait(bar, parity)) return true;
+  if (limit_ns == 0) limit_ns = *cta_wait_limit(abort);
+  const bool short_limit = limit_ns < 20000ull;
+  const uint64_t limit_cyc = 2 * limit_ns;
+  const uint64_t c0 = clock64();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0) {
+    if (short_limit ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if (short_limit || (it & 7u) == 0) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > limit_ns) {
+      if ((uint64_t)clock64() - c0 > limit_cyc) {
         atomicCAS(&g_device_error, 0u, (uint32_t)LF_ERR_TIMEOUT | (role << 8));
         *abort = 1;
         return false;
@@ -487,6 +515,14 @@ __device__ __forceinline__ void tmem_st16_nw(uint32_t taddr, const uint32_t* r) 
       : "memory");
 }
 
+// 32 lanes x 8 columns from r[0..8) without waiting; complete with tmem_wait_st().
+__device__ __forceinline__ void tmem_st8_nw(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr), "r"(r[0]),
+      "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -517,6 +553,13 @@ __device__ __forceinline__ void stmatrix_x4(uint32_t addr, uint32_t x0, uint32_t
   asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr),
                "r"(x0), "r"(x1), "r"(x2), "r"(x3)
                : "memory");
+}
+
+// Per 16-bit half, the unsigned maximum.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
 __device__ __forceinline__ float max3f(float a, float b, float c) {

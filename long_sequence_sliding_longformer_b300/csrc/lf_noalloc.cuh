@@ -22,42 +22,25 @@
 // Included at the end of lf_attn.cu (the library's single translation unit).
 #pragma once
 
-#include <mutex>
 
 namespace lf {
 
 constexpr size_t kStaticScratchBytes = (size_t)16 << 20;
-constexpr int kMaxDevicesNoAlloc = 64;
 
 static __device__ __align__(256) float g_static_scratch[kStaticScratchBytes / sizeof(float)];
 
-static std::mutex g_static_scratch_mu;
-static float* g_static_scratch_addr[kMaxDevicesNoAlloc] = {};
-
-// Device address of g_static_scratch on the current device (looked up once).
+// Device address of g_static_scratch on the current device, looked up on
+// every call rather than cached, so that it stays right after the device's
+// context is torn down and rebuilt (cudaDeviceReset) between calls.
 static lf_status static_scratch_for_current_device(float** addr) {
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) {
-    set_error("cudaGetDevice: %s", cudaGetErrorString(e));
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+  if (e != cudaSuccess || !p) {
+    cudaGetLastError();
+    set_error("cudaGetSymbolAddress(static scratch): %s", cudaGetErrorString(e));
     return LF_ERR_CUDA;
   }
-  if (dev < 0 || dev >= kMaxDevicesNoAlloc) {
-    set_error("device %d is beyond the %d devices the no-alloc entry point tracks", dev,
-              kMaxDevicesNoAlloc);
-    return LF_ERR_UNSUPPORTED;
-  }
-  std::lock_guard<std::mutex> lock(g_static_scratch_mu);
-  if (!g_static_scratch_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess || !p) {
-      set_error("cudaGetSymbolAddress(static scratch) on device %d: %s", dev, cudaGetErrorString(e));
-      return LF_ERR_CUDA;
-    }
-    g_static_scratch_addr[dev] = static_cast<float*>(p);
-  }
-  *addr = g_static_scratch_addr[dev];
+  *addr = static_cast<float*>(p);
   return LF_OK;
 }
 

@@ -48,6 +48,8 @@ def _load():
         lib.lf_oracle_fwd.restype = ctypes.c_int
         lib.lf_oracle_attended.argtypes = [P, i32, i32, i32, i32, i32, P, i32, P, i32, i32, i32, P, P]
         lib.lf_oracle_attended.restype = i32
+        lib.lf_oracle_count_pairs.argtypes = [P, i32, i32, i32, i32, i32, P, i32, P, P, P]
+        lib.lf_oracle_count_pairs.restype = i32
         lib.lf_oracle_max_threads.restype = i32
         _lib = lib
     return _lib
@@ -157,6 +159,29 @@ def attended(*, n: int, w: int, dilation: Sequence[int], causal: bool = False,
     if cnt < 0:
         raise ValueError("oracle rejected the pattern")
     return sorted(int(x) for x in keys[:cnt]), bool(isg[0])
+
+
+def count_pairs(*, B: int, H: int, n: int, w: int, dilation: Sequence[int], causal: bool = False,
+                global_idx: Sequence[int] = (), pad_len: Optional[Sequence[int]] = None):
+    """(attended pairs over every row, pairs on the global tokens' own rows),
+    by enumerating each row's attended set."""
+    lib = _load()
+    dil = _i32(dilation)
+    gidx = _i32(global_idx) if len(global_idx) else None
+    pads = _i32(pad_len)
+    pairs = np.zeros(1, dtype=np.int64)
+    gpairs = np.zeros(1, dtype=np.int64)
+    rc = lib.lf_oracle_count_pairs(_ptr(gidx), len(global_idx), B, H, n, int(w), _ptr(dil),
+                                   int(bool(causal)), _ptr(pads), _ptr(pairs), _ptr(gpairs))
+    if rc != 0:
+        raise ValueError("oracle rejected the pattern")
+    return int(pairs[0]), int(gpairs[0])
+
+
+def wl_count_pairs(wl):
+    """count_pairs() for a workloads.Workload."""
+    return count_pairs(B=wl.B, H=wl.H, n=wl.n, w=wl.w, dilation=wl.dilation, causal=wl.causal,
+                       global_idx=wl.global_idx, pad_len=wl.pad_len)
 
 
 def wl_fwd(wl, inputs, rows=None, threads: int = 0) -> np.ndarray:

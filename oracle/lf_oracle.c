@@ -232,6 +232,42 @@ int32_t lf_oracle_attended(const int32_t* global_idx, int32_t G, int32_t B, int3
   return cnt;
 }
 
+/*
+ * Attended (row, key) pairs of a whole pattern, by enumerating every row's
+ * attended set: *pairs over all rows, *global_pairs over the global tokens'
+ * own rows.  Returns 0, or -1 for a rejected pattern.
+ */
+int32_t lf_oracle_count_pairs(const int32_t* global_idx, int32_t G, int32_t B, int32_t H,
+                              int32_t n, int32_t w, const int32_t* dilation, int32_t causal,
+                              const int32_t* pad_len, int64_t* pairs, int64_t* global_pairs) {
+  problem p = {ORC_F64, 0, 0, 0, 0, 0, 0, global_idx, G, B, H, n, 1, w, causal, dilation, pad_len};
+  if (check_problem(&p)) return -1;
+  int64_t tot = 0, gtot = 0;
+  int err = 0;
+#pragma omp parallel reduction(+ : tot, gtot) reduction(| : err)
+  {
+    int32_t* keys = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
+    if (!keys) {
+      err = 1;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int64_t bh = 0; bh < (int64_t)B * H; ++bh) {
+        for (int32_t i = 0; i < n; ++i) {
+          int g = 0;
+          int32_t cnt = attended_set(&p, (int32_t)(bh / H), (int32_t)(bh % H), i, keys, &g);
+          tot += cnt;
+          if (g) gtot += cnt;
+        }
+      }
+      free(keys);
+    }
+  }
+  if (err) return -1;
+  *pairs = tot;
+  *global_pairs = gtot;
+  return 0;
+}
+
 /* Number of threads an OpenMP region of this library would use. */
 int32_t lf_oracle_max_threads(void) {
 #ifdef _OPENMP

@@ -156,6 +156,33 @@ def test_pair_count_of_named_workloads(lib):
     assert pairs == want
 
 
+@pytest.mark.parametrize("B,H,n,w,dil,causal,pad,gidx", [
+    (2, 2, 100, 10, [1, 3], True, [0, 17], [0, 50]),
+    (1, 3, 37, 0, [1, 2, 5], False, [4], [1, 2, 36]),
+    (1, 2, 90, 12, [4, 1], True, None, list(range(0, 90, 9))),
+])
+def test_oracle_pattern_count_matches_row_sets(B, H, n, w, dil, causal, pad, gidx):
+    # the oracle's whole-pattern count (the benchmark's reference arm counts
+    # FLOPs with it) against the sum of its per-row attended sets
+    pairs, gpairs = oracle.count_pairs(B=B, H=H, n=n, w=w, dilation=dil, causal=causal,
+                                       global_idx=gidx, pad_len=pad)
+    assert pairs == _oracle_pairs(B, H, n, w, dil, causal, pad, gidx)
+    want_g = 0
+    for b in range(B):
+        L = n - (pad[b] if pad else 0)
+        want_g += H * sum((g + 1 if causal else L) for g in gidx if g < L)
+    assert gpairs == want_g
+
+
+@pytest.mark.parametrize("wl", workloads.all_workloads(), ids=lambda wl: wl.name)
+def test_pair_count_of_named_workloads_oracle_vs_library(lib, wl):
+    # both benchmark arms count the same useful work, each without the other's code
+    pairs, _ = oracle.wl_count_pairs(wl)
+    lpairs, _ = lf.count_pairs(B=wl.B, H=wl.H, n=wl.n, d=wl.d, w=wl.w, dilation=wl.dilation,
+                               causal=wl.causal, pad_len=wl.pad_len, global_idx=wl.global_idx)
+    assert pairs == lpairs
+
+
 def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     import importlib
     monkeypatch.setattr(lf, "LIB_PATH", str(tmp_path / "nope.so"))
