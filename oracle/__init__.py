@@ -48,6 +48,9 @@ def _load():
         lib.lf_oracle_fwd.restype = ctypes.c_int
         lib.lf_oracle_attended.argtypes = [P, i32, i32, i32, i32, i32, P, i32, P, i32, i32, i32, P, P]
         lib.lf_oracle_attended.restype = i32
+        lib.lf_oracle_bwd.argtypes = [ctypes.c_int, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
+                                      P, i32, P, P, P, P, P, P, P, i32]
+        lib.lf_oracle_bwd.restype = ctypes.c_int
         lib.lf_oracle_count_pairs.argtypes = [P, i32, i32, i32, i32, i32, P, i32, P, P, P]
         lib.lf_oracle_count_pairs.restype = i32
         lib.lf_oracle_max_threads.restype = i32
@@ -143,6 +146,51 @@ def fwd(q, k, v, *, w: int, dilation: Optional[Sequence[int]] = None, causal: bo
     return out
 
 
+def bwd(q, k, v, dout, *, w: int, dilation: Optional[Sequence[int]] = None, causal: bool = False,
+        pad_len: Optional[Sequence[int]] = None, qg=None, kg=None, vg=None,
+        global_idx: Sequence[int] = (), threads: int = 0) -> dict:
+    """Gradients of sum(dout * out) in float64: a dict with dq, dk, dv and,
+    when there are global tokens, dqg, dkg, dvg (each the shape of its input).
+    dout has out's shape and the inputs' dtype."""
+    lib = _load()
+    qa, code = _as_array(q)
+    ka, kc = _as_array(k)
+    va, vc = _as_array(v)
+    da, dc = _as_array(dout)
+    if not (code == kc == vc == dc):
+        raise TypeError("q, k, v, dout must share a dtype")
+    B, H, n, d = qa.shape
+    if ka.shape != qa.shape or va.shape != qa.shape or da.shape != qa.shape:
+        raise ValueError("q, k, v, dout shapes differ")
+    G = len(global_idx)
+    qga = kga = vga = None
+    if G:
+        qga, c1 = _as_array(qg)
+        kga, c2 = _as_array(kg)
+        vga, c3 = _as_array(vg)
+        if not (c1 == c2 == c3 == code):
+            raise TypeError("qg, kg, vg must share q's dtype")
+        if qga.shape != (B, H, G, d) or kga.shape != qa.shape or vga.shape != qa.shape:
+            raise ValueError("global tensor shapes do not match")
+    dil = _i32(dilation if dilation is not None else [1] * H)
+    if len(dil) != H:
+        raise ValueError("dilation needs one entry per head")
+    gidx = _i32(global_idx) if G else None
+    pads = _i32(pad_len)
+    g = {name: np.zeros((B, H, n, d), dtype=np.float64) for name in ("dq", "dk", "dv")}
+    if G:
+        g["dqg"] = np.zeros((B, H, G, d), dtype=np.float64)
+        g["dkg"] = np.zeros((B, H, n, d), dtype=np.float64)
+        g["dvg"] = np.zeros((B, H, n, d), dtype=np.float64)
+    rc = lib.lf_oracle_bwd(code, _ptr(qa), _ptr(ka), _ptr(va), _ptr(qga), _ptr(kga), _ptr(vga), _ptr(da),
+                           _ptr(gidx), G, B, H, n, d, int(w), _ptr(dil), int(bool(causal)), _ptr(pads),
+                           _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g.get("dqg")),
+                           _ptr(g.get("dkg")), _ptr(g.get("dvg")), int(threads))
+    if rc != 0:
+        raise ValueError("oracle rejected the problem (code %d)" % rc)
+    return g
+
+
 def attended(*, n: int, w: int, dilation: Sequence[int], causal: bool = False,
              global_idx: Sequence[int] = (), pad_len: Optional[Sequence[int]] = None,
              b: int = 0, h: int = 0, i: int = 0, B: int = 1):
@@ -182,6 +230,13 @@ def wl_count_pairs(wl):
     """count_pairs() for a workloads.Workload."""
     return count_pairs(B=wl.B, H=wl.H, n=wl.n, w=wl.w, dilation=wl.dilation, causal=wl.causal,
                        global_idx=wl.global_idx, pad_len=wl.pad_len)
+
+
+def wl_bwd(wl, inputs, dout, threads: int = 0) -> dict:
+    """bwd() for a workloads.Workload, its Inputs and an upstream gradient."""
+    return bwd(inputs.q, inputs.k, inputs.v, dout, w=wl.w, dilation=wl.dilation, causal=wl.causal,
+               pad_len=wl.pad_len, qg=inputs.qg, kg=inputs.kg, vg=inputs.vg,
+               global_idx=wl.global_idx, threads=threads)
 
 
 def wl_fwd(wl, inputs, rows=None, threads: int = 0) -> np.ndarray:

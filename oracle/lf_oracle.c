@@ -219,6 +219,130 @@ int lf_oracle_fwd(int dtype, const void* q, const void* k, const void* v,
   return err;
 }
 
+/*
+ * Backward of one row: with L = sum(dout * out), adds this row's share of
+ * dL/dq (or dL/dqg for a global row), dL/dk, dL/dv (or dL/dkg, dL/dvg) into
+ * the float64 gradient arrays.  The chain rule through the row's softmax,
+ * written out: p_t = softmax(s)_t with s_t = scale * <q_row, k_t>;
+ *   dv_t   += p_t * dout_row
+ *   dp_t    = <dout_row, v_t>
+ *   ds_t    = p_t * (dp_t - sum_u p_u dp_u)
+ *   dq_row += scale * sum_t ds_t k_t
+ *   dk_t   += scale * ds_t q_row
+ */
+static void one_row_bwd(const problem* p, const void* dout, int32_t b, int32_t h, int32_t i,
+                        int32_t* keys, double* scores, double* dp, double* dq, double* dk,
+                        double* dv, double* dqg, double* dkg, double* dvg) {
+  const int32_t n = p->n, d = p->d;
+  const int64_t bh = (int64_t)b * p->H + h;
+  int is_g = 0;
+  int32_t cnt = attended_set(p, b, h, i, keys, &is_g);
+  if (cnt == 0) return;
+  const void *qs, *ks, *vs;
+  double *dq_row, *dks, *dvs;
+  int64_t qrow;
+  if (is_g) {
+    qs = p->qg; ks = p->kg; vs = p->vg;
+    qrow = bh * p->G + global_rank(p, i);
+    dq_row = dqg + qrow * d; dks = dkg; dvs = dvg;
+  } else {
+    qs = p->q; ks = p->k; vs = p->v;
+    qrow = bh * n + i;
+    dq_row = dq + qrow * d; dks = dk; dvs = dv;
+  }
+  const int64_t orow = bh * n + i;  /* the row's output (and dout) position */
+  const double scale = 1.0 / sqrt((double)d);
+  /* softmax weights, exactly as the forward computes them */
+  double mx = -INFINITY;
+  for (int32_t t = 0; t < cnt; ++t) {
+    int64_t krow = bh * n + keys[t];
+    double s = 0.0;
+    for (int32_t c = 0; c < d; ++c)
+      s += load_elem(p->dtype, qs, qrow * d + c) * load_elem(p->dtype, ks, krow * d + c);
+    scores[t] = s * scale;
+    if (scores[t] > mx) mx = scores[t];
+  }
+  double total = 0.0;
+  for (int32_t t = 0; t < cnt; ++t) {
+    scores[t] = exp(scores[t] - mx);
+    total += scores[t];
+  }
+  for (int32_t t = 0; t < cnt; ++t) scores[t] /= total;  /* scores[] now holds p */
+  /* dp_t and their p-weighted sum */
+  double dsum = 0.0;
+  for (int32_t t = 0; t < cnt; ++t) {
+    int64_t vrow = bh * n + keys[t];
+    double x = 0.0;
+    for (int32_t c = 0; c < d; ++c)
+      x += load_elem(p->dtype, dout, orow * d + c) * load_elem(p->dtype, vs, vrow * d + c);
+    dp[t] = x;
+    dsum += scores[t] * x;
+  }
+  for (int32_t t = 0; t < cnt; ++t) {
+    int64_t kvrow = bh * n + keys[t];
+    double ds = scores[t] * (dp[t] - dsum);
+    for (int32_t c = 0; c < d; ++c) {
+      dvs[kvrow * d + c] += scores[t] * load_elem(p->dtype, dout, orow * d + c);
+      dq_row[c] += scale * ds * load_elem(p->dtype, ks, kvrow * d + c);
+      dks[kvrow * d + c] += scale * ds * load_elem(p->dtype, qs, qrow * d + c);
+    }
+  }
+}
+
+/*
+ * Gradients of L = sum(dout * out) with respect to q, k, v (float64 arrays
+ * [B, H, n, d]) and, when G > 0, qg ([B, H, G, d]), kg and vg ([B, H, n, d]).
+ * dout has the inputs' dtype and out's shape.  The arrays are zeroed here.
+ * Each (b, h) slice is independent (its rows only touch its own slices).
+ * Returns 0, 1 for an invalid problem, 2 if memory ran out.
+ */
+int lf_oracle_bwd(int dtype, const void* q, const void* k, const void* v,
+                  const void* qg, const void* kg, const void* vg, const void* dout,
+                  const int32_t* global_idx, int32_t G,
+                  int32_t B, int32_t H, int32_t n, int32_t d, int32_t w,
+                  const int32_t* dilation, int32_t causal, const int32_t* pad_len,
+                  double* dq, double* dk, double* dv, double* dqg, double* dkg, double* dvg,
+                  int32_t nthreads) {
+  problem p = {dtype, q, k, v, qg, kg, vg, global_idx, G, B, H, n, d, w, causal, dilation, pad_len};
+  if (check_problem(&p)) return 1;
+  if (!dq || !dk || !dv || (G > 0 && (!dqg || !dkg || !dvg))) return 1;
+  const size_t full = (size_t)B * H * n * d;
+  memset(dq, 0, full * sizeof(double));
+  memset(dk, 0, full * sizeof(double));
+  memset(dv, 0, full * sizeof(double));
+  if (G > 0) {
+    memset(dqg, 0, (size_t)B * H * G * d * sizeof(double));
+    memset(dkg, 0, full * sizeof(double));
+    memset(dvg, 0, full * sizeof(double));
+  }
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+  int err = 0;
+#pragma omp parallel
+  {
+    int32_t* keys = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
+    double* scores = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    double* dp = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    if (!keys || !scores || !dp) {
+#pragma omp atomic write
+      err = 2;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int64_t bh = 0; bh < (int64_t)B * H; ++bh)
+        for (int32_t i = 0; i < n; ++i)
+          one_row_bwd(&p, dout, (int32_t)(bh / H), (int32_t)(bh % H), i, keys, scores, dp, dq, dk,
+                      dv, dqg, dkg, dvg);
+    }
+    free(keys);
+    free(scores);
+    free(dp);
+  }
+  return err;
+}
+
 /* The attended key set of one row (for pattern tests).  keys must hold n ints. */
 int32_t lf_oracle_attended(const int32_t* global_idx, int32_t G, int32_t B, int32_t H,
                            int32_t n, int32_t w, const int32_t* dilation, int32_t causal,
