@@ -43,24 +43,31 @@ def peaks():
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
 
 
+# The sources of the forward kernels (device code); host planning lives in
+# lf_attn.cu, and the entry's kernel name is checked against the one that ran.
+FWD_KERNEL_FILES = ("lf_internal.cuh", "band_ring.cuh", "band_duo.cuh", "band_pair.cuh", "band_simt.cuh",
+                    "global_rows.cuh")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "long_sequence_sliding_longformer_b300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in FWD_KERNEL_FILES:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def committed_traffic(workload: str):
+def committed_traffic(workload: str, kernel: str):
     """DRAM bytes per band-kernel launch from a committed ncu summary, if it was
-    taken on the current kernel sources for this workload; else None."""
+    taken on the current kernel sources, for this workload and this kernel;
+    else None."""
     path = os.path.join(ROOT, "profiles", "band_traffic.json")
     if not os.path.exists(path):
         return None
     try:
         j = json.load(open(path))
         e = j.get(workload)
-        if e and e.get("source_hash") == kernel_source_hash():
+        if e and e.get("source_hash") == kernel_source_hash() and e.get("kernel") == kernel:
             return e.get("bytes_per_launch_full")
     except (ValueError, OSError):
         pass
@@ -393,7 +400,7 @@ def run_gpu(args, wl):
     band_avg_ms = statistics.mean(band_ms)
     band_achieved = band_flops / (band_avg_ms * 1e-3) / 1e12
     hbm_achieved = band_bytes(wl) / (band_avg_ms * 1e-3) / 1e9
-    traffic = committed_traffic(wl.name)
+    traffic = committed_traffic(wl.name, band_kernel)
     line = None
     if rank == 0:
         cs = clocks.summary()

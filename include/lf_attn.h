@@ -109,9 +109,10 @@ lf_status lf_attn_fwd_f32(const void* q, const void* k, const void* v,
  * Same arguments, semantics and results as lf_attn_fwd (bf16; results agree
  * within rounding, since the global rows may be split into longer key
  * chunks).  The scratch is a 16 MiB array inside the library that every GPU
- * loading the library holds until the process exits.  The first call on each
- * device looks up that array's device address, so make the first call on a
- * device before any stream capture.  Returns LF_ERR_UNSUPPORTED when
+ * loading the library holds until the process exits.  Every call looks up
+ * that array's device address (so it stays right after a device reset); the
+ * first lookup on a device may load the library's module there, so make the
+ * first call on a device before any stream capture.  Returns LF_ERR_UNSUPPORTED when
  * B*H*n_global*(d+2) fp32 values plus B*H*n_global 32-bit counters (per
  * block of 256 batch rows) exceed the array (never for d = 64 with
  * n_global >= 16, which needs no scratch).  Everything runs on `stream`.  All
@@ -126,6 +127,50 @@ lf_status lf_attn_fwd_noalloc(const void* q, const void* k, const void* v,
                               int32_t B, int32_t H, int32_t n, int32_t d,
                               int32_t w, const int32_t* dilation, int32_t causal,
                               const int32_t* pad_len, cudaStream_t stream);
+
+/*
+ * Backward of lf_attn_fwd: the gradients of L = sum(dout * out) with respect
+ * to q, k, v and, when n_global > 0, qg, kg, vg, where out is the forward's
+ * output for the same arguments.  The chain rule through each row's softmax
+ * over the same attended sets as the forward (section 3-1 "Attention
+ * Pattern"): with p the row's weights, dp_t = <dout_row, v_t> and
+ * D = sum_t p_t dp_t, ds_t = p_t (dp_t - D); dq_row = sum_t ds_t k_t / sqrt(d),
+ * dk_t += ds_t q_row / sqrt(d), dv_t += p_t dout_row.  A global token's row
+ * uses qg, kg, vg and adds into dqg, dkg, dvg.
+ *
+ * Inputs as for lf_attn_fwd (bf16, d = 64 or 128), plus dout: [B, H, n, d]
+ * bf16 device memory.  Outputs: dq, dk, dv, dkg, dvg [B, H, n, d] and dqg
+ * [B, H, G, d], fp32 device memory, 16-byte aligned, each written in full
+ * (padding rows and never-attended keys get zeros); none may overlap an
+ * input or another output.  dqg, dkg, dvg may be NULL iff n_global == 0.
+ * The row statistics are recomputed (no forward state is needed).  CUDA-core
+ * arithmetic in fp32 with a fixed summation order: repeated calls give the
+ * same bits.  Scratch of 8 * min(B, 256) * min(H, 256) * n bytes is
+ * allocated stream-ordered on `stream` (LF_ERR_NO_MEMORY if that fails).
+ * Two kernels per block of 256 batch rows and 256 heads, on `stream`.
+ */
+lf_status lf_attn_bwd(const void* q, const void* k, const void* v,
+                      const void* qg, const void* kg, const void* vg,
+                      const int32_t* global_idx, int32_t n_global,
+                      const void* dout,
+                      float* dq, float* dk, float* dv,
+                      float* dqg, float* dkg, float* dvg,
+                      int32_t B, int32_t H, int32_t n, int32_t d,
+                      int32_t w, const int32_t* dilation, int32_t causal,
+                      const int32_t* pad_len, cudaStream_t stream);
+
+/*
+ * fp32 backward: lf_attn_bwd with fp32 inputs (and dout); any d in [1, 128].
+ */
+lf_status lf_attn_bwd_f32(const void* q, const void* k, const void* v,
+                          const void* qg, const void* kg, const void* vg,
+                          const int32_t* global_idx, int32_t n_global,
+                          const void* dout,
+                          float* dq, float* dk, float* dv,
+                          float* dqg, float* dkg, float* dvg,
+                          int32_t B, int32_t H, int32_t n, int32_t d,
+                          int32_t w, const int32_t* dilation, int32_t causal,
+                          const int32_t* pad_len, cudaStream_t stream);
 
 /*
  * Host-only: the useful work of a problem, counted exactly from the pattern.

@@ -20,7 +20,7 @@ from typing import Optional, Sequence
 
 import torch
 
-__all__ = ["attn", "count_pairs", "set_band_events", "launch_count", "last_band_kernel", "set_wait_limit_ns", "device_error", "LfError",
+__all__ = ["attn", "attn_bwd", "count_pairs", "set_band_events", "launch_count", "last_band_kernel", "set_wait_limit_ns", "device_error", "LfError",
            "load", "LIB_PATH"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblf_attn.so")
@@ -49,6 +49,11 @@ def load():
     for name in ("lf_attn_fwd", "lf_attn_fwd_f32"):
         fn = getattr(lib, name)
         fn.argtypes = fwd_args
+        fn.restype = ctypes.c_int
+    bwd_args = [P, P, P, P, P, P, P, i32, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, P, i32, P, P]
+    for name in ("lf_attn_bwd", "lf_attn_bwd_f32"):
+        fn = getattr(lib, name)
+        fn.argtypes = bwd_args
         fn.restype = ctypes.c_int
     lib.lf_attn_count_pairs.argtypes = [i32, i32, i32, i32, i32, P, i32, P, P, i32,
                                         ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double)]
@@ -139,6 +144,60 @@ def count_pairs(*, B: int, H: int, n: int, d: int, w: int, dilation: Sequence[in
                                    _i32_array(pad_len), _i32_array(global_idx) if len(global_idx) else None,
                                    len(global_idx), ctypes.byref(pairs), ctypes.byref(flops)))
     return int(pairs.value), float(flops.value)
+
+
+def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dout: torch.Tensor, *, w: int,
+             dilation: Optional[Sequence[int]] = None, causal: bool = False,
+             pad_len: Optional[Sequence[int]] = None, qg: Optional[torch.Tensor] = None,
+             kg: Optional[torch.Tensor] = None, vg: Optional[torch.Tensor] = None,
+             global_idx: Sequence[int] = (), grads: Optional[dict] = None,
+             stream: Optional[torch.cuda.Stream] = None) -> dict:
+    """Gradients of sum(dout * attn(...)): a dict of fp32 tensors dq, dk, dv
+    and, with global tokens, dqg, dkg, dvg (preallocated ones may be passed in
+    `grads`)."""
+    lib = load()
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, n, d]")
+    B, H, n, d = q.shape
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("q must be bf16 or fp32, got %s" % q.dtype)
+    G = len(global_idx)
+    tensors = [("q", q), ("k", k), ("v", v), ("dout", dout)]
+    if G:
+        tensors += [("qg", qg), ("kg", kg), ("vg", vg)]
+    for name, t in tensors:
+        if t is None:
+            raise ValueError("%s is required" % name)
+        if not t.is_cuda or t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA tensor of dtype %s" % (name, q.dtype))
+        want = (B, H, G, d) if name == "qg" else (B, H, n, d)
+        if tuple(t.shape) != want:
+            raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), want))
+    names = ["dq", "dk", "dv"] + (["dqg", "dkg", "dvg"] if G else [])
+    g = dict(grads) if grads else {}
+    for name in names:
+        want = (B, H, G, d) if name == "dqg" else (B, H, n, d)
+        if name not in g:
+            g[name] = torch.empty(want, dtype=torch.float32, device=q.device)
+        t = g[name]
+        if tuple(t.shape) != want or t.dtype != torch.float32 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("%s must be a contiguous fp32 CUDA tensor of shape %s" % (name, want))
+    dil = _i32_array(dilation if dilation is not None else [1] * H)
+    if len(dilation if dilation is not None else [1] * H) != H:
+        raise ValueError("dilation needs one entry per head")
+    gidx = _i32_array(global_idx) if G else None
+    pads = _i32_array(pad_len)
+    if pad_len is not None and len(pad_len) != B:
+        raise ValueError("pad_len needs one entry per batch row")
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    fn = lib.lf_attn_bwd if q.dtype == torch.bfloat16 else lib.lf_attn_bwd_f32
+    gp = lambda name: _ptr(g[name]) if name in g else None
+    with torch.cuda.device(q.device):
+        _check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr(qg) if G else None,
+                  _ptr(kg) if G else None, _ptr(vg) if G else None, gidx, G, dout.data_ptr(),
+                  gp("dq"), gp("dk"), gp("dv"), gp("dqg"), gp("dkg"), gp("dvg"),
+                  B, H, n, d, int(w), dil, int(bool(causal)), pads, s.cuda_stream))
+    return {name: g[name] for name in names}
 
 
 def set_band_events(start: Optional[torch.cuda.Event], stop: Optional[torch.cuda.Event]):

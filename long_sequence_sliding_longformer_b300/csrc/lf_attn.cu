@@ -835,3 +835,5 @@ int lf_prof_dump(unsigned long long* dst) {
 
 // The allocation-free variant of lf_attn_fwd (same translation unit).
 #include "lf_noalloc.cuh"
+// The backward (same translation unit).
+#include "lf_bwd.cuh"

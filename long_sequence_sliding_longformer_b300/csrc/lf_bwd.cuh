@@ -1,0 +1,204 @@
+// lf_bwd.cuh -- host side of the backward (lf_attn_bwd, lf_attn_bwd_f32):
+// validation, scratch for the per-row statistics, and the launches of the
+// row and key passes of band_bwd.cuh, in blocks of at most kMaxBatch batch
+// rows and kMaxHeadsSimt heads.  Included at the end of lf_attn.cu (same
+// translation unit: it uses that file's validation and error helpers).
+#pragma once
+
+#include "band_bwd.cuh"
+
+namespace lf {
+
+struct BwdOut {
+  float *dq, *dk, *dv, *dqg, *dkg, *dvg;
+};
+
+static lf_status validate_bwd(const Problem& P, const void* dout, const BwdOut& g, bool bf16) {
+  lf_status st = validate_pattern(P);
+  if (st != LF_OK) return st;
+  if (bf16 && P.d != 64 && P.d != 128) {
+    set_error("bf16 backward supports d = 64 or 128 (got %d)", P.d);
+    return LF_ERR_UNSUPPORTED;
+  }
+  if (!bf16 && P.d > 128) {
+    set_error("fp32 backward supports d <= 128 (got %d)", P.d);
+    return LF_ERR_UNSUPPORTED;
+  }
+  if (P.n >= (1 << 28)) {
+    set_error("n must be < 2^28 (got %d)", P.n);
+    return LF_ERR_UNSUPPORTED;
+  }
+  const int64_t elems = (int64_t)P.B * P.H * P.n * P.d;
+  if (elems == 0) return LF_OK;
+  const bool G = P.G > 0;
+  const void* in[7] = {P.q, P.k, P.v, dout, P.qg, P.kg, P.vg};
+  const char* in_names[7] = {"q", "k", "v", "dout", "qg", "kg", "vg"};
+  const void* out[6] = {g.dq, g.dk, g.dv, g.dqg, g.dkg, g.dvg};
+  const char* out_names[6] = {"dq", "dk", "dv", "dqg", "dkg", "dvg"};
+  const int nin = G ? 7 : 4, nout = G ? 6 : 3;
+  for (int t = 0; t < nin; ++t) {
+    if (!in[t]) {
+      set_error("%s must not be NULL", in_names[t]);
+      return LF_ERR_INVALID_ARG;
+    }
+    if (((uintptr_t)in[t]) & 15) {
+      set_error("%s must be 16-byte aligned", in_names[t]);
+      return LF_ERR_INVALID_ARG;
+    }
+  }
+  for (int t = 0; t < nout; ++t) {
+    if (!out[t]) {
+      set_error("%s must not be NULL", out_names[t]);
+      return LF_ERR_INVALID_ARG;
+    }
+    if (((uintptr_t)out[t]) & 15) {
+      set_error("%s must be 16-byte aligned", out_names[t]);
+      return LF_ERR_INVALID_ARG;
+    }
+  }
+  // no gradient may overlap an input or another gradient
+  const size_t ib = (size_t)elems * P.elem, igb = (size_t)P.B * P.H * P.G * P.d * P.elem;
+  const size_t ob = (size_t)elems * sizeof(float), ogb = (size_t)P.B * P.H * P.G * P.d * sizeof(float);
+  for (int a = 0; a < nout; ++a) {
+    const size_t na = a == 3 ? ogb : ob;
+    for (int t = 0; t < nin; ++t)
+      if (overlaps(out[a], na, in[t], t == 4 ? igb : ib)) {
+        set_error("%s overlaps %s", out_names[a], in_names[t]);
+        return LF_ERR_INVALID_ARG;
+      }
+    for (int c = a + 1; c < nout; ++c)
+      if (overlaps(out[a], na, out[c], c == 3 ? ogb : ob)) {
+        set_error("%s overlaps %s", out_names[a], out_names[c]);
+        return LF_ERR_INVALID_ARG;
+      }
+  }
+  return LF_OK;
+}
+
+template <typename T, int D>
+static lf_status launch_bwd(const bwdk::BwdParams& bp, const void* q, const void* k, const void* v,
+                            const void* qg, const void* kg, const void* vg, const void* dout,
+                            const BwdOut& g, float2* stats, cudaStream_t s) {
+  if (injected_fault("launch")) {
+    set_error("backward launch: injected failure (LF_FAULT=launch)");
+    return LF_ERR_CUDA;
+  }
+  const int64_t warps = (int64_t)bp.B * bp.H * bp.n;
+  const unsigned grid = (unsigned)((warps + bwdk::kWarps - 1) / bwdk::kWarps);
+  const T *tq = (const T*)q, *tk = (const T*)k, *tv = (const T*)v;
+  const T *tqg = (const T*)qg, *tkg = (const T*)kg, *tvg = (const T*)vg, *tdo = (const T*)dout;
+  bwdk::bwd_row_kernel<T, D><<<grid, bwdk::kWarps * 32, 0, s>>>(bp, tq, tk, tv, tqg, tkg, tvg, tdo, g.dq,
+                                                                 g.dqg, stats);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) {
+    count_launch();
+    bwdk::bwd_key_kernel<T, D><<<grid, bwdk::kWarps * 32, 0, s>>>(bp, tq, tk, tv, tqg, tkg, tvg, tdo, g.dk,
+                                                                   g.dv, g.dkg, g.dvg, stats);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) count_launch();
+  }
+  if (e != cudaSuccess) {
+    set_error("backward launch: %s", cudaGetErrorString(e));
+    return LF_ERR_CUDA;
+  }
+  return LF_OK;
+}
+
+// The parameter block of the backward launches (~18 KB: kept off the stack;
+// each launch copies it), one per host thread.
+static bwdk::BwdParams* bwd_params() {
+  static thread_local bwdk::BwdParams* bp = nullptr;
+  if (!bp) bp = new (std::nothrow) bwdk::BwdParams;
+  if (!bp) set_error("host allocation of the backward parameter block failed");
+  return bp;
+}
+
+template <typename T>
+static lf_status backward_t(const Problem& P, const void* dout, const BwdOut& g) {
+  const int nbmax = std::min(P.B, kMaxBatch), nhmax = std::min(P.H, kMaxHeadsSimt);
+  const size_t sbytes = (size_t)nbmax * nhmax * P.n * sizeof(float2);
+  float2* stats = nullptr;
+  cudaError_t e = injected_fault("alloc") ? cudaErrorMemoryAllocation
+                                          : cudaMallocAsync((void**)&stats, sbytes, P.stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    set_error("scratch allocation of %zu bytes failed: %s", sbytes, cudaGetErrorString(e));
+    return LF_ERR_NO_MEMORY;
+  }
+  bwdk::BwdParams* holder = bwd_params();
+  lf_status st = holder ? LF_OK : LF_ERR_NO_MEMORY;
+  for (int b0 = 0; st == LF_OK && b0 < P.B; b0 += kMaxBatch) {
+    for (int h0 = 0; st == LF_OK && h0 < P.H; h0 += kMaxHeadsSimt) {
+      bwdk::BwdParams& bp = *holder;
+      memset(&bp, 0, sizeof bp);
+      bp.B = std::min(kMaxBatch, P.B - b0);
+      bp.H = std::min(kMaxHeadsSimt, P.H - h0);
+      bp.n = P.n;
+      bp.d = P.d;
+      bp.Htot = P.H;
+      bp.b0 = b0;
+      bp.h0 = h0;
+      const int64_t half = std::min<int64_t>(P.w / 2, P.n);
+      bp.half = (int32_t)half;
+      bp.right = P.causal ? 0 : (int32_t)half;
+      bp.causal = P.causal;
+      bp.G = P.G;
+      bp.scale = (float)(1.0 / std::sqrt((double)P.d));
+      bp.sl2 = (float)(1.4426950408889634 / std::sqrt((double)P.d));
+      for (int b = 0; b < bp.B; ++b) bp.pad[b] = P.pad ? P.pad[b0 + b] : 0;
+      for (int r = 0; r < P.G; ++r) bp.gidx[r] = P.gidx[r];
+      for (int h = 0; h < bp.H; ++h) bp.dil[h] = P.dil[h0 + h];
+      if (P.elem == 2) {
+        st = P.d == 64 ? launch_bwd<__nv_bfloat16, 64>(bp, P.q, P.k, P.v, P.qg, P.kg, P.vg, dout, g, stats, P.stream)
+                       : launch_bwd<__nv_bfloat16, 128>(bp, P.q, P.k, P.v, P.qg, P.kg, P.vg, dout, g, stats, P.stream);
+      } else if (P.d <= 32) {
+        st = launch_bwd<float, 32>(bp, P.q, P.k, P.v, P.qg, P.kg, P.vg, dout, g, stats, P.stream);
+      } else if (P.d <= 64) {
+        st = launch_bwd<float, 64>(bp, P.q, P.k, P.v, P.qg, P.kg, P.vg, dout, g, stats, P.stream);
+      } else {
+        st = launch_bwd<float, 128>(bp, P.q, P.k, P.v, P.qg, P.kg, P.vg, dout, g, stats, P.stream);
+      }
+    }
+  }
+  cudaError_t fe = cudaFreeAsync(stats, P.stream);
+  if (st == LF_OK && fe != cudaSuccess) {
+    set_error("scratch free: %s", cudaGetErrorString(fe));
+    st = LF_ERR_CUDA;
+  }
+  return st;
+}
+
+static lf_status backward(const Problem& P, const void* dout, const BwdOut& g, bool bf16) {
+  t_msg[0] = 0;
+  lf_status st = validate_bwd(P, dout, g, bf16);
+  if (st != LF_OK) return st;
+  if ((int64_t)P.B * P.H * P.n == 0) return LF_OK;
+  cudaGetLastError();  // a stale error from someone else must not be reported as ours
+  return bf16 ? backward_t<__nv_bfloat16>(P, dout, g) : backward_t<float>(P, dout, g);
+}
+
+}  // namespace lf
+
+extern "C" {
+
+lf_status lf_attn_bwd(const void* q, const void* k, const void* v, const void* qg, const void* kg,
+                      const void* vg, const int32_t* global_idx, int32_t n_global, const void* dout,
+                      float* dq, float* dk, float* dv, float* dqg, float* dkg, float* dvg, int32_t B,
+                      int32_t H, int32_t n, int32_t d, int32_t w, const int32_t* dilation, int32_t causal,
+                      const int32_t* pad_len, cudaStream_t stream) {
+  lf::Problem P{q, k, v, qg, kg, vg, global_idx, n_global, nullptr, B, H, n, d, w, dilation, causal,
+                pad_len, stream, 2};
+  return lf::backward(P, dout, lf::BwdOut{dq, dk, dv, dqg, dkg, dvg}, true);
+}
+
+lf_status lf_attn_bwd_f32(const void* q, const void* k, const void* v, const void* qg, const void* kg,
+                          const void* vg, const int32_t* global_idx, int32_t n_global, const void* dout,
+                          float* dq, float* dk, float* dv, float* dqg, float* dkg, float* dvg, int32_t B,
+                          int32_t H, int32_t n, int32_t d, int32_t w, const int32_t* dilation,
+                          int32_t causal, const int32_t* pad_len, cudaStream_t stream) {
+  lf::Problem P{q, k, v, qg, kg, vg, global_idx, n_global, nullptr, B, H, n, d, w, dilation, causal,
+                pad_len, stream, 4};
+  return lf::backward(P, dout, lf::BwdOut{dq, dk, dv, dqg, dkg, dvg}, false);
+}
+
+}  // extern "C"
