@@ -32,6 +32,9 @@ import workloads  # noqa: E402
 
 METRIC = "band-attn fwd useful TFLOP/s & % bf16 tensor peak; tokens/s vs n"
 L2_FLUSH_BYTES = 256 << 20
+# fp32 FMA rate of the CUDA cores (the backward's bound): 148 SMs x 128 lanes
+# x 2 flops x 2.032 GHz maximum SM clock
+FP32_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
 
 
 def peaks():
@@ -393,6 +396,29 @@ def run_gpu(args, wl):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_k, ws, dev)
     host_out = host_out[(e2e_k - 1) % 2]
 
+    # ---- backward (the gradients of sum(dout * out)) on the same inputs, one
+    # call per step, L2 flushed before each; events on the launching stream
+    gen = torch.Generator(device="cpu").manual_seed(wl.seed + 1000 + rank)
+    dout = torch.randn(tuple(inp.q.shape), generator=gen).to(inp.q.dtype).to(dev)
+    grads = lf.attn_bwd(inp.q, inp.k, inp.v, dout, w=wl.w, dilation=wl.dilation, causal=wl.causal,
+                        pad_len=wl.pad_len, qg=inp.qg, kg=inp.kg, vg=inp.vg, global_idx=wl.global_idx)
+    Kb = max(3, min(K, 30))
+    for _ in range(2):
+        lf.attn_bwd(inp.q, inp.k, inp.v, dout, w=wl.w, dilation=wl.dilation, causal=wl.causal,
+                    pad_len=wl.pad_len, qg=inp.qg, kg=inp.kg, vg=inp.vg, global_idx=wl.global_idx, grads=grads)
+    evb = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Kb)]
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    for i in range(Kb):
+        flush.zero_()
+        evb[i][0].record(stream)
+        lf.attn_bwd(inp.q, inp.k, inp.v, dout, w=wl.w, dilation=wl.dilation, causal=wl.causal,
+                    pad_len=wl.pad_len, qg=inp.qg, kg=inp.kg, vg=inp.vg, global_idx=wl.global_idx, grads=grads)
+        evb[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    bwd_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evb) / Kb, ws, dev)
+    del grads, dout
+
     pairs, flops, gflops_part = useful_work(wl)
     band_flops = flops - gflops_part
     pk = peaks()
@@ -425,6 +451,17 @@ def run_gpu(args, wl):
                        "steps": Kh, "l2": "not flushed between steps"},
             "e2e": {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "backward": {
+                "ms_per_step": bwd_ms, "steps": Kb, "unit": "TFLOP/s",
+                "value": ws * 2.0 * flops / (bwd_ms * 1e-3) / 1e12,
+                "flops_per_step": 2.0 * flops,
+                "flops_counted": "8*d per attended pair (dP, dV, dQ, dK; the recomputed scores not counted)",
+                "kernels": "bwd_row_kernel + bwd_key_kernel (CUDA cores, fp32)",
+                "roofline": {"bound": "alu", "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
+                             "achieved": 2.0 * flops / (bwd_ms * 1e-3) / 1e12,
+                             "frac": 2.0 * flops / (bwd_ms * 1e-3) / 1e12 / FP32_PEAK_TFLOPS,
+                             "peak_source": "148 SMs x 128 fp32 lanes x 2 flops x 2.032 GHz"},
+                "l2": "flushed before every step"},
             "gpu_launches": launches,
             "clocks": {"sm_mhz": cs["sm_mhz"], "sm_max_mhz": cs["sm_max_mhz"], "reasons": cs["reasons"],
                        "samples": cs["samples"]},
