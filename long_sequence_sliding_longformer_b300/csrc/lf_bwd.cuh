@@ -83,24 +83,38 @@ static lf_status launch_bwd(const bwdk::BwdParams& bp, const void* q, const void
     set_error("backward launch: injected failure (LF_FAULT=launch)");
     return LF_ERR_CUDA;
   }
-  const int64_t warps = (int64_t)bp.B * bp.H * bp.n;
-  const unsigned grid = (unsigned)((warps + bwdk::kWarps - 1) / bwdk::kWarps);
+  static std::atomic<uint64_t> rows_attr{0}, keys_attr{0};
+  constexpr int rows_smem = bwdk::rows_smem_bytes<D>(), keys_smem = bwdk::keys_smem_bytes<D>();
+  lf_status st = smem_attr_once((const void*)bwdk::bwd_rows_tiled<T, D>, rows_smem, rows_attr, "backward rows");
+  if (st == LF_OK)
+    st = smem_attr_once((const void*)bwdk::bwd_keys_tiled<T, D>, keys_smem, keys_attr, "backward keys");
+  if (st != LF_OK) return st;
   const T *tq = (const T*)q, *tk = (const T*)k, *tv = (const T*)v;
   const T *tqg = (const T*)qg, *tkg = (const T*)kg, *tvg = (const T*)vg, *tdo = (const T*)dout;
-  bwdk::bwd_row_kernel<T, D><<<grid, bwdk::kWarps * 32, 0, s>>>(bp, tq, tk, tv, tqg, tkg, tvg, tdo, g.dq,
-                                                                 g.dqg, stats);
-  cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess) {
-    count_launch();
-    bwdk::bwd_key_kernel<T, D><<<grid, bwdk::kWarps * 32, 0, s>>>(bp, tq, tk, tv, tqg, tkg, tvg, tdo, g.dk,
-                                                                   g.dv, g.dkg, g.dvg, stats);
-    e = cudaGetLastError();
-    if (e == cudaSuccess) count_launch();
+  const unsigned tiles = (unsigned)((int64_t)bp.B * bp.tiles_b);
+  const unsigned gblocks = (unsigned)((int64_t)bp.B * bp.H * bp.G);
+  const unsigned kwarps = (unsigned)(((int64_t)bp.B * bp.H * bp.n + bwdk::kWarps - 1) / bwdk::kWarps);
+  // statistics and dq, dqg; then dk, dv (band rows, then global columns' rows); then dkg, dvg
+  int launched = 0;
+  bwdk::bwd_rows_tiled<T, D><<<tiles, bwdk::kThreads, rows_smem, s>>>(bp, tq, tk, tv, tdo, g.dq, stats);
+  ++launched;
+  if (bp.G > 0) {
+    bwdk::bwd_grows<T, D><<<gblocks, bwdk::kWarps * 32, 0, s>>>(bp, tqg, tkg, tvg, tdo, g.dqg, stats);
+    ++launched;
   }
+  bwdk::bwd_keys_tiled<T, D><<<tiles, bwdk::kThreads, keys_smem, s>>>(bp, tq, tk, tv, tdo, g.dk, g.dv, stats);
+  ++launched;
+  if (bp.G > 0) {
+    bwdk::bwd_gkeys<T, D><<<gblocks, bwdk::kWarps * 32, 0, s>>>(bp, tq, tk, tv, tdo, g.dk, g.dv, stats);
+    bwdk::bwd_kgvg<T, D><<<kwarps, bwdk::kWarps * 32, 0, s>>>(bp, tqg, tkg, tvg, tdo, g.dkg, g.dvg, stats);
+    launched += 2;
+  }
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("backward launch: %s", cudaGetErrorString(e));
     return LF_ERR_CUDA;
   }
+  count_launch(launched);
   return LF_OK;
 }
 
@@ -147,7 +161,23 @@ static lf_status backward_t(const Problem& P, const void* dout, const BwdOut& g)
       bp.sl2 = (float)(1.4426950408889634 / std::sqrt((double)P.d));
       for (int b = 0; b < bp.B; ++b) bp.pad[b] = P.pad ? P.pad[b0 + b] : 0;
       for (int r = 0; r < P.G; ++r) bp.gidx[r] = P.gidx[r];
-      for (int h = 0; h < bp.H; ++h) bp.dil[h] = P.dil[h0 + h];
+      // tiles of 64 class positions: per head, the classes r < n % delta hold
+      // n / delta + 1 positions, the others n / delta
+      int64_t off = 0;
+      for (int h = 0; h < bp.H; ++h) {
+        const int delta = P.dil[h0 + h];
+        bp.dil[h] = delta;
+        bp.head_tile_off[h] = (int32_t)off;
+        const int64_t qn = P.n / delta, rem = P.n % delta;
+        off += rem * ((qn + 1 + bwdk::kTR - 1) / bwdk::kTR) + (delta - rem) * ((qn + bwdk::kTR - 1) / bwdk::kTR);
+      }
+      bp.head_tile_off[bp.H] = (int32_t)off;
+      if (off * bp.B > 0x7fffffff) {
+        st = LF_ERR_UNSUPPORTED;
+        set_error("too many backward tiles (%lld)", (long long)(off * bp.B));
+        break;
+      }
+      bp.tiles_b = (int32_t)off;
       if (P.elem == 2) {
         st = P.d == 64 ? launch_bwd<__nv_bfloat16, 64>(bp, P.q, P.k, P.v, P.qg, P.kg, P.vg, dout, g, stats, P.stream)
                        : launch_bwd<__nv_bfloat16, 128>(bp, P.q, P.k, P.v, P.qg, P.kg, P.vg, dout, g, stats, P.stream);

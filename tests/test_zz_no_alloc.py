@@ -70,3 +70,35 @@ def test_no_alloc_rejects_scratch_beyond_its_array():
            wl.B, wl.H, wl.n, wl.d, wl.w, _i32(wl.dilation), 0, None, None)
     assert st == 2
     assert "static scratch" in lib.lf_last_error_message().decode()
+
+
+@pytest.mark.gpu
+def test_no_alloc_grows_key_chunks_to_fit_on_the_d128_streaming_path():
+    """d = 128 takes the CUDA-core streaming pass for the global rows.  With
+    n = 200 the occupancy rule leaves 128-key chunks (two per row); 1500
+    (b, h) planes x 15 global tokens then need 23.4 MB of partial states, more
+    than the 16 MiB array, and the chunk grows to the whole row (11.7 MB)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    lib, f = _fn()
+    stream = torch.cuda.current_stream().cuda_stream
+    wl = workloads.custom("grow", "bf16", 6, 250, 200, 128, 32, (1,) * 250, False,
+                          tuple(range(0, 200, 14))[:15], None, seed=41)
+    assert wl.G == 15
+    inp = workloads.make_inputs(wl, "cuda")
+    ref = lf.attn(inp.q, inp.k, inp.v, w=wl.w, dilation=wl.dilation, causal=wl.causal,
+                  pad_len=wl.pad_len, qg=inp.qg, kg=inp.kg, vg=inp.vg, global_idx=wl.global_idx)
+    out = torch.full_like(inp.q, float("nan"))
+    st = _call(f, wl, inp, out, stream)
+    assert st == 0, lib.lf_last_error_message().decode()
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()
+    err = (out.float() - ref.float()).abs()
+    assert err.max().item() <= BF16_MAX and err.mean().item() <= BF16_MEAN
+    # the global tokens' rows against the oracle, row by row
+    import oracle
+    rows = np.array([(b * wl.H + h) * wl.n + g for b in (0, 5) for h in (0, 123, 249) for g in wl.global_idx])
+    want = oracle.wl_fwd(wl, inp, rows=rows)
+    got = out.float().cpu().numpy().reshape(-1, wl.d)[rows].astype(np.float64)
+    assert np.abs(got - want).max() <= BF16_MAX
+    assert lf.device_error() == 0
