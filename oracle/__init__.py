@@ -51,6 +51,8 @@ def _load():
         lib.lf_oracle_bwd.argtypes = [ctypes.c_int, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
                                       P, i32, P, P, P, P, P, P, P, i32]
         lib.lf_oracle_bwd.restype = ctypes.c_int
+        lib.lf_oracle_proj.argtypes = [ctypes.c_int, P, P, P, i32, i32, i32, i32, i32, i32, P, i32]
+        lib.lf_oracle_proj.restype = ctypes.c_int
         lib.lf_oracle_count_pairs.argtypes = [P, i32, i32, i32, i32, i32, P, i32, P, P, P]
         lib.lf_oracle_count_pairs.restype = i32
         lib.lf_oracle_max_threads.restype = i32
@@ -189,6 +191,32 @@ def bwd(q, k, v, dout, *, w: int, dilation: Optional[Sequence[int]] = None, caus
     if rc != 0:
         raise ValueError("oracle rejected the problem (code %d)" % rc)
     return g
+
+
+def proj(x, w, *, H: int, d: int, bias=None, threads: int = 0) -> np.ndarray:
+    """Per-head linear projections in float64: x [B, n, K] hidden states,
+    w [n_out*H*d, K] stacked weights, bias [n_out*H*d] (float32) or None ->
+    [n_out, B, H, n, d], y[t, b, h, i, c] = x[b, i] . w[t*H*d + h*d + c] + bias."""
+    lib = _load()
+    xa, code = _as_array(x)
+    wa, wc = _as_array(w)
+    if code != wc:
+        raise TypeError("x and w must share a dtype")
+    B, n, K = xa.shape
+    N = wa.shape[0]
+    if wa.shape[1] != K or N % (H * d) != 0:
+        raise ValueError("w must be [n_out*H*d, K]")
+    n_out = N // (H * d)
+    ba = None
+    if bias is not None:
+        ba = np.ascontiguousarray(np.asarray(bias.cpu() if hasattr(bias, "cpu") else bias, dtype=np.float32))
+        if ba.shape != (N,):
+            raise ValueError("bias must be [n_out*H*d]")
+    y = np.zeros((n_out, B, H, n, d), dtype=np.float64)
+    rc = lib.lf_oracle_proj(code, _ptr(xa), _ptr(wa), _ptr(ba), B, n, K, n_out, H, d, _ptr(y), int(threads))
+    if rc != 0:
+        raise ValueError("oracle rejected the projection sizes")
+    return y
 
 
 def attended(*, n: int, w: int, dilation: Sequence[int], causal: bool = False,

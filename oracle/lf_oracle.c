@@ -343,6 +343,39 @@ int lf_oracle_bwd(int dtype, const void* q, const void* k, const void* v,
   return err;
 }
 
+/*
+ * Linear projections of hidden states into per-head tensors (section 3-1,
+ * "Linear Projections for Global Attention": the band and the global
+ * attention each have their own W_q, W_k, W_v).  x: [B, n, K] hidden states;
+ * w: [N, K] with N = n_out * H * d, the weights of n_out projections stacked
+ * along N (row t*H*d + h*d + c gives output t, head h, column c); bias: [N]
+ * float32 or NULL.  y: float64 [n_out, B, H, n, d],
+ *   y[t, b, h, i, c] = sum_k x[b, i, k] * w[t*H*d + h*d + c, k] + bias[...].
+ * x and w share dtype.  Returns 0, or 1 for invalid sizes.
+ */
+int lf_oracle_proj(int dtype, const void* x, const void* w, const float* bias, int32_t B, int32_t n,
+                   int32_t K, int32_t n_out, int32_t H, int32_t d, double* y, int32_t nthreads) {
+  if (B < 0 || n < 0 || K < 1 || n_out < 1 || H < 1 || d < 1) return 1;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+  const int64_t N = (int64_t)n_out * H * d;
+#pragma omp parallel for schedule(static)
+  for (int64_t row = 0; row < (int64_t)B * n; ++row) {
+    const int64_t b = row / n, i = row % n;
+    for (int64_t col = 0; col < N; ++col) {
+      double acc = bias ? (double)bias[col] : 0.0;
+      for (int32_t kk = 0; kk < K; ++kk)
+        acc += load_elem(dtype, x, row * K + kk) * load_elem(dtype, w, col * K + kk);
+      const int64_t t = col / ((int64_t)H * d), h = (col / d) % H, c = col % d;
+      y[((((t * B + b) * H + h) * n) + i) * d + c] = acc;
+    }
+  }
+  return 0;
+}
+
 /* The attended key set of one row (for pattern tests).  keys must hold n ints. */
 int32_t lf_oracle_attended(const int32_t* global_idx, int32_t G, int32_t B, int32_t H,
                            int32_t n, int32_t w, const int32_t* dilation, int32_t causal,
