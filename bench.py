@@ -419,6 +419,43 @@ def run_gpu(args, wl):
     bwd_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evb) / Kb, ws, dev)
     del grads, dout
 
+    # ---- the projections that produce this workload's inputs from hidden
+    # states [B, n, H*d] (q, k, v, and kg, vg with global tokens: one call),
+    # bf16 workloads only; L2 flushed before each call
+    proj = None
+    if wl.dtype == "bf16":
+        Kh = wl.H * wl.d
+        n_out = 5 if wl.G > 0 else 3
+        genp = torch.Generator(device="cpu").manual_seed(wl.seed + 2000 + rank)
+        xh = torch.randn(wl.B, wl.n, Kh, generator=genp).to(torch.bfloat16).to(dev)
+        wh = (torch.randn(n_out * Kh, Kh, generator=genp) / Kh ** 0.5).to(torch.bfloat16).to(dev)
+        yh = lf.proj_heads(xh, wh, H=wl.H, d=wl.d)
+        for _ in range(2):
+            lf.proj_heads(xh, wh, H=wl.H, d=wl.d, out=yh)
+        Kp = max(3, min(K, 100))
+        evp = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Kp)]
+        barrier(ws)
+        torch.cuda.synchronize(dev)
+        for i in range(Kp):
+            flush.zero_()
+            evp[i][0].record(stream)
+            lf.proj_heads(xh, wh, H=wl.H, d=wl.d, out=yh)
+            evp[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        proj_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evp) / Kp, ws, dev)
+        pflops = 2.0 * wl.B * wl.n * Kh * n_out * Kh
+        pk0 = peaks()
+        proj = {"ms_per_call": proj_ms, "steps": Kp, "unit": "TFLOP/s",
+                "value": ws * pflops / (proj_ms * 1e-3) / 1e12, "flops_per_call": pflops,
+                "shape": {"M": wl.B * wl.n, "K": Kh, "N": n_out * Kh, "outputs": n_out},
+                "kernel": "proj_gemm_kernel (tcgen05)",
+                "roofline": {"bound": "tensor", "peak": pk0["bf16_tflops"], "unit": "TFLOP/s",
+                             "achieved": pflops / (proj_ms * 1e-3) / 1e12,
+                             "frac": pflops / (proj_ms * 1e-3) / 1e12 / pk0["bf16_tflops"],
+                             "peak_source": pk0["source"] + " (burst)"},
+                "l2": "flushed before every call"}
+        del xh, wh, yh
+
     pairs, flops, gflops_part = useful_work(wl)
     band_flops = flops - gflops_part
     pk = peaks()
@@ -462,6 +499,7 @@ def run_gpu(args, wl):
                              "frac": 2.0 * flops / (bwd_ms * 1e-3) / 1e12 / FP32_PEAK_TFLOPS,
                              "peak_source": "148 SMs x 128 fp32 lanes x 2 flops x 2.032 GHz"},
                 "l2": "flushed before every step"},
+            "projection": proj,
             "gpu_launches": launches,
             "clocks": {"sm_mhz": cs["sm_mhz"], "sm_max_mhz": cs["sm_max_mhz"], "reasons": cs["reasons"],
                        "samples": cs["samples"]},

@@ -173,6 +173,26 @@ lf_status lf_attn_bwd_f32(const void* q, const void* k, const void* v,
                           const int32_t* pad_len, cudaStream_t stream);
 
 /*
+ * Per-head linear projections of hidden states (section 3-1, "Linear
+ * Projections for Global Attention": the band and the global attention each
+ * use their own W_q, W_k, W_v), producing the inputs of lf_attn_fwd:
+ *   y[t, b, h, i, c] = sum_k x[b, i, k] * w[t*H*d + h*d + c, k] (+ bias[...])
+ * x: [B, n, K] bf16 hidden states; w: [n_out*H*d, K] bf16, the weights of
+ * n_out projections stacked row-wise (a row holds one output column's
+ * weights, as in a linear layer's [out, in] weight); bias: [n_out*H*d] fp32
+ * or NULL; y: [n_out, B, H, n, d] bf16, n_out consecutive head-major tensors
+ * (e.g. q, k, v, kg, vg with n_out = 5; qg from the global tokens' hidden
+ * states with its own weights in a second call).  All device memory, x, w, y
+ * 16-byte aligned, y not overlapping x or w.  Requires K a multiple of 64,
+ * d a multiple of 32 and n_out*H*d a multiple of 128 (LF_ERR_UNSUPPORTED
+ * otherwise).  Tensor cores (bf16 operands, fp32 accumulation, output rounded
+ * to bf16, nearest even); one launch on `stream`.
+ */
+lf_status lf_proj_heads(const void* x, const void* w, const float* bias, void* y,
+                        int32_t B, int32_t n, int32_t K, int32_t n_out, int32_t H, int32_t d,
+                        cudaStream_t stream);
+
+/*
  * Host-only: the useful work of a problem, counted exactly from the pattern.
  * *pairs = number of attended (query, key) pairs over all valid rows and
  * heads; *flops = 4 * d * pairs (one multiply-add each for QK^T and PV).

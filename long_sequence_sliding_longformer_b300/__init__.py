@@ -20,7 +20,7 @@ from typing import Optional, Sequence
 
 import torch
 
-__all__ = ["attn", "attn_bwd", "count_pairs", "set_band_events", "launch_count", "last_band_kernel", "set_wait_limit_ns", "device_error", "LfError",
+__all__ = ["attn", "attn_bwd", "proj_heads", "count_pairs", "set_band_events", "launch_count", "last_band_kernel", "set_wait_limit_ns", "device_error", "LfError",
            "load", "LIB_PATH"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblf_attn.so")
@@ -55,6 +55,8 @@ def load():
         fn = getattr(lib, name)
         fn.argtypes = bwd_args
         fn.restype = ctypes.c_int
+    lib.lf_proj_heads.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, P]
+    lib.lf_proj_heads.restype = ctypes.c_int
     lib.lf_attn_count_pairs.argtypes = [i32, i32, i32, i32, i32, P, i32, P, P, i32,
                                         ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double)]
     lib.lf_attn_count_pairs.restype = ctypes.c_int
@@ -198,6 +200,35 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dout: torch.Tens
                   gp("dq"), gp("dk"), gp("dv"), gp("dqg"), gp("dkg"), gp("dvg"),
                   B, H, n, d, int(w), dil, int(bool(causal)), pads, s.cuda_stream))
     return {name: g[name] for name in names}
+
+
+def proj_heads(x: torch.Tensor, w: torch.Tensor, *, H: int, d: int, bias: Optional[torch.Tensor] = None,
+               out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Per-head projections: x [B, n, K] bf16, w [n_out*H*d, K] bf16, bias
+    [n_out*H*d] fp32 or None -> [n_out, B, H, n, d] bf16."""
+    lib = load()
+    if x.dim() != 3 or w.dim() != 2:
+        raise ValueError("x must be [B, n, K] and w [n_out*H*d, K]")
+    B, n, K = x.shape
+    N = w.shape[0]
+    if w.shape[1] != K or N % (H * d) != 0:
+        raise ValueError("w must be [n_out*H*d, K]")
+    for name, t in (("x", x), ("w", w)):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous bf16 CUDA tensor" % name)
+    if bias is not None and (not bias.is_cuda or bias.dtype != torch.float32 or tuple(bias.shape) != (N,)
+                             or not bias.is_contiguous()):
+        raise ValueError("bias must be a contiguous fp32 CUDA tensor of shape [%d]" % N)
+    n_out = N // (H * d)
+    if out is None:
+        out = torch.empty((n_out, B, H, n, d), dtype=torch.bfloat16, device=x.device)
+    elif tuple(out.shape) != (n_out, B, H, n, d) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor of shape %s" % ((n_out, B, H, n, d),))
+    s = stream if stream is not None else torch.cuda.current_stream(x.device)
+    with torch.cuda.device(x.device):
+        _check(lib.lf_proj_heads(x.data_ptr(), w.data_ptr(), _ptr(bias) if bias is not None else None,
+                                 out.data_ptr(), B, n, K, n_out, H, d, s.cuda_stream))
+    return out
 
 
 def set_band_events(start: Optional[torch.cuda.Event], stop: Optional[torch.cuda.Event]):

@@ -837,3 +837,5 @@ int lf_prof_dump(unsigned long long* dst) {
 #include "lf_noalloc.cuh"
 // The backward (same translation unit).
 #include "lf_bwd.cuh"
+// The per-head projections (same translation unit).
+#include "lf_proj.cuh"
