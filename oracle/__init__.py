@@ -53,6 +53,8 @@ def _load():
         lib.lf_oracle_bwd.restype = ctypes.c_int
         lib.lf_oracle_proj.argtypes = [ctypes.c_int, P, P, P, i32, i32, i32, i32, i32, i32, P, i32]
         lib.lf_oracle_proj.restype = ctypes.c_int
+        lib.lf_oracle_mem_combine.argtypes = [ctypes.c_int, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P, i32]
+        lib.lf_oracle_mem_combine.restype = ctypes.c_int
         lib.lf_oracle_count_pairs.argtypes = [P, i32, i32, i32, i32, i32, P, i32, P, P, P]
         lib.lf_oracle_count_pairs.restype = i32
         lib.lf_oracle_max_threads.restype = i32
@@ -217,6 +219,34 @@ def proj(x, w, *, H: int, d: int, bias=None, threads: int = 0) -> np.ndarray:
     if rc != 0:
         raise ValueError("oracle rejected the projection sizes")
     return y
+
+
+def mem_combine(q, local, mem_k, mem_v, idx, gate, threads: int = 0) -> np.ndarray:
+    """Memory attention over retrieved (key, value) pairs mixed with the local
+    output, in float64: q, local [B, H, n, d]; mem_k, mem_v [B, H, M, d];
+    idx [B, H, n, km] int32 (-1: empty slot); gate [H] in [0, 1]."""
+    lib = _load()
+    qa, code = _as_array(q)
+    la, lc = _as_array(local)
+    ka, kc = _as_array(mem_k)
+    va, vc = _as_array(mem_v)
+    if not (code == lc == kc == vc):
+        raise TypeError("q, local, mem_k, mem_v must share a dtype")
+    B, H, n, d = qa.shape
+    M = ka.shape[2]
+    ia = np.ascontiguousarray(np.asarray(idx.cpu() if hasattr(idx, "cpu") else idx, dtype=np.int32))
+    km = ia.shape[3]
+    if la.shape != qa.shape or ka.shape != (B, H, M, d) or va.shape != ka.shape or ia.shape != (B, H, n, km):
+        raise ValueError("shapes do not match")
+    ga = np.ascontiguousarray(np.asarray(gate.cpu() if hasattr(gate, "cpu") else gate, dtype=np.float64))
+    if ga.shape != (H,):
+        raise ValueError("gate needs one weight per head")
+    out = np.zeros((B, H, n, d), dtype=np.float64)
+    rc = lib.lf_oracle_mem_combine(code, _ptr(qa), _ptr(la), _ptr(ka), _ptr(va), _ptr(ia), _ptr(ga), B, H, n, d,
+                                   M, km, _ptr(out), int(threads))
+    if rc != 0:
+        raise ValueError("oracle rejected the memory combine (sizes or an index out of range)")
+    return out
 
 
 def attended(*, n: int, w: int, dilation: Sequence[int], causal: bool = False,

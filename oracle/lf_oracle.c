@@ -376,6 +376,68 @@ int lf_oracle_proj(int dtype, const void* x, const void* w, const float* bias, i
   return 0;
 }
 
+/*
+ * Memory attention combined with the local output (Memorizing Transformer
+ * notes, section "Memorizing Transformer": each query also attends the k
+ * (key, value) pairs a kNN lookup retrieved from a memory of earlier
+ * segments, and the two results are mixed per head by a scalar weight).
+ * q, local: [B, H, n, d]; mem_k, mem_v: [B, H, M, d] (the memory of each
+ * (b, h)); idx: [B, H, n, km] int32 positions in that memory, -1 for an empty
+ * slot; gate: [H] weights in [0, 1].  out: float64 [B, H, n, d],
+ *   o_mem = sum_j softmax_j(<q, mem_k[idx_j]> / sqrt(d)) mem_v[idx_j] over the
+ *           non-empty slots (zero if every slot is empty),
+ *   out = gate[h] * o_mem + (1 - gate[h]) * local.
+ * q, local, mem_k, mem_v share dtype.  Returns 0, or 1 for invalid sizes or
+ * an index outside [-1, M).
+ */
+int lf_oracle_mem_combine(int dtype, const void* q, const void* local, const void* mem_k, const void* mem_v,
+                          const int32_t* idx, const double* gate, int32_t B, int32_t H, int32_t n, int32_t d,
+                          int32_t M, int32_t km, double* out, int32_t nthreads) {
+  if (B < 0 || H < 1 || n < 0 || d < 1 || M < 0 || km < 1) return 1;
+  for (int64_t t = 0; t < (int64_t)B * H * n * km; ++t)
+    if (idx[t] < -1 || idx[t] >= M) return 1;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+  const double scale = 1.0 / sqrt((double)d);
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)km);
+#pragma omp for schedule(static)
+    for (int64_t row = 0; row < (int64_t)B * H * n; ++row) {
+      const int64_t bh = row / n;
+      const int32_t h = (int32_t)(bh % H);
+      const int32_t* ix = idx + row * km;
+      double mx = -INFINITY;
+      for (int32_t j = 0; j < km; ++j) {
+        s[j] = -INFINITY;
+        if (ix[j] < 0) continue;
+        double acc = 0.0;
+        for (int32_t c = 0; c < d; ++c)
+          acc += load_elem(dtype, q, row * d + c) * load_elem(dtype, mem_k, (bh * M + ix[j]) * d + c);
+        s[j] = acc * scale;
+        if (s[j] > mx) mx = s[j];
+      }
+      double total = 0.0;
+      for (int32_t j = 0; j < km; ++j) {
+        s[j] = (ix[j] < 0) ? 0.0 : exp(s[j] - mx);
+        total += s[j];
+      }
+      for (int32_t c = 0; c < d; ++c) {
+        double om = 0.0;
+        for (int32_t j = 0; j < km; ++j)
+          if (ix[j] >= 0) om += s[j] * load_elem(dtype, mem_v, (bh * M + ix[j]) * d + c);
+        if (total > 0.0) om /= total;
+        out[row * d + c] = gate[h] * om + (1.0 - gate[h]) * load_elem(dtype, local, row * d + c);
+      }
+    }
+    free(s);
+  }
+  return 0;
+}
+
 /* The attended key set of one row (for pattern tests).  keys must hold n ints. */
 int32_t lf_oracle_attended(const int32_t* global_idx, int32_t G, int32_t B, int32_t H,
                            int32_t n, int32_t w, const int32_t* dilation, int32_t causal,
