@@ -456,6 +456,44 @@ def run_gpu(args, wl):
                 "l2": "flushed before every call"}
         del xh, wh, yh
 
+    # ---- the Memorizing-Transformer combine on this workload's shape: 32
+    # pairs per query retrieved (uniformly at random) from a 65536-entry
+    # memory per (b, h), mixed with the band output; HBM-bound gathers
+    memc = None
+    if wl.dtype == "bf16":
+        Mm, km = 65536, 32
+        genm = torch.Generator(device="cpu").manual_seed(wl.seed + 3000 + rank)
+        mk = torch.randn(wl.B, wl.H, Mm, wl.d, generator=genm).to(torch.bfloat16).to(dev)
+        mv = torch.randn(wl.B, wl.H, Mm, wl.d, generator=genm).to(torch.bfloat16).to(dev)
+        midx = torch.randint(0, Mm, (wl.B, wl.H, wl.n, km), generator=genm, dtype=torch.int32).to(dev)
+        gate = torch.rand(wl.H, generator=genm).to(dev)
+        mout = torch.empty_like(out)
+        lf.mem_combine(inp.q, out, mk, mv, midx, gate, out=mout)
+        Km = max(3, min(K, 100))
+        evm = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Km)]
+        barrier(ws)
+        torch.cuda.synchronize(dev)
+        for i in range(Km):
+            flush.zero_()
+            evm[i][0].record(stream)
+            lf.mem_combine(inp.q, out, mk, mv, midx, gate, out=mout)
+            evm[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        mem_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evm) / Km, ws, dev)
+        rows_m = wl.B * wl.H * wl.n
+        mbytes = rows_m * (3 * wl.d * 2 + km * 4 + km * 2 * wl.d * 2)
+        pk1 = peaks()
+        memc = {"ms_per_call": mem_ms, "steps": Km, "memory_entries": Mm, "retrieved_per_query": km,
+                "bytes_per_call": mbytes,
+                "bytes_counted": "q, local, out rows + the indices + the retrieved key and value rows, each once per query",
+                "kernel": "mem_combine_kernel (CUDA cores)",
+                "roofline": {"bound": "hbm", "peak": pk1["hbm_gbs"], "unit": "GB/s",
+                             "achieved": mbytes / (mem_ms * 1e-3) / 1e9,
+                             "frac": mbytes / (mem_ms * 1e-3) / 1e9 / pk1["hbm_gbs"],
+                             "peak_source": pk1["source"]},
+                "l2": "flushed before every call"}
+        del mk, mv, midx, mout
+
     pairs, flops, gflops_part = useful_work(wl)
     band_flops = flops - gflops_part
     pk = peaks()
@@ -500,6 +538,7 @@ def run_gpu(args, wl):
                              "peak_source": "148 SMs x 128 fp32 lanes x 2 flops x 2.032 GHz"},
                 "l2": "flushed before every step"},
             "projection": proj,
+            "memory_combine": memc,
             "gpu_launches": launches,
             "clocks": {"sm_mhz": cs["sm_mhz"], "sm_max_mhz": cs["sm_max_mhz"], "reasons": cs["reasons"],
                        "samples": cs["samples"]},

@@ -193,6 +193,30 @@ lf_status lf_proj_heads(const void* x, const void* w, const float* bias, void* y
                         cudaStream_t stream);
 
 /*
+ * Memorizing-Transformer combine (Memorizing Transformer notes, section
+ * "Memorizing Transformer"): each query also attends the km (key, value)
+ * pairs a kNN lookup retrieved from a memory of earlier segments, and the
+ * two results are mixed per head:
+ *   o_mem = sum_j softmax_j(<q, mem_k[idx_j]> / sqrt(d)) mem_v[idx_j]
+ *           over the non-empty slots (zero if every slot is empty)
+ *   out   = gate[h] * o_mem + (1 - gate[h]) * local
+ * q, local, out: [B, H, n, d] bf16 (local: the band attention's output; out
+ * may be local itself, not any other input); mem_k, mem_v: [B, H, M, d] bf16
+ * (the memory of each (b, h); may be NULL iff M == 0); idx: [B, H, n, km]
+ * int32 positions in that memory, -1 for an empty slot; gate: [H] fp32
+ * weights (the per-head scalar, already mapped to [0, 1] by the caller).
+ * All device memory; bf16 tensors 16-byte aligned, idx and gate 4-byte.
+ * d = 64 or 128; 1 <= km <= 32.  The lookup itself is not part of this call.
+ * An index outside [-1, M) is treated as an empty slot and recorded in the
+ * device error word (LF_ERR_INVALID_ARG, role 7; see lf_device_error).
+ * CUDA cores, fp32 arithmetic; one launch on `stream`.
+ */
+lf_status lf_mem_combine(const void* q, const void* local, const void* mem_k, const void* mem_v,
+                         const int32_t* idx, const float* gate, void* out,
+                         int32_t B, int32_t H, int32_t n, int32_t d, int32_t M, int32_t km,
+                         cudaStream_t stream);
+
+/*
  * Host-only: the useful work of a problem, counted exactly from the pattern.
  * *pairs = number of attended (query, key) pairs over all valid rows and
  * heads; *flops = 4 * d * pairs (one multiply-add each for QK^T and PV).
@@ -229,7 +253,8 @@ const char* lf_attn_last_band_kernel(void);
 /*
  * Synchronises the current device and reads the library's device error word
  * (0 = none; otherwise LF_ERR_TIMEOUT in the low byte and the kernel role
- * that gave up in the next byte).  clear != 0 resets it to 0.
+ * that gave up in the next byte, or LF_ERR_INVALID_ARG with role 7 when
+ * lf_mem_combine met an index out of range).  clear != 0 resets it to 0.
  */
 lf_status lf_device_error(uint32_t* code, int32_t clear);
 

@@ -20,7 +20,7 @@ from typing import Optional, Sequence
 
 import torch
 
-__all__ = ["attn", "attn_bwd", "proj_heads", "count_pairs", "set_band_events", "launch_count", "last_band_kernel", "set_wait_limit_ns", "device_error", "LfError",
+__all__ = ["attn", "attn_bwd", "proj_heads", "mem_combine", "count_pairs", "set_band_events", "launch_count", "last_band_kernel", "set_wait_limit_ns", "device_error", "LfError",
            "load", "LIB_PATH"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblf_attn.so")
@@ -57,6 +57,8 @@ def load():
         fn.restype = ctypes.c_int
     lib.lf_proj_heads.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, P]
     lib.lf_proj_heads.restype = ctypes.c_int
+    lib.lf_mem_combine.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P]
+    lib.lf_mem_combine.restype = ctypes.c_int
     lib.lf_attn_count_pairs.argtypes = [i32, i32, i32, i32, i32, P, i32, P, P, i32,
                                         ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double)]
     lib.lf_attn_count_pairs.restype = ctypes.c_int
@@ -228,6 +230,33 @@ def proj_heads(x: torch.Tensor, w: torch.Tensor, *, H: int, d: int, bias: Option
     with torch.cuda.device(x.device):
         _check(lib.lf_proj_heads(x.data_ptr(), w.data_ptr(), _ptr(bias) if bias is not None else None,
                                  out.data_ptr(), B, n, K, n_out, H, d, s.cuda_stream))
+    return out
+
+
+def mem_combine(q: torch.Tensor, local: torch.Tensor, mem_k: torch.Tensor, mem_v: torch.Tensor,
+                idx: torch.Tensor, gate: torch.Tensor, *, out: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """gate[h] * attention(q, retrieved memory pairs) + (1 - gate[h]) * local.
+    q, local [B, H, n, d] bf16; mem_k, mem_v [B, H, M, d] bf16; idx [B, H, n, km]
+    int32 (-1: empty slot); gate [H] fp32.  out may be local (in place)."""
+    lib = load()
+    B, H, n, d = q.shape
+    M, km = mem_k.shape[2], idx.shape[3]
+    checks = [("q", q, torch.bfloat16, (B, H, n, d)), ("local", local, torch.bfloat16, (B, H, n, d)),
+              ("mem_k", mem_k, torch.bfloat16, (B, H, M, d)), ("mem_v", mem_v, torch.bfloat16, (B, H, M, d)),
+              ("idx", idx, torch.int32, (B, H, n, km)), ("gate", gate, torch.float32, (H,))]
+    for name, t, dt, shape in checks:
+        if not t.is_cuda or t.dtype != dt or not t.is_contiguous() or tuple(t.shape) != shape:
+            raise ValueError("%s must be a contiguous %s CUDA tensor of shape %s" % (name, dt, shape))
+    if out is None:
+        out = torch.empty_like(q)
+    elif tuple(out.shape) != (B, H, n, d) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor of q's shape")
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        _check(lib.lf_mem_combine(q.data_ptr(), local.data_ptr(), mem_k.data_ptr(), mem_v.data_ptr(),
+                                  idx.data_ptr(), gate.data_ptr(), out.data_ptr(), B, H, n, d, M, km,
+                                  s.cuda_stream))
     return out
 
 

@@ -839,3 +839,5 @@ int lf_prof_dump(unsigned long long* dst) {
 #include "lf_bwd.cuh"
 // The per-head projections (same translation unit).
 #include "lf_proj.cuh"
+// The memory combine (same translation unit).
+#include "mem_combine.cuh"
