@@ -217,6 +217,42 @@ lf_status lf_mem_combine(const void* q, const void* local, const void* mem_k, co
                          cudaStream_t stream);
 
 /*
+ * Global tokens that differ between batch rows (section 3-1 "Global
+ * Attention": the question tokens of a QA example are its global tokens, and
+ * questions differ per example).  Batch row b's global positions are
+ * global_idx[global_offsets[b] .. global_offsets[b+1]) (host arrays;
+ * global_offsets has B + 1 entries, starts at 0, non-decreasing; each row's
+ * list strictly increasing in [0, n)).  qg is packed: batch row b's
+ * [H, G_b, d] block starts at row global_offsets[b] * H (elements
+ * global_offsets[b] * H * d).  kg, vg: [B, H, n, d] as for lf_attn_fwd (may
+ * be NULL iff every row has no global token).  Everything else as for
+ * lf_attn_fwd (bf16).  Runs each batch row's forward in turn on `stream`;
+ * every row is validated before anything is enqueued.
+ */
+lf_status lf_attn_fwd_varglobal(const void* q, const void* k, const void* v,
+                                const void* qg, const void* kg, const void* vg,
+                                const int32_t* global_offsets, const int32_t* global_idx,
+                                void* out,
+                                int32_t B, int32_t H, int32_t n, int32_t d,
+                                int32_t w, const int32_t* dilation, int32_t causal,
+                                const int32_t* pad_len, cudaStream_t stream);
+
+/*
+ * Backward of lf_attn_fwd_varglobal: as lf_attn_bwd, with the global lists
+ * and the packed qg of lf_attn_fwd_varglobal; dqg is packed like qg; the dkg,
+ * dvg rows of a batch row without global tokens are written as zeros.
+ */
+lf_status lf_attn_bwd_varglobal(const void* q, const void* k, const void* v,
+                                const void* qg, const void* kg, const void* vg,
+                                const int32_t* global_offsets, const int32_t* global_idx,
+                                const void* dout,
+                                float* dq, float* dk, float* dv,
+                                float* dqg, float* dkg, float* dvg,
+                                int32_t B, int32_t H, int32_t n, int32_t d,
+                                int32_t w, const int32_t* dilation, int32_t causal,
+                                const int32_t* pad_len, cudaStream_t stream);
+
+/*
  * Host-only: the useful work of a problem, counted exactly from the pattern.
  * *pairs = number of attended (query, key) pairs over all valid rows and
  * heads; *flops = 4 * d * pairs (one multiply-add each for QK^T and PV).

@@ -20,7 +20,7 @@ from typing import Optional, Sequence
 
 import torch
 
-__all__ = ["attn", "attn_bwd", "proj_heads", "mem_combine", "count_pairs", "set_band_events", "launch_count", "last_band_kernel", "set_wait_limit_ns", "device_error", "LfError",
+__all__ = ["attn", "attn_bwd", "proj_heads", "mem_combine", "attn_varglobal", "attn_bwd_varglobal", "count_pairs", "set_band_events", "launch_count", "last_band_kernel", "set_wait_limit_ns", "device_error", "LfError",
            "load", "LIB_PATH"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblf_attn.so")
@@ -59,6 +59,11 @@ def load():
     lib.lf_proj_heads.restype = ctypes.c_int
     lib.lf_mem_combine.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P]
     lib.lf_mem_combine.restype = ctypes.c_int
+    lib.lf_attn_fwd_varglobal.argtypes = [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, P, i32, P, P]
+    lib.lf_attn_fwd_varglobal.restype = ctypes.c_int
+    lib.lf_attn_bwd_varglobal.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, P, P,
+                                          i32, i32, i32, i32, i32, P, i32, P, P]
+    lib.lf_attn_bwd_varglobal.restype = ctypes.c_int
     lib.lf_attn_count_pairs.argtypes = [i32, i32, i32, i32, i32, P, i32, P, P, i32,
                                         ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double)]
     lib.lf_attn_count_pairs.restype = ctypes.c_int
@@ -258,6 +263,78 @@ def mem_combine(q: torch.Tensor, local: torch.Tensor, mem_k: torch.Tensor, mem_v
                                   idx.data_ptr(), gate.data_ptr(), out.data_ptr(), B, H, n, d, M, km,
                                   s.cuda_stream))
     return out
+
+
+def attn_varglobal(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, w: int,
+                   global_idx: Sequence[Sequence[int]], qg: Optional[torch.Tensor] = None,
+                   kg: Optional[torch.Tensor] = None, vg: Optional[torch.Tensor] = None,
+                   dilation: Optional[Sequence[int]] = None, causal: bool = False,
+                   pad_len: Optional[Sequence[int]] = None, out: Optional[torch.Tensor] = None,
+                   stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """attn() with one global list per batch row: global_idx[b] lists batch row
+    b's global positions; qg packs the rows' [H, G_b, d] blocks one after the
+    other ([sum_b H * G_b, d] or any shape with that many elements)."""
+    lib = load()
+    B, H, n, d = q.shape
+    if len(global_idx) != B:
+        raise ValueError("global_idx needs one list per batch row")
+    offs = [0]
+    for lst in global_idx:
+        offs.append(offs[-1] + len(lst))
+    total = offs[-1]
+    for name, t in (("q", q), ("k", k), ("v", v)) + ((("kg", kg), ("vg", vg)) if total else ()):
+        if t is None or not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or tuple(t.shape) != (B, H, n, d):
+            raise ValueError("%s must be a contiguous bf16 CUDA tensor of shape %s" % (name, (B, H, n, d)))
+    if total and (qg is None or not qg.is_cuda or qg.dtype != torch.bfloat16 or not qg.is_contiguous()
+                  or qg.numel() != total * H * d):
+        raise ValueError("qg must be a contiguous bf16 CUDA tensor of %d elements" % (total * H * d))
+    if out is None:
+        out = torch.empty_like(q)
+    flat = [int(x) for lst in global_idx for x in lst]
+    dil = _i32_array(dilation if dilation is not None else [1] * H)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        _check(lib.lf_attn_fwd_varglobal(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                         _ptr(qg) if total else None, _ptr(kg) if total else None,
+                                         _ptr(vg) if total else None, _i32_array(offs),
+                                         _i32_array(flat) if total else None, out.data_ptr(), B, H, n, d,
+                                         int(w), dil, int(bool(causal)), _i32_array(pad_len), s.cuda_stream))
+    return out
+
+
+def attn_bwd_varglobal(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dout: torch.Tensor, *, w: int,
+                       global_idx: Sequence[Sequence[int]], qg: Optional[torch.Tensor] = None,
+                       kg: Optional[torch.Tensor] = None, vg: Optional[torch.Tensor] = None,
+                       dilation: Optional[Sequence[int]] = None, causal: bool = False,
+                       pad_len: Optional[Sequence[int]] = None,
+                       stream: Optional[torch.cuda.Stream] = None) -> dict:
+    """attn_bwd() for attn_varglobal(): fp32 dq, dk, dv and, with any global
+    token, dqg (packed like qg), dkg, dvg."""
+    lib = load()
+    B, H, n, d = q.shape
+    offs = [0]
+    for lst in global_idx:
+        offs.append(offs[-1] + len(lst))
+    total = offs[-1]
+    if dout.shape != q.shape or dout.dtype != q.dtype or not dout.is_contiguous():
+        raise ValueError("dout must be a contiguous tensor like q")
+    f32 = lambda shape: torch.empty(shape, dtype=torch.float32, device=q.device)
+    g = {"dq": f32((B, H, n, d)), "dk": f32((B, H, n, d)), "dv": f32((B, H, n, d))}
+    if total:
+        g.update(dqg=f32((total * H, d)), dkg=f32((B, H, n, d)), dvg=f32((B, H, n, d)))
+    flat = [int(x) for lst in global_idx for x in lst]
+    dil = _i32_array(dilation if dilation is not None else [1] * H)
+    gp = lambda name: _ptr(g[name]) if name in g else None
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        _check(lib.lf_attn_bwd_varglobal(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                         _ptr(qg) if total else None, _ptr(kg) if total else None,
+                                         _ptr(vg) if total else None, _i32_array(offs),
+                                         _i32_array(flat) if total else None, dout.data_ptr(),
+                                         gp("dq"), gp("dk"), gp("dv"), gp("dqg"), gp("dkg"), gp("dvg"),
+                                         B, H, n, d, int(w), dil, int(bool(causal)), _i32_array(pad_len),
+                                         s.cuda_stream))
+    return g
 
 
 def set_band_events(start: Optional[torch.cuda.Event], stop: Optional[torch.cuda.Event]):

@@ -841,3 +841,5 @@ int lf_prof_dump(unsigned long long* dst) {
 #include "lf_proj.cuh"
 // The memory combine (same translation unit).
 #include "mem_combine.cuh"
+// Global tokens that differ between batch rows (same translation unit).
+#include "lf_varglobal.cuh"
