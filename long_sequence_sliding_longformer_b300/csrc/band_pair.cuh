@@ -23,14 +23,15 @@
 //   warp 0     allocates TMEM; V producer: TMA loads of the V entries into
 //              a ring of shared-memory slots, gathers of global-token rows
 //   warp 1     Q/K producer: TMA loads of Q and of the K entries
-//   warps 2-3  transpose each V entry into V^T (the layout the P.V MMA reads
-//              at full rate)
+//   warps 2-3  no role (they keep the register split of the warpgroups)
 //   warps 4-7  softmax of tile 0, warps 8-11 softmax of tile 1: one query row
 //              per thread; S rows are read from TMEM, masked, turned into
 //              P = exp2(S*scale - m) with a lazily updated row maximum, and P
 //              (bf16) is written back to TMEM; an elected lane of the tile's
 //              first warp then issues the tile's tcgen05.mma products,
-//              O_X += P_X V (V^T from shared memory) and the next
+//              O_X += P_X V (V read MN-major straight from the TMA slot: the
+//              instruction descriptor's transpose bit, the two 64-column
+//              boxes one leading-dimension offset apart) and the next
 //              S_X = Q_X K^T (both operands in shared memory)
 // While the softmax warps of one tile compute, the tensor cores can run the
 // other tile's products.
@@ -55,18 +56,16 @@ template <int D>
 struct BandCfg {
   static constexpr int kQBuf = 1;                  // Q is reloaded ~2 steps before an item ends
   static constexpr int kKSt = (D == 64) ? 5 : 2;   // K slots
-  static constexpr int kVSt = (D == 64) ? 3 : 1;   // V slots (as loaded: [keys, D])
-  static constexpr int kTSt = (D == 64) ? 4 : 2;   // V^T slots ([D, keys], the P.V operand)
+  static constexpr int kVSt = 3;                   // V slots (as loaded: [keys, D]; the P.V operand)
   static constexpr int kTile = 128 * D * 2;     // bytes of one [128, D] bf16 tile
   static constexpr int kOffQ = 0;               // Q[qb][X] at kOffQ + (2*qb + X) * kTile
   static constexpr int kOffK = kQBuf * 2 * kTile;
   static constexpr int kOffV = kOffK + kKSt * kTile;
-  static constexpr int kOffVT = kOffV + kVSt * kTile;
-  static constexpr int kOffBar = kOffVT + kTSt * kTile;
+  static constexpr int kOffBar = kOffV + kVSt * kTile;
   // q_full[2], q_empty[2], k_full[8], k_empty[8], v_full[4], v_empty[4], v_land,
-  // s_full[2], (unused)[2], p_full[2], pv_done[2], (unused)[2], fin, vt_full[4], vt_empty[4]
+  // s_full[2], (unused)[2], p_full[2], pv_done[2], (unused)[2], fin, (unused)[8]
   static constexpr int kNumBar = 2 + 2 + 8 + 8 + 4 + 4 + 1 + 2 + 2 + 2 + 2 + 2 + 1 + 4 + 4;
-  static_assert(kKSt <= 8 && kVSt <= 4 && kTSt <= 4 && kQBuf <= 2, "barrier arrays");
+  static_assert(kKSt <= 8 && kVSt <= 4 && kQBuf <= 2, "barrier arrays");
   static constexpr int kOffMisc = kOffBar + kNumBar * 8;
   static constexpr int kSmem = kOffMisc + 16 + kMaxSeg * (int)sizeof(BandSeg) + 32 + 1024;  // + slack to align the base to 1024
   static constexpr int kTmemCols = 512;
@@ -221,7 +220,6 @@ struct BandSmem {
   __device__ __forceinline__ uint32_t q(int qb, int X) const { return sbase + C::kOffQ + (2 * qb + X) * C::kTile; }
   __device__ __forceinline__ uint32_t k(int s) const { return sbase + C::kOffK + s * C::kTile; }
   __device__ __forceinline__ uint32_t v(int s) const { return sbase + C::kOffV + s * C::kTile; }
-  __device__ __forceinline__ uint32_t vt(int s) const { return sbase + C::kOffVT + s * C::kTile; }
   __device__ __forceinline__ uint8_t* k_ptr(int s) const { return base + C::kOffK + s * C::kTile; }
   __device__ __forceinline__ uint8_t* v_ptr(int s) const { return base + C::kOffV + s * C::kTile; }
   __device__ __forceinline__ uint32_t bar(int i) const { return sbase + C::kOffBar + 8 * i; }
@@ -236,8 +234,6 @@ struct BandSmem {
   __device__ __forceinline__ uint32_t p_full(int X) const { return bar(33 + X); }
   __device__ __forceinline__ uint32_t pv_done(int X) const { return bar(35 + X); }
   __device__ __forceinline__ uint32_t fin() const { return bar(39); }
-  __device__ __forceinline__ uint32_t vt_full(int s) const { return bar(40 + s); }
-  __device__ __forceinline__ uint32_t vt_empty(int s) const { return bar(44 + s); }
   __device__ __forceinline__ uint32_t* tmem_holder() const { return reinterpret_cast<uint32_t*>(base + C::kOffMisc); }
   __device__ __forceinline__ volatile int* abort_flag() const { return reinterpret_cast<volatile int*>(base + C::kOffMisc + 4); }
   __device__ __forceinline__ BandSeg* segs() const { return reinterpret_cast<BandSeg*>(base + C::kOffMisc + 16); }
@@ -259,8 +255,8 @@ __device__ __forceinline__ int residue_coord(int g, int r, int delta) {
 
 // ------------------------------------------------------------------ producers
 // Two warps: KV = false loads Q and the K entries, KV = true the V entries,
-// so that a full V ring (waiting for the transposer) never holds back the K
-// an S product needs.
+// so that a full V ring (waiting for the P.V products) never holds back the
+// K an S product needs.
 template <int D, bool kIsV>
 __device__ void band_producer(const BandParams& p, const BandSmem<D>& sm, int lane) {
   using C = BandCfg<D>;
@@ -386,7 +382,7 @@ __device__ void band_producer(const BandParams& p, const BandSmem<D>& sm, int la
 // Q_X K(j+1)^T (in that order: S_X(j+1) overwrites P_X(j)).  The whole warp
 // runs the bookkeeping so that descriptors stay in uniform registers.
 //
-// K and V^T slots are released by both tiles: each slot's "empty" barrier
+// K and V slots are released by both tiles: each slot's "empty" barrier
 // takes one arrival per tile and fill, from tcgen05.commit after the tile's
 // last product that reads it, or a plain arrival from a tile that does not
 // use the entry once that fill is visible (so the arrival cannot count
@@ -407,9 +403,12 @@ struct TileIssuer {
       : sm(sm_), abort(sm_.abort_flag()), X(X_), tmem(tmem_) {
     qdesc0 = smem_desc_sw128(sm.q(0, 0), 16, 1024);
     kdesc0 = smem_desc_sw128(sm.k(0), 16, 1024);
-    vdesc0 = smem_desc_sw128(sm.vt(0), 16, 1024);
+    // V as loaded: MN-major (D contiguous), 64-column boxes of [128 keys,
+    // 128 bytes] one after the other (the leading-dimension offset between
+    // the boxes), 8-key groups 1024 bytes apart
+    vdesc0 = smem_desc_sw128(sm.v(0), 128 * 128, 1024);
     idesc_s128 = idesc_bf16_f32(128, 128, 0);
-    idesc_pv = idesc_bf16_f32(128, D, 0);  // V^T: K-major
+    idesc_pv = idesc_bf16_f32(128, D, 1);
   }
 
   // columns of global entry e (its padded token count)
@@ -420,7 +419,7 @@ struct TileIssuer {
   }
 
   // Entry e (fill kv + e) is not read by this tile: release its K slot
-  // (skip_k) and its V^T slot (skip_v).  A tile must not wait for a V^T fill
+  // (skip_k) and its V slot (skip_v).  A tile must not wait for a V fill
   // it skips before issuing the P.V of its own earlier entries: with a
   // shallow ring that fill may need the very slot the P.V still holds.
   __device__ bool skip_k(uint32_t kv, int e) const {
@@ -433,9 +432,9 @@ struct TileIssuer {
   }
   __device__ bool skip_v(uint32_t kv, int e) const {
     const uint32_t f = kv + e;
-    const int ts = f % C::kTSt;
-    if (!warp_wait(sm.vt_full(ts), (f / C::kTSt) & 1, abort, kRoleSoftmax)) return false;
-    if (elect_one()) mbar_arrive(sm.vt_empty(ts));
+    const int vs = f % C::kVSt;
+    if (!warp_wait(sm.v_full(vs), (f / C::kVSt) & 1, abort, kRoleSoftmax)) return false;
+    if (elect_one()) mbar_arrive(sm.v_empty(vs));
     __syncwarp();
     return true;
   }
@@ -446,10 +445,10 @@ struct TileIssuer {
     const uint32_t f = kv + e;
     return warp_wait(sm.k_full(f % C::kKSt), (f / C::kKSt) & 1, abort, kRoleSoftmax);
   }
-  // V^T(e) is ready
+  // V(e) has landed
   __device__ bool wait_v(uint32_t kv, int e) const {
     const uint32_t f = kv + e;
-    return warp_wait(sm.vt_full(f % C::kTSt), (f / C::kTSt) & 1, abort, kRoleSoftmax);
+    return warp_wait(sm.v_full(f % C::kVSt), (f / C::kVSt) & 1, abort, kRoleSoftmax);
   }
 
   // S_X = Q_X K(e)^T into TMEM (K(e) already waited for); `last_s` also releases Q
@@ -483,7 +482,7 @@ struct TileIssuer {
   __device__ bool issue_pv(const PairItem& it, uint32_t kv, int e, bool first, bool last,
                            bool waited = false) const {
     const uint32_t f = kv + e;
-    const int ts = f % C::kTSt;
+    const int vs = f % C::kVSt;
     // key steps of 16 that some row of this tile attends: value rows outside
     // them (the partner tile's keys) are never read
     int kk0 = 0, kk1;
@@ -498,8 +497,8 @@ struct TileIssuer {
     const uint32_t acc0 = first ? 0u : 1u;
     const uint32_t pt = tmem + C::kColS + 128 * X;  // P_X over the first 64 columns of S_X
     const uint32_t ot = tmem + C::kColO + D * X;
-    // V^T: 64-key blocks of [D rows, 128 bytes]; a 16-key step is 32 bytes
-    const uint64_t vd = vdesc0 + ts * kTile16;
+    // V: a 16-key step is 16 rows of 128 bytes
+    const uint64_t vd = vdesc0 + vs * kTile16;
     if (!waited && !wait_v(kv, e)) return false;
     if (tr) tr->ev(20);
     tc_fence_after();
@@ -507,73 +506,23 @@ struct TileIssuer {
       if (full) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = ((kk >> 2) * (D * 128) + (kk & 3) * 32) >> 4;
+          const uint32_t off = (kk * 16 * 128) >> 4;
           mma_bf16_ts(ot, pt + kk * 8, vd + off, idesc_pv, kk > 0 ? 1u : acc0);
         }
       } else {
         for (int kk = kk0; kk <= kk1; ++kk) {
-          const uint32_t off = ((kk >> 2) * (D * 128) + (kk & 3) * 32) >> 4;
+          const uint32_t off = (kk * 16 * 128) >> 4;
           mma_bf16_ts(ot, pt + kk * 8, vd + off, idesc_pv, kk > kk0 ? 1u : acc0);
         }
       }
       if (last) mma_commit(sm.pv_done(X));  // O_X complete: the epilogue may read it
-      mma_commit(sm.vt_empty(ts));
+      mma_commit(sm.v_empty(vs));
     }
     __syncwarp();
     if (tr) tr->ev(21);
     return true;
   }
 };
-
-// ------------------------------------------------------------------ V transposer (two warps)
-// The P.V product takes V as a K-major operand (keys contiguous), which the
-// tensor cores read at full rate from a [D, keys] layout.  TMA delivers V as
-// [keys, D]; warp w of the pair moves keys [64w, 64w + 64) of every entry
-// into 8x8 blocks of V^T with ldmatrix.trans / stmatrix, both 128-byte
-// swizzled.
-template <int D>
-__device__ void band_transposer(const BandParams& p, const BandSmem<D>& sm, int w, int lane) {
-  using C = BandCfg<D>;
-  volatile int* abort = sm.abort_flag();
-  uint32_t kv = 0;
-  bool ok = true;
-  const int m = lane >> 3, r = lane & 7;  // this lane addresses row r of matrix m
-  Tracer tr;
-  if (blockIdx.x == 0 && w == 0 && lane == 0) tr.track = 4;
-  for (int item = blockIdx.x; ok && item < p.total_items; item += gridDim.x) {
-    const PairItem it = decode_pair(p, sm.segs(), item);
-    if (it.zero) continue;
-    for (int e = 0; e < it.nE; ++e, ++kv) {
-      const int vs = kv % C::kVSt, ts = kv % C::kTSt;
-      tr.ev(40);
-      if (!warp_wait(sm.v_full(vs), (kv / C::kVSt) & 1, abort, kRoleTranspose)) { ok = false; break; }
-      tr.ev(41);
-      if (!warp_wait(sm.vt_empty(ts), ((kv / C::kTSt) & 1) ^ 1, abort, kRoleTranspose)) { ok = false; break; }
-      tr.ev(42);
-      const uint32_t src = sm.v(vs), dst = sm.vt(ts) + w * (D * 128);
-#pragma unroll
-      for (int ki = 0; ki < 8; ++ki) {
-        const int key = 64 * w + 8 * ki + r;  // source row of this lane
-#pragma unroll
-        for (int dg = 0; dg < D / 32; ++dg) {
-          const int di = 4 * dg + m;  // 8-column group of D
-          uint32_t x0, x1, x2, x3;
-          ldmatrix_x4_trans(src + (di >> 3) * 16384 + key * 128 + (((di & 7) ^ (key & 7)) << 4), x0, x1, x2, x3);
-          const int dr = 8 * di + r;  // destination row (a column of V)
-          stmatrix_x4(dst + dr * 128 + ((ki ^ (dr & 7)) << 4), x0, x1, x2, x3);
-        }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(sm.v_empty(vs));
-        mbar_arrive(sm.vt_full(ts));
-      }
-      tr.ev(43);
-    }
-  }
-  tr.done();
-}
 
 // ------------------------------------------------------------------ softmax / epilogue
 // Lazy rescaling: the running maximum of a row is raised only when a new
@@ -894,8 +843,8 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
   }
 }
 
-// Three warpgroups: the MMA, producer and two transposer warps, then two of
-// softmax warps.  Launched at 168 registers per thread
+// Three warpgroups: the producer warps and two warps without a role, then
+// two of softmax warps.  Launched at 168 registers per thread
 // (384 x 168 = 64512 of the SM's 65536), the third warpgroup gives registers
 // back (setmaxnreg.dec to kRegsOther) and the softmax warpgroups take them
 // (setmaxnreg.inc to kRegsSoftmax): 256 x 200 + 128 x 96 = 63488 <= 64512.
@@ -928,9 +877,7 @@ __global__ void __launch_bounds__(kBandThreads, 1) band_tc_kernel(const __grid_c
     }
     for (int s = 0; s < 4; ++s) {
       mbar_init(sm.v_full(s), 1);
-      mbar_init(sm.v_empty(s), 2);   // both transposer warps
-      mbar_init(sm.vt_full(s), 2);   // both transposer warps
-      mbar_init(sm.vt_empty(s), 2);  // one arrival per tile
+      mbar_init(sm.v_empty(s), 2);   // one release per tile
     }
     mbar_init(sm.v_land(), 1);
     for (int X = 0; X < 2; ++X) {
@@ -966,9 +913,7 @@ __global__ void __launch_bounds__(kBandThreads, 1) band_tc_kernel(const __grid_c
       band_producer<D, true>(p, sm, lane);
     } else if (warp == 1) {
       band_producer<D, false>(p, sm, lane);
-    } else {
-      band_transposer<D>(p, sm, warp - 2, lane);
-    }
+    }  // warps 2-3: no role (P.V reads V as loaded)
   }
 
   tc_fence_before();
