@@ -189,3 +189,73 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(lf, "_lib", None)
     with pytest.raises(RuntimeError):
         lf.load()
+
+
+# ---------------------------------------------------------------- new entry points: refused on the host
+# (fake, 16-byte aligned pointers that are never dereferenced: each call must
+# fail its validation before it touches the device)
+_FAKE = [(0x100000 * (t + 1)) << 12 for t in range(16)]
+
+
+def _i32p(xs):
+    import ctypes
+    return (ctypes.c_int32 * max(len(xs), 1))(*xs)
+
+
+@pytest.mark.parametrize("K,n_out,H,d,status", [
+    (96, 3, 2, 64, 2),    # K not a multiple of 64
+    (128, 3, 2, 48, 2),   # d not a multiple of 32
+    (128, 1, 1, 96, 2),   # n_out*H*d = 96, not a multiple of 128
+    (128, 0, 2, 64, 1),   # no output
+    (0, 3, 2, 64, 1),     # K < 1
+])
+def test_projection_sizes_refused_on_host(lib, K, n_out, H, d, status):
+    st = lib.lf_proj_heads(_FAKE[0], _FAKE[1], None, _FAKE[2], 2, 100, K, n_out, H, d, None)
+    assert st == status, lib.lf_last_error_message().decode()
+
+
+def test_projection_misaligned_pointer_refused(lib):
+    assert lib.lf_proj_heads(_FAKE[0] + 8, _FAKE[1], None, _FAKE[2], 2, 100, 128, 3, 2, 64, None) == 1
+    assert "aligned" in lib.lf_last_error_message().decode()
+
+
+@pytest.mark.parametrize("d,km,status", [(96, 32, 2), (64, 33, 2), (64, 0, 2)])
+def test_memory_combine_sizes_refused_on_host(lib, d, km, status):
+    st = lib.lf_mem_combine(_FAKE[0], _FAKE[1], _FAKE[2], _FAKE[3], _FAKE[4], _FAKE[5], _FAKE[6],
+                            1, 2, 100, d, 1000, km, None)
+    assert st == status, lib.lf_last_error_message().decode()
+
+
+def test_memory_combine_out_overlapping_an_input_refused(lib):
+    # out == local is allowed (in place); out overlapping q is not
+    st = lib.lf_mem_combine(_FAKE[0], _FAKE[1], _FAKE[2], _FAKE[3], _FAKE[4], _FAKE[5], _FAKE[0] + 16,
+                            1, 2, 100, 64, 1000, 32, None)
+    assert st == 1
+    assert "overlaps" in lib.lf_last_error_message().decode()
+
+
+def _bwd_args(lib, d=64, w=8, G=0, gidx=None):
+    import ctypes
+    f = _FAKE
+    return [f[0], f[1], f[2], f[3] if G else None, f[4] if G else None, f[5] if G else None,
+            _i32p(gidx) if G else None, G, f[6], f[7], f[8], f[9], f[10] if G else None,
+            f[11] if G else None, f[12] if G else None, 1, 2, 64, d, w, _i32p([1, 2]), 0, None, None]
+
+
+def test_backward_refuses_bad_patterns_on_host(lib):
+    assert lib.lf_attn_bwd(*_bwd_args(lib, w=7)) == 1            # odd window
+    assert lib.lf_attn_bwd(*_bwd_args(lib, d=96)) == 2           # bf16 d = 96
+    assert lib.lf_attn_bwd(*_bwd_args(lib, G=2, gidx=[5, 5])) == 1  # global list not increasing
+    args = _bwd_args(lib)
+    args[9] = _FAKE[0]  # dk overlapping q
+    assert lib.lf_attn_bwd(*args) == 1
+    assert "overlaps" in lib.lf_last_error_message().decode()
+
+
+def test_varglobal_refuses_bad_offsets_on_host(lib):
+    f = _FAKE
+    # offsets must start at 0 and not decrease; a bad list in the last row is found first
+    for offs, gidx in (([1, 1, 2], [3, 4]), ([0, 2, 1], [3, 4]), ([0, 1, 3], [3, 9, 9])):
+        st = lib.lf_attn_fwd_varglobal(f[0], f[1], f[2], f[3], f[4], f[5], _i32p(offs), _i32p(gidx), f[6],
+                                       2, 2, 64, 64, 8, _i32p([1, 1]), 0, None, None)
+        assert st == 1, (offs, gidx)
