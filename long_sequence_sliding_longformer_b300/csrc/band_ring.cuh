@@ -27,10 +27,12 @@
 //              the softmax has written P, then S = Q K^T of entry g + kSBuf
 //              into the buffer that P.V read
 //   warp 1     Q/K producer: TMA loads of Q and of the K entries
-//   warp 2     V producer: TMA loads of the V entries (the global tokens'
-//              K/V rows are gathered by the producers with plain loads)
-//   warp 3     transposes each V entry into V^T, the K-major layout the P.V
-//              product reads at full rate
+//   warp 2     V producer: TMA loads of the V entries into a ring of four
+//              slots, each freed by the completion of the P.V that reads it
+//              (the global tokens' K/V rows are gathered by the producers
+//              with plain loads)
+//   warp 3     no role: the P.V products read V MN-major straight from its
+//              slot (the instruction descriptor's transpose bit)
 //   warps 4-7  softmax and epilogue: one query row per thread; S rows are read
 //              from TMEM, masked, turned into P = exp2(S*scale - m) with a
 //              lazily updated row maximum, and P (bf16) is written back over
@@ -67,24 +69,22 @@ struct BandCfg {
   static constexpr int kCtaPerSm = kWide ? 1 : 2;
   static constexpr int kQBuf = 2;                  // Q tiles (the next item's Q loads early)
   static constexpr int kKSt = (D == 64) ? 3 : 2;   // K slots
-  static constexpr int kVSt = (D == 64) ? (kWide ? 3 : 2) : 1;  // V slots (as loaded: [keys, D])
-  static constexpr int kTSt = (D == 64) ? 4 : 2;   // V^T slots ([D, keys], the P.V operand)
+  static constexpr int kVSt = (D == 64) ? 4 : 1;   // V slots (as loaded: [keys, D]; the P.V operand)
   static constexpr int kSBuf = 3;                  // S buffers in TMEM
   static constexpr int kTileQ = 128 * D * 2;       // bytes of one [128, D] bf16 query tile
   static constexpr int kTile = kE * D * 2;         // bytes of one [kE, D] key/value tile
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBuf * kTileQ;
   static constexpr int kOffV = kOffK + kKSt * kTile;
-  static constexpr int kOffVT = kOffV + kVSt * kTile;
-  static constexpr int kOffBar = kOffVT + kTSt * kTile;
-  // q_full[2], q_empty[2], k_full[4], (unused)[4], v_full[4], v_empty[4],
-  // vt_full[4], pv_done[4], v_land, s_full[3], p_full[3], (unused), o_empty, fin
+  static constexpr int kOffBar = kOffV + kVSt * kTile;
+  // q_full[2], q_empty[2], k_full[4], (unused)[4], v_full[4], (unused)[8],
+  // pv_done[4], v_land, s_full[3], p_full[3], (unused), o_empty, fin
   static constexpr int kNumBar = 2 + 2 + 4 * 6 + 1 + 3 + 3 + 1 + 1 + 1;
-  static_assert(kKSt <= 4 && kVSt <= 4 && kTSt <= 4 && kQBuf <= 2 && kSBuf <= 3, "barrier arrays");
-  // A K slot is free once the S product that read it is done, and a V^T slot
+  static_assert(kKSt <= 4 && kVSt <= 4 && kQBuf <= 2 && kSBuf <= 3, "barrier arrays");
+  // A K slot is free once the S product that read it is done, and a V slot
   // once its P.V product is done: the S and P.V completions are those of the
-  // K and V^T slots only while the rings are as deep as s_full and pv_done.
-  static_assert(D != 64 || (kKSt == kSBuf && kTSt == 4), "K ring = S buffers, V^T ring = pv_done barriers");
+  // K and V slots only while the rings are as deep as s_full and pv_done.
+  static_assert(D != 64 || (kKSt == kSBuf && kVSt == 4), "K ring = S buffers, V ring = pv_done barriers");
   static constexpr int kOffMisc = kOffBar + kNumBar * 8;
   // after the barriers: TMEM address and abort flag (16 bytes), the segment
   // table, the batch rows' padding and the first kGSmem global positions
@@ -205,7 +205,6 @@ struct BandSmem {
   __device__ __forceinline__ uint32_t q(int qb) const { return sbase + C::kOffQ + qb * C::kTileQ; }
   __device__ __forceinline__ uint32_t k(int s) const { return sbase + C::kOffK + s * C::kTile; }
   __device__ __forceinline__ uint32_t v(int s) const { return sbase + C::kOffV + s * C::kTile; }
-  __device__ __forceinline__ uint32_t vt(int s) const { return sbase + C::kOffVT + s * C::kTile; }
   __device__ __forceinline__ uint8_t* k_ptr(int s) const { return base + C::kOffK + s * C::kTile; }
   __device__ __forceinline__ uint8_t* v_ptr(int s) const { return base + C::kOffV + s * C::kTile; }
   __device__ __forceinline__ uint32_t bar(int i) const { return sbase + C::kOffBar + 8 * i; }
@@ -213,15 +212,13 @@ struct BandSmem {
   __device__ __forceinline__ uint32_t q_empty(int b) const { return bar(2 + b); }
   __device__ __forceinline__ uint32_t k_full(int s) const { return bar(4 + s); }
   __device__ __forceinline__ uint32_t v_full(int s) const { return bar(12 + s); }
-  __device__ __forceinline__ uint32_t v_empty(int s) const { return bar(16 + s); }
-  __device__ __forceinline__ uint32_t vt_full(int s) const { return bar(20 + s); }
   __device__ __forceinline__ uint32_t v_land() const { return bar(28); }
   __device__ __forceinline__ uint32_t s_full(int b) const { return bar(29 + b); }
   __device__ __forceinline__ uint32_t p_full(int b) const { return bar(32 + b); }
   // Completion of the P.V of entry k arrives on pv_done(k & 3); it also frees
-  // V^T slot k % 4.  The softmax waits only for the completions it needs (the
+  // V slot k % 4.  The softmax waits only for the completions it needs (the
   // previous entry's before it rescales O, the last one before the epilogue);
-  // the transposer waits for the one four entries back.  A waiter for entry k
+  // the V producer waits for the one four entries back.  A waiter for entry k
   // knows that the P.V of entry k - 4 is done and that of k + 4 cannot be, so
   // the barrier is in the phase of entry k.
   __device__ __forceinline__ uint32_t pv_done(uint32_t k) const { return bar(24 + (k & 3)); }
@@ -251,7 +248,7 @@ __device__ __forceinline__ int residue_coord(int g, int r, int delta) {
 
 // ------------------------------------------------------------------ producers
 // kIsV = false loads Q and the K entries, kIsV = true the V entries, so that a
-// full V ring (waiting for the transposer) never holds back a K.
+// full V ring (waiting for the P.V products) never holds back a K.
 template <int D, bool kIsV, bool kG>
 __device__ void band_producer(const BandParams& p, const BandSmem<D>& sm, int lane) {
   using C = BandCfg<D>;
@@ -322,8 +319,9 @@ __device__ void band_producer(const BandParams& p, const BandSmem<D>& sm, int la
       if (!kIsV && q_it == n_act && q_have && !q_issue(false)) { ok = false; break; }  // the next item's Q
       const int slot = kv % kSt;
       const uint32_t full = kIsV ? sm.v_full(slot) : sm.k_full(slot);
-      // a K slot is free when the S product of the entry kKSt back (same S buffer) is done
-      const uint32_t empty = kIsV ? sm.v_empty(slot) : sm.s_full(slot);
+      // a K slot is free when the S product of the entry kKSt back (same S buffer)
+      // is done, a V slot when the P.V product of the entry kVSt back is
+      const uint32_t empty = kIsV ? sm.pv_done(kv) : sm.s_full(slot);
       const uint32_t dst = kIsV ? sm.v(slot) : sm.k(slot);
       uint8_t* dst_ptr = kIsV ? sm.v_ptr(slot) : sm.k_ptr(slot);
       // A global entry is gathered row by row with plain loads; the first
@@ -418,64 +416,6 @@ __device__ void band_producer(const BandParams& p, const BandSmem<D>& sm, int la
   if (land_pending >= 0) mbar_wait(sm.v_land(), (uint32_t)land_pending & 1, &dummy, kRoleDrain, kDrainLimitNs);
 }
 
-// ------------------------------------------------------------------ V transposer (one warp)
-// The P.V product takes V as a K-major operand (keys contiguous), which the
-// tensor cores read at full rate from a [D, keys] layout.  TMA delivers V as
-// [keys, D]; the warp moves every entry into 8x8 blocks of V^T with
-// ldmatrix.trans / stmatrix, both sides 128-byte swizzled: V^T is kE/64
-// blocks of 64 keys, each [D rows, 128 bytes].
-template <int D, bool kG>
-__device__ void band_transposer(const BandParams& p, const BandSmem<D>& sm, int lane) {
-  using C = BandCfg<D>;
-  volatile int* abort = sm.abort_flag();
-  uint32_t kv = 0;
-  bool ok = true;
-  const int m = lane >> 3, r = lane & 7;  // this lane addresses row r of matrix m
-  Tracer tr;
-  if (blockIdx.x == 0 && lane == 0) tr.track = 4;
-  Prof pf;
-  for (int item = blockIdx.x; ok && item < p.total_items; item += gridDim.x) {
-    const TileItem it = decode_tile<C::kE, kG>(p, sm.tables(), item);
-    if (!it.act) continue;
-    for (int e = 0; e < it.nE; ++e, ++kv) {
-      const int vs = kv % C::kVSt, ts = kv % C::kTSt;
-      tr.ev(40);
-      pf.lap(0);
-      if (!warp_wait(sm.v_full(vs), (kv / C::kVSt) & 1, abort, kRoleTranspose)) { ok = false; break; }
-      pf.lap(1);
-      // V^T slot ts is free once the P.V of entry kv - kTSt is done
-      if (!warp_wait(sm.pv_done(kv), ((kv / C::kTSt) & 1) ^ 1, abort, kRoleTranspose)) { ok = false; break; }
-      tr.ev(41);
-      pf.lap(2);
-      const uint32_t src = sm.v(vs), dst = sm.vt(ts);
-#pragma unroll 2
-      for (int ki = 0; ki < C::kE / 8; ++ki) {  // 8-key groups
-        const int key = 8 * ki + r;              // source row of this lane
-        const uint32_t dblk = dst + (ki >> 3) * (D * 128);
-#pragma unroll
-        for (int dg = 0; dg < D / 32; ++dg) {
-          const int di = 4 * dg + m;  // 8-column group of D
-          uint32_t x0, x1, x2, x3;
-          ldmatrix_x4_trans(src + (di >> 3) * (C::kE * 128) + key * 128 + (((di & 7) ^ (key & 7)) << 4), x0, x1, x2, x3);
-          const int dr = 8 * di + r;  // destination row (a column of V)
-          stmatrix_x4(dblk + dr * 128 + (((ki & 7) ^ (dr & 7)) << 4), x0, x1, x2, x3);
-        }
-      }
-      pf.lap(3);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(sm.v_empty(vs));
-        mbar_arrive(sm.vt_full(ts));
-      }
-      tr.ev(43);
-      pf.lap(4);
-    }
-  }
-  tr.done();
-  pf.flush(5, lane == 0);
-}
-
 // ------------------------------------------------------------------ MMA issuer (one warp)
 // Walks the same sequence of entries as the softmax warps.  Two cursors: one
 // for the S products, running up to kSBuf entries ahead, and one for the
@@ -526,14 +466,14 @@ __device__ __forceinline__ void cursor_next(const BandParams& p, const Tables& t
 template <int D, bool kG>
 __device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tmem) {
   using C = BandCfg<D>;
-  constexpr uint32_t kTile16 = C::kTile >> 4;    // a K / V^T slot, in descriptor address units
+  constexpr uint32_t kTile16 = C::kTile >> 4;    // a K / V slot, in descriptor address units
   constexpr uint32_t kTileQ16 = C::kTileQ >> 4;  // a Q tile
   volatile int* abort = sm.abort_flag();
   const uint32_t idesc_sband = idesc_bf16_f32(128, C::kE, 0);
-  const uint32_t idesc_pv = idesc_bf16_f32(128, D, 0);  // V^T: K-major
+  const uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);  // V as loaded: MN-major (D contiguous)
   const uint64_t qdesc0 = smem_desc_sw128(sm.q(0), 16, 1024);
   const uint64_t kdesc0 = smem_desc_sw128(sm.k(0), 16, 1024);
-  const uint64_t vdesc0 = smem_desc_sw128(sm.vt(0), 16, 1024);
+  const uint64_t vdesc0 = smem_desc_sw128(sm.v(0), 16, 1024);
   const uint32_t ot = tmem + C::kColO;
   const Tables tb = sm.tables();
   uint32_t o_cnt = 0;
@@ -580,25 +520,25 @@ __device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tm
   auto mma_pv = [&]() {
     const TileItem& it = cp.it;
     const uint32_t f = cp.kv + cp.e;
-    const int ts = f % C::kTSt;
+    const int vs = f % C::kVSt;
     const uint32_t buf = cp.g % C::kSBuf;
     const int ksteps = (cp.e < it.nU) ? C::kE / 16 : ((global_count<C::kE>(it, cp.e) + 15) >> 4);
     const uint32_t pt = tmem + C::kE * buf;  // P over the first kE/2 columns of the buffer
-    const uint64_t vd = vdesc0 + ts * kTile16;
+    const uint64_t vd = vdesc0 + vs * kTile16;
     const uint32_t acc0 = cp.e > 0 ? 1u : 0u;
     if (ksteps == C::kE / 16) {
 #pragma unroll
       for (int kk = 0; kk < C::kE / 16; ++kk) {
-        const uint32_t off = ((kk >> 2) * (D * 128) + (kk & 3) * 32) >> 4;
+        const uint32_t off = (kk * 16 * 128) >> 4;  // 16 value rows of 128 bytes
         mma_bf16_ts_w(ot, pt + kk * 8, vd + off, idesc_pv, kk > 0 ? 1u : acc0);
       }
     } else {
       for (int kk = 0; kk < ksteps; ++kk) {
-        const uint32_t off = ((kk >> 2) * (D * 128) + (kk & 3) * 32) >> 4;
+        const uint32_t off = (kk * 16 * 128) >> 4;
         mma_bf16_ts_w(ot, pt + kk * 8, vd + off, idesc_pv, kk > 0 ? 1u : acc0);
       }
     }
-    mma_commit_w(sm.pv_done(cp.g));  // also frees V^T slot ts
+    mma_commit_w(sm.pv_done(cp.g));  // also frees V slot vs
   };
 
   // the first kSBuf S products
@@ -621,7 +561,7 @@ __device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tm
     const int qb = cs.n_items % C::kQBuf;
     // (tests are reads: the ones not needed this time are made anyway and
     // ignored, so that all five are in flight together)
-    const bool r_vt = mbar_test_wait(sm.vt_full(fp % C::kTSt), (fp / C::kTSt) & 1);
+    const bool r_vt = mbar_test_wait(sm.v_full(fp % C::kVSt), (fp / C::kVSt) & 1);
     const bool r_p = mbar_test_wait(sm.p_full(cp.g % C::kSBuf), (cp.g / C::kSBuf) & 1);
     const bool r_o = mbar_test_wait(sm.o_empty(), (o_cnt & 1) ^ 1);
     const bool r_k = mbar_test_wait(sm.k_full(fs % C::kKSt), (fs / C::kKSt) & 1);
@@ -636,7 +576,7 @@ __device__ void band_mma(const BandParams& p, const BandSmem<D>& sm, uint32_t tm
     } else {
       // the P.V goes as soon as its own inputs are there (the epilogue of
       // an item waits for its last P.V), then the S
-      ok = warp_wait(sm.vt_full(fp % C::kTSt), (fp / C::kTSt) & 1, abort, kRoleMma) &&
+      ok = warp_wait(sm.v_full(fp % C::kVSt), (fp / C::kVSt) & 1, abort, kRoleMma) &&
            warp_wait(sm.p_full(cp.g % C::kSBuf), (cp.g / C::kSBuf) & 1, abort, kRoleMma);
       // O is overwritten by the first P.V of an item: the previous item's epilogue must have read it
       if (ok && cp.e == 0) ok = warp_wait(sm.o_empty(), (o_cnt & 1) ^ 1, abort, kRoleMma);
@@ -1016,8 +956,6 @@ __global__ void __launch_bounds__(kBandThreads, BandCfg<D>::kCtaPerSm)
     for (int s = 0; s < 4; ++s) {
       mbar_init(sm.k_full(s), 1);
       mbar_init(sm.v_full(s), 1);
-      mbar_init(sm.v_empty(s), 1);
-      mbar_init(sm.vt_full(s), 1);
       mbar_init(sm.pv_done(s), 1);
     }
     mbar_init(sm.v_land(), 1);
@@ -1052,9 +990,7 @@ __global__ void __launch_bounds__(kBandThreads, BandCfg<D>::kCtaPerSm)
     band_producer<D, false, kG>(p, sm, lane);
   } else if (warp == 2) {
     band_producer<D, true, kG>(p, sm, lane);
-  } else {
-    band_transposer<D, kG>(p, sm, lane);
-  }
+  }  // warp 3: no role (the P.V products read V as loaded)
 
   tc_fence_before();
   __syncthreads();
