@@ -419,14 +419,15 @@ static lf_status run_global_band_bf16(const Problem& P, int b0, int nbat, BandPa
 // items are its 128-row tiles (D = 64) or pairs of them (D = 128).  Segments are generated in order straight
 // into the parameter block `p` (no heap use), one launch per kMaxSeg segments
 // or kMaxSets (dilation, residue) tensor-map sets.
-// For D = 64 the choice is measured (whole calls, one B300, L2 flushed):
-// with global tokens and a two-sided window the duo kernel is 3-22% faster
-// (it gathers the global key columns once per 256 rows instead of once per
-// 128); without global tokens, or with a one-sided (causal) window, the ring
-// kernel is 8-35% faster.
+// For D = 64 the choice is measured (whole calls, one B300, L2 flushed,
+// both kernels reading V as loaded): with 16 or more global tokens and a
+// two-sided window the duo kernel is 8-13% faster (it gathers the global key
+// columns once per 256 rows instead of once per 128); with fewer global
+// tokens the two are within 4% of each other and the ring kernel is taken;
+// with a one-sided (causal) window the ring kernel is 21-28% faster.
 static BandKernel band_kernel_for(const Problem& P) {
   if (P.d == 128) return BandKernel::pair;
-  return (P.G > 0 && !P.causal) ? BandKernel::duo : BandKernel::ring;
+  return (P.G >= 16 && !P.causal) ? BandKernel::duo : BandKernel::ring;
 }
 
 static lf_status run_band_bf16(const Problem& P, int b0, int nbat, BandParams& p) {

@@ -83,7 +83,8 @@ def test_batch_beyond_one_launch_padded_causal():
 @pytest.mark.parametrize("wl,kernel", [
     (workloads.custom("to_ring", "bf16", 1, 4, 2048, 64, 128, (1, 1, 2, 4), False, (), None, seed=23),
      "band_ring"),
-    (workloads.custom("to_duo", "bf16", 1, 4, 2048, 64, 128, (1,) * 4, False, (0,), None, seed=24),
+    (workloads.custom("to_duo", "bf16", 1, 4, 2048, 64, 128, (1,) * 4, False, tuple(range(0, 1600, 100)), None,
+                      seed=24),
      "band_duo"),
     (workloads.custom("to_pair", "bf16", 1, 2, 2048, 128, 256, (1, 1), False, (), None, seed=25),
      "band_pair"),
