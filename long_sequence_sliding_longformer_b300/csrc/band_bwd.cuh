@@ -12,11 +12,11 @@
 //
 // Five kernels, in stream order, fixed summation orders and no atomics
 // (bitwise reproducible):
-//   rows_tiled   per 64 consecutive rows of one residue class: their
-//                statistics (log2-sum-exp of the scaled scores and D_row, one
-//                sweep over the tile's keys with an online maximum) and dq (a
-//                second sweep), over 32-key chunks of the band and of the
-//                global columns staged in shared memory
+//   rows_tiled   per 64 consecutive rows of one residue class, one sweep
+//                over 32-key chunks of the band and of the global columns
+//                staged in shared memory, with an online row maximum: the
+//                rows' statistics (log2-sum-exp of the scaled scores and
+//                D_row) and dq = scale (sum e dp k - D_row sum e k) / sum e
 //   grows        per global token's row (one CTA, 8 warps over its keys):
 //                its statistics and dqg
 //   keys_tiled   per 64 consecutive keys of one residue class: dk, dv from
@@ -176,7 +176,7 @@ __device__ __forceinline__ void dot_block(const float* a1, const float* b1, cons
 // Shared-memory bytes of the tiled kernels (fp32 operand tiles, row stride D + 4).
 template <int D>
 constexpr int rows_smem_bytes() {
-  return (2 * kTR + 2 * kKC) * (D + 4) * 4 + kTR * (kKC + 1) * 4 + 4 * kTR * 4;
+  return (2 * kTR + 2 * kKC) * (D + 4) * 4 + 2 * kTR * (kKC + 1) * 4 + 4 * kTR * 4;
 }
 template <int D>
 constexpr int keys_smem_bytes() {
@@ -186,9 +186,11 @@ constexpr int keys_smem_bytes() {
 // ---------------------------------------------------------------- rows_tiled
 // 64 class rows [m0, m0 + 64): thread (ty, tx) = (tid / 16, tid % 16) holds
 // rows 4ty..4ty+3 and keys tx, tx + 16 of every 32-key chunk; for dq it owns
-// rows 4ty..4ty+3 and columns [tx * D/16, (tx + 1) * D/16).
+// rows 4ty..4ty+3 and columns [tx * D/16, (tx + 1) * D/16).  At d = 128 the
+// accumulators need more than half the register file per thread: one CTA
+// per SM.
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) bwd_rows_tiled(BwdParams p, const T* __restrict__ q,
+__global__ void __launch_bounds__(kThreads, D == 128 ? 1 : 2) bwd_rows_tiled(BwdParams p, const T* __restrict__ q,
                                                           const T* __restrict__ k, const T* __restrict__ v,
                                                           const T* __restrict__ dout, float* __restrict__ dq,
                                                           float2* __restrict__ stats) {
@@ -198,8 +200,8 @@ __global__ void __launch_bounds__(kThreads) bwd_rows_tiled(BwdParams p, const T*
   float* Ds = Qs + kTR * SD;      // dout rows [64][SD]
   float* Ks = Ds + kTR * SD;      // [32][SD]
   float* Vs = Ks + kKC * SD;      // [32][SD]
-  float* dS = Vs + kKC * SD;      // [64][33]
-  float* rl = dS + kTR * (kKC + 1);  // per row: log2-sum-exp
+  float* dS = Vs + kKC * SD;      // [64][33]: e dp of the chunk
+  float* rl = dS + 2 * kTR * (kKC + 1);  // (e of the chunk in the [64][33] before rl)
   float* rD = rl + kTR;              // per row: D
   int* rpos = reinterpret_cast<int*>(rD + kTR);  // per row: position, -1 if not an ordinary valid row
   int* rzero = rpos + kTR;                      // per row: position whose dq row is written as zeros, or -1
@@ -255,84 +257,64 @@ __global__ void __launch_bounds__(kThreads) bwd_rows_tiled(BwdParams p, const T*
     return j < t.L && (!p.causal || j <= i) && !in_band(p, i, j, t.delta);
   };
 
+  // One sweep over the chunks with a running row maximum mx (shared by the 16
+  // threads of a row group): e = 2^(s - mx), ls = sum e, as = sum e dp, and
+  // the dq accumulators A = sum (e dp) k and Bk = sum e k, rescaled when mx
+  // rises; at the end D = as / ls and dq = scale (A - D Bk) / ls.
   float mx[4], ls[4], as[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     mx[i] = -INFINITY;
     ls[i] = as[i] = 0.f;
   }
-  float s[4][2], dp[4][2];
-  // ---- sweep 1: statistics
-  for (int c = 0; c < nchunks; ++c) {
-    __syncthreads();  // the previous chunk's K/V are no longer read
-    stage_rows<T, D, kKC>(Ks, kb, d, [&](int kk) { return key_at(c, kk); });
-    stage_rows<T, D, kKC>(Vs, vb, d, [&](int kk) { return key_at(c, kk); });
-    __syncthreads();
-    dot_block<D>(Qs, Ks, Ds, Vs, 4 * ty, tx, tx + 16, s, dp);
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int key = key_at(c, tx + 16 * j);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (!attends(4 * ty + i, c, key)) continue;
-        const float s2 = s[i][j] * p.sl2;
-        if (s2 > mx[i]) {
-          const float f = exp2f(mx[i] - s2);  // 0 while mx is -inf
-          ls[i] *= f;
-          as[i] *= f;
-          mx[i] = s2;
-        }
-        const float e = exp2f(s2 - mx[i]);
-        ls[i] += e;
-        as[i] = fmaf(e, dp[i][j], as[i]);
-      }
-    }
-  }
-  // combine over the 16 threads of a row group (lanes of one half warp)
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float M = mx[i];
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    const float f = (mx[i] == -INFINITY) ? 0.f : exp2f(mx[i] - M);
-    float l = ls[i] * f, a = as[i] * f;
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) {
-      l += __shfl_xor_sync(0xffffffffu, l, o);
-      a += __shfl_xor_sync(0xffffffffu, a, o);
-    }
-    if (tx == 0) {
-      const int row = 4 * ty + i;
-      const bool ok = rpos[row] >= 0 && l > 0.f;
-      rl[row] = ok ? M + log2f(l) : INFINITY;  // +inf: p = 0 for a row that is not computed
-      rD[row] = ok ? a / l : 0.f;
-    }
-  }
-  __syncthreads();
-  if (tid < kTR && rpos[tid] >= 0)
-    stats[((int64_t)t.b * p.H + t.h) * p.n + rpos[tid]] = make_float2(rl[tid], rD[tid]);
-
-  // ---- sweep 2: ds into shared memory, then dq += ds K
-  float acc[4][CPT];
+  float accA[4][CPT], accB[4][CPT];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int cc = 0; cc < CPT; ++cc) acc[i][cc] = 0.f;
+    for (int cc = 0; cc < CPT; ++cc) accA[i][cc] = accB[i][cc] = 0.f;
+  float* Es = rl - kTR * (kKC + 1);  // e of the chunk [64][33] (just below rl)
+  float s[4][2], dp[4][2];
   for (int c = 0; c < nchunks; ++c) {
-    __syncthreads();
+    __syncthreads();  // the previous chunk's K, V, e and e dp are no longer read
     stage_rows<T, D, kKC>(Ks, kb, d, [&](int kk) { return key_at(c, kk); });
     stage_rows<T, D, kKC>(Vs, vb, d, [&](int kk) { return key_at(c, kk); });
     __syncthreads();
     dot_block<D>(Qs, Ks, Ds, Vs, 4 * ty, tx, tx + 16, s, dp);
+    bool att[4][2];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int key = key_at(c, tx + 16 * j);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int row = 4 * ty + i;
-        float x = 0.f;
-        if (attends(row, c, key)) x = exp2f(s[i][j] * p.sl2 - rl[row]) * (dp[i][j] - rD[row]);
-        dS[row * (kKC + 1) + tx + 16 * j] = x;
+      for (int i = 0; i < 4; ++i) att[i][j] = attends(4 * ty + i, c, key);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float cm = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+        if (att[i][j]) cm = fmaxf(cm, s[i][j] * p.sl2);
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+      if (cm > mx[i]) {
+        const float f = exp2f(mx[i] - cm);  // 0 while mx is -inf
+        ls[i] *= f;
+        as[i] *= f;
+#pragma unroll
+        for (int cc = 0; cc < CPT; ++cc) {
+          accA[i][cc] *= f;
+          accB[i][cc] *= f;
+        }
+        mx[i] = cm;
+      }
+      const int row = 4 * ty + i;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float e = 0.f;
+        if (att[i][j]) e = exp2f(s[i][j] * p.sl2 - mx[i]);
+        ls[i] += e;
+        as[i] = fmaf(e, dp[i][j], as[i]);
+        Es[row * (kKC + 1) + tx + 16 * j] = e;
+        dS[row * (kKC + 1) + tx + 16 * j] = e * dp[i][j];
       }
     }
     __syncthreads();
@@ -343,11 +325,32 @@ __global__ void __launch_bounds__(kThreads) bwd_rows_tiled(BwdParams p, const T*
       for (int cc = 0; cc < CPT; ++cc) kv[cc] = Ks[kk * SD + tx * CPT + cc];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float x = dS[(4 * ty + i) * (kKC + 1) + kk];
+        const float xe = Es[(4 * ty + i) * (kKC + 1) + kk];
+        const float xd = dS[(4 * ty + i) * (kKC + 1) + kk];
 #pragma unroll
-        for (int cc = 0; cc < CPT; ++cc) acc[i][cc] = fmaf(x, kv[cc], acc[i][cc]);
+        for (int cc = 0; cc < CPT; ++cc) {
+          accB[i][cc] = fmaf(xe, kv[cc], accB[i][cc]);
+          accA[i][cc] = fmaf(xd, kv[cc], accA[i][cc]);
+        }
       }
     }
+  }
+  // the row group's totals (the 16 threads share mx)
+  float acc[4][CPT];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float l = ls[i], a = as[i];
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) {
+      l += __shfl_xor_sync(0xffffffffu, l, o);
+      a += __shfl_xor_sync(0xffffffffu, a, o);
+    }
+    const int row = 4 * ty + i;
+    const bool ok = rpos[row] >= 0 && l > 0.f;
+    const float Drow = ok ? a / l : 0.f, inv = ok ? 1.f / l : 0.f;
+    if (tx == 0 && ok) stats[((int64_t)t.b * p.H + t.h) * p.n + rpos[row]] = make_float2(mx[i] + log2f(l), Drow);
+#pragma unroll
+    for (int cc = 0; cc < CPT; ++cc) acc[i][cc] = (accA[i][cc] - Drow * accB[i][cc]) * inv;
   }
   // write dq rows (zeros at padding and global tokens' positions)
 #pragma unroll
