@@ -399,7 +399,7 @@ __device__ __forceinline__ float dot_row(const T* row, const float* sv, int d) {
 // tx + 16 of every 32-row chunk; for the accumulation keys 4ty..4ty+3 and
 // columns [tx * D/16, (tx + 1) * D/16).
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) bwd_keys_tiled(BwdParams p, const T* __restrict__ q,
+__global__ void __launch_bounds__(kThreads, D == 128 ? 1 : 2) bwd_keys_tiled(BwdParams p, const T* __restrict__ q,
                                                           const T* __restrict__ k, const T* __restrict__ v,
                                                           const T* __restrict__ dout, float* __restrict__ dk,
                                                           float* __restrict__ dv, const float2* __restrict__ stats) {
