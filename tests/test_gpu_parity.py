@@ -175,6 +175,22 @@ def test_bf16_more_globals_than_shared_memory_holds():
     check(wl, run(wl, inp), oracle.wl_fwd(wl, inp))
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("G,w", [(1, 64), (2, 64), (4, 64), (5, 64), (4, 2000), (3, 6)])
+def test_bf16_few_globals_on_ring(G, w, causal):
+    """d = 64 with one to five global tokens (the ring kernel's gathered key
+    entry holding a few columns).  The tokens sit at the start, inside, near
+    the end and in batch row 1's padding; dilated heads put some of them
+    outside a row's residue class, w = 2000 puts every one inside every band,
+    and causal rows before a token must not see it."""
+    gidx = (0, 301, 702, 850, 999)[:G]
+    wl = workloads.custom("fold", "bf16", 2, 3, 1000, 64, w, (1, 2, 3), causal, gidx, (0, 230), seed=40 + G)
+    inp = workloads.make_inputs(wl, "cuda")
+    out = run(wl, inp)
+    assert lf.last_band_kernel() == "band_ring"
+    check(wl, out, oracle.wl_fwd(wl, inp))
+
+
 def test_bf16_many_globals():
     wl = workloads.custom("glob", "bf16", 1, 2, 1500, 64, 32, (1, 2), False, tuple(range(0, 1500, 5)),
                           (0,), seed=4)
