@@ -173,6 +173,43 @@ lf_status lf_attn_bwd_f32(const void* q, const void* k, const void* v,
                           const int32_t* pad_len, cudaStream_t stream);
 
 /*
+ * Per-head windows (velog.io/@lainshower/Longformer, section 4.1: the window
+ * size is chosen per layer, and within a layer heads differ, some dilated and
+ * some not): as lf_attn_fwd / lf_attn_fwd_f32 / lf_attn_bwd / lf_attn_bwd_f32,
+ * with head h using the window w_heads[h] (even, >= 0) in place of the one w.
+ * w_heads: host array of H values, read during the call, NULL only if H == 0.
+ * Heads sharing a window run in one set of launches (bf16: one launch per
+ * distinct window, each holding the tiles of its heads only).  Errors as in
+ * the calls they extend; a bad w_heads entry is LF_ERR_INVALID_ARG.
+ */
+lf_status lf_attn_fwd_hw(const void* q, const void* k, const void* v,
+                         const void* qg, const void* kg, const void* vg,
+                         const int32_t* global_idx, int32_t n_global, void* out,
+                         int32_t B, int32_t H, int32_t n, int32_t d,
+                         const int32_t* w_heads, const int32_t* dilation, int32_t causal,
+                         const int32_t* pad_len, cudaStream_t stream);
+lf_status lf_attn_fwd_hw_f32(const void* q, const void* k, const void* v,
+                             const void* qg, const void* kg, const void* vg,
+                             const int32_t* global_idx, int32_t n_global, void* out,
+                             int32_t B, int32_t H, int32_t n, int32_t d,
+                             const int32_t* w_heads, const int32_t* dilation, int32_t causal,
+                             const int32_t* pad_len, cudaStream_t stream);
+lf_status lf_attn_bwd_hw(const void* q, const void* k, const void* v,
+                         const void* qg, const void* kg, const void* vg,
+                         const int32_t* global_idx, int32_t n_global, const void* dout,
+                         float* dq, float* dk, float* dv, float* dqg, float* dkg, float* dvg,
+                         int32_t B, int32_t H, int32_t n, int32_t d,
+                         const int32_t* w_heads, const int32_t* dilation, int32_t causal,
+                         const int32_t* pad_len, cudaStream_t stream);
+lf_status lf_attn_bwd_hw_f32(const void* q, const void* k, const void* v,
+                             const void* qg, const void* kg, const void* vg,
+                             const int32_t* global_idx, int32_t n_global, const void* dout,
+                             float* dq, float* dk, float* dv, float* dqg, float* dkg, float* dvg,
+                             int32_t B, int32_t H, int32_t n, int32_t d,
+                             const int32_t* w_heads, const int32_t* dilation, int32_t causal,
+                             const int32_t* pad_len, cudaStream_t stream);
+
+/*
  * Per-head linear projections of hidden states (section 3-1, "Linear
  * Projections for Global Attention": the band and the global attention each
  * use their own W_q, W_k, W_v), producing the inputs of lf_attn_fwd:

@@ -55,6 +55,12 @@ def load():
         fn = getattr(lib, name)
         fn.argtypes = bwd_args
         fn.restype = ctypes.c_int
+    # per-head windows: the w argument becomes a host array
+    for name, args, at in (("lf_attn_fwd_hw", fwd_args, 13), ("lf_attn_fwd_hw_f32", fwd_args, 13),
+                           ("lf_attn_bwd_hw", bwd_args, 19), ("lf_attn_bwd_hw_f32", bwd_args, 19)):
+        fn = getattr(lib, name)
+        fn.argtypes = args[:at] + [P] + args[at + 1:]
+        fn.restype = ctypes.c_int
     lib.lf_proj_heads.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, P]
     lib.lf_proj_heads.restype = ctypes.c_int
     lib.lf_mem_combine.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P]
@@ -97,13 +103,25 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
-def attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, w: int,
+def _window(w, H: int):
+    """w as one int (every head) or one int per head: (the call's w
+    argument, whether it is the per-head array)."""
+    if isinstance(w, int) or (torch.is_tensor(w) and w.dim() == 0) or hasattr(w, "__index__"):
+        return int(w), False
+    ws = [int(x) for x in w]
+    if len(ws) != H:
+        raise ValueError("w needs one entry per head (or a single int)")
+    return _i32_array(ws), True
+
+
+def attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, w,
          dilation: Optional[Sequence[int]] = None, causal: bool = False,
          pad_len: Optional[Sequence[int]] = None, qg: Optional[torch.Tensor] = None,
          kg: Optional[torch.Tensor] = None, vg: Optional[torch.Tensor] = None,
          global_idx: Sequence[int] = (), out: Optional[torch.Tensor] = None,
          stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
-    """Sliding / dilated / causal window attention with global tokens."""
+    """Sliding / dilated / causal window attention with global tokens.  w is
+    the window of every head, or a sequence of one window per head."""
     lib = load()
     if q.dim() != 4:
         raise ValueError("q must be [B, H, n, d]")
@@ -134,11 +152,14 @@ def attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, w: int,
     if pad_len is not None and len(pad_len) != B:
         raise ValueError("pad_len needs one entry per batch row")
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
-    fn = lib.lf_attn_fwd if q.dtype == torch.bfloat16 else lib.lf_attn_fwd_f32
+    warg, per_head = _window(w, H)
+    bf = q.dtype == torch.bfloat16
+    fn = (lib.lf_attn_fwd_hw if bf else lib.lf_attn_fwd_hw_f32) if per_head else \
+        (lib.lf_attn_fwd if bf else lib.lf_attn_fwd_f32)
     with torch.cuda.device(q.device):
         _check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr(qg) if G else None,
                   _ptr(kg) if G else None, _ptr(vg) if G else None, gidx, G, out.data_ptr(),
-                  B, H, n, d, int(w), dil, int(bool(causal)), pads, s.cuda_stream))
+                  B, H, n, d, warg, dil, int(bool(causal)), pads, s.cuda_stream))
     return out
 
 
@@ -155,7 +176,7 @@ def count_pairs(*, B: int, H: int, n: int, d: int, w: int, dilation: Sequence[in
     return int(pairs.value), float(flops.value)
 
 
-def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dout: torch.Tensor, *, w: int,
+def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dout: torch.Tensor, *, w,
              dilation: Optional[Sequence[int]] = None, causal: bool = False,
              pad_len: Optional[Sequence[int]] = None, qg: Optional[torch.Tensor] = None,
              kg: Optional[torch.Tensor] = None, vg: Optional[torch.Tensor] = None,
@@ -199,13 +220,16 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dout: torch.Tens
     if pad_len is not None and len(pad_len) != B:
         raise ValueError("pad_len needs one entry per batch row")
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
-    fn = lib.lf_attn_bwd if q.dtype == torch.bfloat16 else lib.lf_attn_bwd_f32
+    warg, per_head = _window(w, H)
+    bf = q.dtype == torch.bfloat16
+    fn = (lib.lf_attn_bwd_hw if bf else lib.lf_attn_bwd_hw_f32) if per_head else \
+        (lib.lf_attn_bwd if bf else lib.lf_attn_bwd_f32)
     gp = lambda name: _ptr(g[name]) if name in g else None
     with torch.cuda.device(q.device):
         _check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr(qg) if G else None,
                   _ptr(kg) if G else None, _ptr(vg) if G else None, gidx, G, dout.data_ptr(),
                   gp("dq"), gp("dk"), gp("dv"), gp("dqg"), gp("dkg"), gp("dvg"),
-                  B, H, n, d, int(w), dil, int(bool(causal)), pads, s.cuda_stream))
+                  B, H, n, d, warg, dil, int(bool(causal)), pads, s.cuda_stream))
     return {name: g[name] for name in names}
 
 

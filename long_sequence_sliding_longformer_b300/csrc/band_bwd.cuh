@@ -44,13 +44,14 @@ constexpr int kWarps = 8;      // warp kernels: warps per CTA
 struct BwdParams {
   int32_t B, H, n, d;    // this launch's batch rows and heads; sequence, head size
   int32_t Htot, b0, h0;  // the launch's block within the [B, H] tensors
-  int32_t half, right, causal, G;
+  int32_t causal, G;
   float scale, sl2;      // 1/sqrt(d) and that times log2(e)
   int32_t tiles_b;       // tiles of 64 class positions per batch row (all heads, classes)
   int32_t head_tile_off[kMaxHeadsSimt + 1];
   int32_t pad[kMaxBatch];
   int32_t gidx[kMaxGlobal];
   int32_t dil[kMaxHeadsSimt];
+  int32_t half_h[kMaxHeadsSimt];  // window reach per head in class steps: back half_h, ahead causal ? 0 : half_h
 };
 
 __device__ __forceinline__ float ldf(const float* p) { return __ldg(p); }
@@ -68,18 +69,19 @@ __device__ __forceinline__ int grank(const BwdParams& p, int i) {
   return -1;
 }
 
-// Is key j in row i's band (same class, within the window)?
-__device__ __forceinline__ bool in_band(const BwdParams& p, int i, int j, int delta) {
+// Is key j in row i's band (same class, within head h's window)?
+__device__ __forceinline__ bool in_band(const BwdParams& p, int h, int i, int j, int delta) {
   const int off = j - i;
   if (off % delta != 0) return false;
   const int steps = off / delta;
-  return steps >= -p.half && steps <= p.right;
+  return steps >= -p.half_h[h] && steps <= (p.causal ? 0 : p.half_h[h]);
 }
 
 // One tile of a tiled kernel: batch row, head, residue class and the class
 // coordinates [m0, m0 + 64) it covers.
 struct Tile {
   int b, h, delta, r, n_r, m0, L;
+  int half, right;  // the head's window reach in class steps (back, ahead)
   int64_t bh;  // the (b, h) plane in the tensors
   int mlast;   // last class coordinate whose position is valid (< L), or -1
 };
@@ -96,6 +98,8 @@ __device__ __forceinline__ Tile tile_of(const BwdParams& p, int blk) {
   t.h = lo;
   local -= p.head_tile_off[lo];
   t.delta = p.dil[t.h];
+  t.half = p.half_h[t.h];
+  t.right = p.causal ? 0 : t.half;
   // classes r < rem hold q + 1 positions, the others q
   const int q = p.n / t.delta, rem = p.n % t.delta;
   const int c1 = (q + 1 + kTR - 1) / kTR, c0 = (q + kTR - 1) / kTR;
@@ -229,8 +233,8 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 1 : 2) bwd_rows_tiled(Bwd
   stage_rows<T, D, kTR>(Ds, db, d, [&](int a) { return rpos[a]; });
 
   // keys: band class coordinates [klo, khi], then the global list in chunks
-  const int klo = max(0, t.m0 - p.half);
-  const int khi = min(t.m0 + kTR - 1 + p.right, t.mlast);
+  const int klo = max(0, t.m0 - t.half);
+  const int khi = min(t.m0 + kTR - 1 + t.right, t.mlast);
   const int nband = khi >= klo ? (khi - klo + 1 + kKC - 1) / kKC : 0;
   const int nglob = (p.G + kKC - 1) / kKC;
   const int nchunks = nband + nglob;
@@ -252,9 +256,9 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 1 : 2) bwd_rows_tiled(Bwd
     if (i < 0 || j < 0) return false;
     if (c < nband) {
       const int off = (j - i) / t.delta;  // same class: exact
-      return off >= -p.half && off <= p.right;
+      return off >= -t.half && off <= t.right;
     }
-    return j < t.L && (!p.causal || j <= i) && !in_band(p, i, j, t.delta);
+    return j < t.L && (!p.causal || j <= i) && !in_band(p, t.h, i, j, t.delta);
   };
 
   // One sweep over the chunks with a running row maximum mx (shared by the 16
@@ -433,8 +437,8 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 1 : 2) bwd_keys_tiled(Bwd
   stage_rows<T, D, kTR>(Vs, vb, d, [&](int a) { return kpos[a]; });
 
   // rows whose band can hold a key of the tile: class coordinates [rlo, rhi]
-  const int rlo = max(0, t.m0 - p.right);
-  const int rhi = min(t.m0 + kTR - 1 + p.half, t.mlast);
+  const int rlo = max(0, t.m0 - t.right);
+  const int rhi = min(t.m0 + kTR - 1 + t.half, t.mlast);
   const int nchunks = rhi >= rlo ? (rhi - rlo + 1 + kKC - 1) / kKC : 0;
 
   float accv[4][CPT], acck[4][CPT];
@@ -472,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 1 : 2) bwd_keys_tiled(Bwd
         const int a = 4 * ty + a4;
         const int off = (t.m0 + a) - mr;  // key offset from the row, in class steps
         float pv = 0.f, ds = 0.f;
-        if (i >= 0 && kpos[a] >= 0 && off >= -p.half && off <= p.right) {
+        if (i >= 0 && kpos[a] >= 0 && off >= -t.half && off <= t.right) {
           pv = exp2f(s[a4][j] * p.sl2 - cl[rr]);
           ds = pv * (dp[a4][j] - cD[rr]);
         }
@@ -670,7 +674,7 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_gkeys(BwdParams p, const T* _
   for (int i0 = lo + warp * 32; i0 < L; i0 += kWarps * 32) {
     const int i = i0 + lane;
     float pr = 0.f, ds = 0.f;
-    bool use = i < L && !in_band(p, i, g, delta) && !(p.G > 0 && grank(p, i) >= 0);
+    bool use = i < L && !in_band(p, h, i, g, delta) && !(p.G > 0 && grank(p, i) >= 0);
     if (use) {
       const float2 sd = st[i];
       const int64_t orow = bh * p.n + i;

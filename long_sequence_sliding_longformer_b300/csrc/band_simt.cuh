@@ -64,9 +64,10 @@ band_simt_f32_kernel(const __grid_constant__ SimtParams sp, const float* __restr
   for (int c = lane; c < D; c += 32) qs[warp][c] = qrow[c];
   __syncwarp();
   const int delta = sp.dil[h];
+  const int half = sp.half_h[h], right = p.causal ? 0 : half;
   // window steps t with key j = i + delta*t inside [0, L)
-  const int tlo = max(-p.half, -(i / delta));
-  const int thi = min(p.right, (L - 1 - i) / delta);
+  const int tlo = max(-half, -(i / delta));
+  const int thi = min(right, (L - 1 - i) / delta);
   const float* kb = k + bh * (int64_t)p.n * D;
   const float* vb = v + bh * (int64_t)p.n * D;
   const float NEG_INF = -__int_as_float(0x7f800000);
@@ -119,7 +120,7 @@ band_simt_f32_kernel(const __grid_constant__ SimtParams sp, const float* __restr
       const int off = g - i;
       if (off % delta == 0) {
         const int st = off / delta;
-        if (st >= -p.half && st <= p.right) valid = false;
+        if (st >= -half && st <= right) valid = false;
       }
     }
     float s = NEG_INF;

@@ -137,7 +137,11 @@ struct Problem {
   const int32_t* pad;
   cudaStream_t stream;
   int elem;  // bytes per element
+  const int32_t* wh = nullptr;  // window per head (host), or nullptr: w for every head
 };
+
+// the window of head h
+static inline int32_t win_of(const Problem& P, int h) { return P.wh ? P.wh[h] : P.w; }
 
 static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   if (!a || !b || na == 0 || nb == 0) return false;
@@ -155,10 +159,16 @@ static lf_status validate_pattern(const Problem& P) {
     set_error("d must be >= 1 (got %d)", P.d);
     return LF_ERR_INVALID_ARG;
   }
-  if (P.w < 0 || (P.w & 1)) {
+  if (!P.wh && (P.w < 0 || (P.w & 1))) {
     set_error("w must be even and >= 0 (got %d)", P.w);
     return LF_ERR_INVALID_ARG;
   }
+  if (P.wh)
+    for (int h = 0; h < P.H; ++h)
+      if (P.wh[h] < 0 || (P.wh[h] & 1)) {
+        set_error("w_heads[%d] = %d must be even and >= 0", h, P.wh[h]);
+        return LF_ERR_INVALID_ARG;
+      }
   if (P.causal != 0 && P.causal != 1) {
     set_error("causal must be 0 or 1 (got %d)", P.causal);
     return LF_ERR_INVALID_ARG;
@@ -257,9 +267,6 @@ static void fill_pattern(PatternParams& pp, const Problem& P, int b0, int nb) {
   pp.H = P.H;
   pp.n = P.n;
   pp.d = P.d;
-  const int64_t half = std::min<int64_t>(P.w / 2, P.n);
-  pp.half = (int32_t)half;
-  pp.right = P.causal ? 0 : (int32_t)half;
   pp.causal = P.causal;
   pp.G = P.G;
   pp.scale = (float)(1.0 / std::sqrt((double)P.d));
@@ -430,11 +437,14 @@ static BandKernel band_kernel_for(const Problem& P) {
   return (P.G >= 16 && !P.causal) ? BandKernel::duo : BandKernel::ring;
 }
 
-static lf_status run_band_bf16(const Problem& P, int b0, int nbat, BandParams& p) {
+// The launches of the heads whose window is wv (every head when there is one
+// window): the segments of those heads only, a launch per kMaxSeg segments or
+// kMaxSets (dilation, residue) tensor-map sets.
+static lf_status run_band_bf16_window(const Problem& P, int b0, int nbat, int32_t wv, BandParams& p) {
   const BandKernel kind = band_kernel_for(P);
   // persistent CTAs: two per SM for the ring kernel, one for the others
   const int grid_cap = sm_count() * (kind == BandKernel::ring ? ringk::BandCfg<64>::kCtaPerSm : 1);
-  const int64_t half0 = std::min<int64_t>(P.w / 2, P.n);
+  const int64_t half0 = std::min<int64_t>(wv / 2, P.n);
   const int64_t right0 = P.causal ? 0 : half0;
   // The duo kernel pairs tiles when the window reach is a multiple of 16
   // keys (the tiles' key ranges then meet on 16-key steps); the pair kernel
@@ -449,7 +459,7 @@ static lf_status run_band_bf16(const Problem& P, int b0, int nbat, BandParams& p
   const __nv_bfloat16* v = reinterpret_cast<const __nv_bfloat16*>(P.v) + off;
   __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(P.out) + off;
   const int64_t planes = (int64_t)nbat * P.H;
-  const int64_t half = std::min<int64_t>(P.w / 2, P.n);
+  const int64_t half = half0;
   int h = 0, r = 0;  // next segment to place
   while (h < P.H) {
     memset(&p, 0, sizeof p);
@@ -457,7 +467,7 @@ static lf_status run_band_bf16(const Problem& P, int b0, int nbat, BandParams& p
     int set_delta[kMaxSets], set_r[kMaxSets];
     while (h < P.H && nseg < kMaxSeg) {
       const int delta = P.dil[h];
-      if (r >= delta || r >= P.n) {
+      if (r >= delta || r >= P.n || win_of(P, h) != wv) {
         ++h;
         r = 0;
         continue;
@@ -526,6 +536,18 @@ static lf_status run_band_bf16(const Problem& P, int b0, int nbat, BandParams& p
   return LF_OK;
 }
 
+// Heads whose windows differ run in separate launches, one per window, each
+// holding the segments of its heads only.
+static lf_status run_band_bf16(const Problem& P, int b0, int nbat, BandParams& p) {
+  for (int hw = 0; hw < P.H; ++hw) {
+    bool first = true;  // hw is the first head with its window
+    for (int t = 0; t < hw && first; ++t) first = win_of(P, t) != win_of(P, hw);
+    if (!first) continue;
+    lf_status st = run_band_bf16_window(P, b0, nbat, win_of(P, hw), p);
+    if (st != LF_OK) return st;
+  }
+  return LF_OK;
+}
 static lf_status run_band_f32(const Problem& P, int b0, int nbat) {
   static thread_local SimtParams* sp = nullptr;  // ~18 KB: keep it off the stack
   if (!sp) sp = new (std::nothrow) SimtParams;
@@ -535,7 +557,10 @@ static lf_status run_band_f32(const Problem& P, int b0, int nbat) {
   }
   const size_t off = (size_t)b0 * P.H * P.n * P.d;
   fill_pattern(sp->pat, P, b0, nbat);
-  for (int h = 0; h < P.H; ++h) sp->dil[h] = P.dil[h];
+  for (int h = 0; h < P.H; ++h) {
+    sp->dil[h] = P.dil[h];
+    sp->half_h[h] = (int32_t)std::min<int64_t>(win_of(P, h) / 2, P.n);
+  }
   if (injected_fault("launch")) {
     set_error("band kernel launch: injected failure (LF_FAULT=launch)");
     return LF_ERR_CUDA;
@@ -666,6 +691,16 @@ static lf_status forward_t(const Problem& P, bool bf16) {
   return st;
 }
 
+// The per-head window entries need the window list whenever there are heads.
+static lf_status check_heads_window(const int32_t* w_heads, int32_t H) {
+  if (H > 0 && !w_heads) {
+    t_msg[0] = 0;
+    set_error("w_heads must not be NULL");
+    return LF_ERR_INVALID_ARG;
+  }
+  return LF_OK;
+}
+
 static lf_status forward(const Problem& P, bool bf16) {
   t_msg[0] = 0;
   lf_status st = validate(P, bf16);
@@ -701,6 +736,30 @@ lf_status lf_attn_fwd_f32(const void* q, const void* k, const void* v, const voi
                           const int32_t* pad_len, cudaStream_t stream) {
   lf::Problem P{q, k, v, qg, kg, vg, global_idx, n_global, out, B, H, n, d, w, dilation, causal,
                 pad_len, stream, 4};
+  return lf::forward(P, false);
+}
+
+lf_status lf_attn_fwd_hw(const void* q, const void* k, const void* v, const void* qg, const void* kg,
+                         const void* vg, const int32_t* global_idx, int32_t n_global, void* out,
+                         int32_t B, int32_t H, int32_t n, int32_t d, const int32_t* w_heads,
+                         const int32_t* dilation, int32_t causal, const int32_t* pad_len,
+                         cudaStream_t stream) {
+  lf_status st = lf::check_heads_window(w_heads, H);
+  if (st != LF_OK) return st;
+  lf::Problem P{q, k, v, qg, kg, vg, global_idx, n_global, out, B, H, n, d, 0, dilation, causal,
+                pad_len, stream, 2, w_heads};
+  return lf::forward(P, true);
+}
+
+lf_status lf_attn_fwd_hw_f32(const void* q, const void* k, const void* v, const void* qg,
+                             const void* kg, const void* vg, const int32_t* global_idx,
+                             int32_t n_global, void* out, int32_t B, int32_t H, int32_t n, int32_t d,
+                             const int32_t* w_heads, const int32_t* dilation, int32_t causal,
+                             const int32_t* pad_len, cudaStream_t stream) {
+  lf_status st = lf::check_heads_window(w_heads, H);
+  if (st != LF_OK) return st;
+  lf::Problem P{q, k, v, qg, kg, vg, global_idx, n_global, out, B, H, n, d, 0, dilation, causal,
+                pad_len, stream, 4, w_heads};
   return lf::forward(P, false);
 }
 

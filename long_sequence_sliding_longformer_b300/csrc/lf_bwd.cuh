@@ -152,9 +152,6 @@ static lf_status backward_t(const Problem& P, const void* dout, const BwdOut& g)
       bp.Htot = P.H;
       bp.b0 = b0;
       bp.h0 = h0;
-      const int64_t half = std::min<int64_t>(P.w / 2, P.n);
-      bp.half = (int32_t)half;
-      bp.right = P.causal ? 0 : (int32_t)half;
       bp.causal = P.causal;
       bp.G = P.G;
       bp.scale = (float)(1.0 / std::sqrt((double)P.d));
@@ -167,6 +164,7 @@ static lf_status backward_t(const Problem& P, const void* dout, const BwdOut& g)
       for (int h = 0; h < bp.H; ++h) {
         const int delta = P.dil[h0 + h];
         bp.dil[h] = delta;
+        bp.half_h[h] = (int32_t)std::min<int64_t>(win_of(P, h0 + h) / 2, P.n);
         bp.head_tile_off[h] = (int32_t)off;
         const int64_t qn = P.n / delta, rem = P.n % delta;
         off += rem * ((qn + 1 + bwdk::kTR - 1) / bwdk::kTR) + (delta - rem) * ((qn + bwdk::kTR - 1) / bwdk::kTR);
@@ -228,6 +226,31 @@ lf_status lf_attn_bwd_f32(const void* q, const void* k, const void* v, const voi
                           int32_t causal, const int32_t* pad_len, cudaStream_t stream) {
   lf::Problem P{q, k, v, qg, kg, vg, global_idx, n_global, nullptr, B, H, n, d, w, dilation, causal,
                 pad_len, stream, 4};
+  return lf::backward(P, dout, lf::BwdOut{dq, dk, dv, dqg, dkg, dvg}, false);
+}
+
+lf_status lf_attn_bwd_hw(const void* q, const void* k, const void* v, const void* qg, const void* kg,
+                         const void* vg, const int32_t* global_idx, int32_t n_global, const void* dout,
+                         float* dq, float* dk, float* dv, float* dqg, float* dkg, float* dvg, int32_t B,
+                         int32_t H, int32_t n, int32_t d, const int32_t* w_heads, const int32_t* dilation,
+                         int32_t causal, const int32_t* pad_len, cudaStream_t stream) {
+  lf_status st = lf::check_heads_window(w_heads, H);
+  if (st != LF_OK) return st;
+  lf::Problem P{q, k, v, qg, kg, vg, global_idx, n_global, nullptr, B, H, n, d, 0, dilation, causal,
+                pad_len, stream, 2, w_heads};
+  return lf::backward(P, dout, lf::BwdOut{dq, dk, dv, dqg, dkg, dvg}, true);
+}
+
+lf_status lf_attn_bwd_hw_f32(const void* q, const void* k, const void* v, const void* qg, const void* kg,
+                             const void* vg, const int32_t* global_idx, int32_t n_global, const void* dout,
+                             float* dq, float* dk, float* dv, float* dqg, float* dkg, float* dvg,
+                             int32_t B, int32_t H, int32_t n, int32_t d, const int32_t* w_heads,
+                             const int32_t* dilation, int32_t causal, const int32_t* pad_len,
+                             cudaStream_t stream) {
+  lf_status st = lf::check_heads_window(w_heads, H);
+  if (st != LF_OK) return st;
+  lf::Problem P{q, k, v, qg, kg, vg, global_idx, n_global, nullptr, B, H, n, d, 0, dilation, causal,
+                pad_len, stream, 4, w_heads};
   return lf::backward(P, dout, lf::BwdOut{dq, dk, dv, dqg, dkg, dvg}, false);
 }
 

@@ -90,18 +90,19 @@ struct BandParams {
 
 // ----------------------------------------------------------------- simt / global-row params
 struct PatternParams {
-  int32_t B, H, n, d, half, right, causal, G;
+  int32_t B, H, n, d, causal, G;
   float scale;
   int32_t dil_max;               // unused by kernels; kept for host checks
   int32_t pad[kMaxBatch];
   int32_t gidx[kMaxGlobal];
 };
 
-// dilation per head for the SIMT kernel (heads beyond are split on the host)
+// dilation and window per head for the SIMT kernel (at most kMaxHeadsSimt heads)
 constexpr int kMaxHeadsSimt = 256;
 struct SimtParams {
   PatternParams pat;
   int32_t dil[kMaxHeadsSimt];
+  int32_t half_h[kMaxHeadsSimt];  // reach in steps: back half_h, ahead causal ? 0 : half_h
 };
 
 // ----------------------------------------------------------------- host-side launchers

@@ -43,19 +43,19 @@ def _load():
         lib = ctypes.CDLL(_LIB_PATH)
         P = ctypes.c_void_p
         i32 = ctypes.c_int32
-        lib.lf_oracle_fwd.argtypes = [ctypes.c_int, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
+        lib.lf_oracle_fwd.argtypes = [ctypes.c_int, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P,
                                       P, i32, P, P, ctypes.c_int64, P, i32]
         lib.lf_oracle_fwd.restype = ctypes.c_int
-        lib.lf_oracle_attended.argtypes = [P, i32, i32, i32, i32, i32, P, i32, P, i32, i32, i32, P, P]
+        lib.lf_oracle_attended.argtypes = [P, i32, i32, i32, i32, i32, P, P, i32, P, i32, i32, i32, P, P]
         lib.lf_oracle_attended.restype = i32
-        lib.lf_oracle_bwd.argtypes = [ctypes.c_int, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
+        lib.lf_oracle_bwd.argtypes = [ctypes.c_int, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P,
                                       P, i32, P, P, P, P, P, P, P, i32]
         lib.lf_oracle_bwd.restype = ctypes.c_int
         lib.lf_oracle_proj.argtypes = [ctypes.c_int, P, P, P, i32, i32, i32, i32, i32, i32, P, i32]
         lib.lf_oracle_proj.restype = ctypes.c_int
         lib.lf_oracle_mem_combine.argtypes = [ctypes.c_int, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P, i32]
         lib.lf_oracle_mem_combine.restype = ctypes.c_int
-        lib.lf_oracle_count_pairs.argtypes = [P, i32, i32, i32, i32, i32, P, i32, P, P, P]
+        lib.lf_oracle_count_pairs.argtypes = [P, i32, i32, i32, i32, i32, P, P, i32, P, P, P]
         lib.lf_oracle_count_pairs.restype = i32
         lib.lf_oracle_max_threads.restype = i32
         _lib = lib
@@ -96,11 +96,22 @@ def _ptr(a) -> Optional[int]:
     return None if a is None else a.ctypes.data
 
 
+def _window(w, H: int):
+    """w: one window for every head, or one per head -> (scalar, per-head
+    int32 array or None)."""
+    if np.ndim(w) == 0:
+        return int(w), None
+    wh = _i32(w)
+    if len(wh) != H:
+        raise ValueError("w needs one entry per head (or a single int)")
+    return 0, wh
+
+
 def max_threads() -> int:
     return int(_load().lf_oracle_max_threads())
 
 
-def fwd(q, k, v, *, w: int, dilation: Optional[Sequence[int]] = None, causal: bool = False,
+def fwd(q, k, v, *, w, dilation: Optional[Sequence[int]] = None, causal: bool = False,
         pad_len: Optional[Sequence[int]] = None, qg=None, kg=None, vg=None,
         global_idx: Sequence[int] = (), rows: Optional[Sequence[int]] = None,
         threads: int = 0) -> np.ndarray:
@@ -109,7 +120,8 @@ def fwd(q, k, v, *, w: int, dilation: Optional[Sequence[int]] = None, causal: bo
     q, k, v, kg, vg: [B, H, n, d]; qg: [B, H, G, d] (row r belongs to
     global_idx[r]).  All inputs share one dtype (float64, float32 or bf16).
     rows: optional flat row ids ((b*H + h)*n + i); then the result is
-    [len(rows), d] instead of [B, H, n, d].
+    [len(rows), d] instead of [B, H, n, d].  w: the window of every head, or
+    a sequence with the window of each head.
     """
     lib = _load()
     qa, code = _as_array(q)
@@ -131,6 +143,7 @@ def fwd(q, k, v, *, w: int, dilation: Optional[Sequence[int]] = None, causal: bo
     if ka.shape != qa.shape or va.shape != qa.shape:
         raise ValueError("q, k, v shapes differ")
     dil = _i32(dilation if dilation is not None else [1] * H)
+    w0, wh = _window(w, H)
     if len(dil) != H:
         raise ValueError("dilation needs one entry per head")
     gidx = _i32(global_idx) if G else None
@@ -142,7 +155,7 @@ def fwd(q, k, v, *, w: int, dilation: Optional[Sequence[int]] = None, causal: bo
     else:
         out = np.zeros((B, H, n, d), dtype=np.float64)
     rc = lib.lf_oracle_fwd(code, _ptr(qa), _ptr(ka), _ptr(va), _ptr(qga), _ptr(kga), _ptr(vga),
-                           _ptr(gidx), G, B, H, n, d, int(w), _ptr(dil), int(bool(causal)),
+                           _ptr(gidx), G, B, H, n, d, w0, _ptr(wh), _ptr(dil), int(bool(causal)),
                            _ptr(pads), _ptr(rws), 0 if rws is None else len(rws), _ptr(out),
                            int(threads))
     if rc != 0:
@@ -150,7 +163,7 @@ def fwd(q, k, v, *, w: int, dilation: Optional[Sequence[int]] = None, causal: bo
     return out
 
 
-def bwd(q, k, v, dout, *, w: int, dilation: Optional[Sequence[int]] = None, causal: bool = False,
+def bwd(q, k, v, dout, *, w, dilation: Optional[Sequence[int]] = None, causal: bool = False,
         pad_len: Optional[Sequence[int]] = None, qg=None, kg=None, vg=None,
         global_idx: Sequence[int] = (), threads: int = 0) -> dict:
     """Gradients of sum(dout * out) in float64: a dict with dq, dk, dv and,
@@ -177,6 +190,7 @@ def bwd(q, k, v, dout, *, w: int, dilation: Optional[Sequence[int]] = None, caus
         if qga.shape != (B, H, G, d) or kga.shape != qa.shape or vga.shape != qa.shape:
             raise ValueError("global tensor shapes do not match")
     dil = _i32(dilation if dilation is not None else [1] * H)
+    w0, wh = _window(w, H)
     if len(dil) != H:
         raise ValueError("dilation needs one entry per head")
     gidx = _i32(global_idx) if G else None
@@ -187,7 +201,7 @@ def bwd(q, k, v, dout, *, w: int, dilation: Optional[Sequence[int]] = None, caus
         g["dkg"] = np.zeros((B, H, n, d), dtype=np.float64)
         g["dvg"] = np.zeros((B, H, n, d), dtype=np.float64)
     rc = lib.lf_oracle_bwd(code, _ptr(qa), _ptr(ka), _ptr(va), _ptr(qga), _ptr(kga), _ptr(vga), _ptr(da),
-                           _ptr(gidx), G, B, H, n, d, int(w), _ptr(dil), int(bool(causal)), _ptr(pads),
+                           _ptr(gidx), G, B, H, n, d, w0, _ptr(wh), _ptr(dil), int(bool(causal)), _ptr(pads),
                            _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g.get("dqg")),
                            _ptr(g.get("dkg")), _ptr(g.get("dvg")), int(threads))
     if rc != 0:
@@ -249,7 +263,7 @@ def mem_combine(q, local, mem_k, mem_v, idx, gate, threads: int = 0) -> np.ndarr
     return out
 
 
-def attended(*, n: int, w: int, dilation: Sequence[int], causal: bool = False,
+def attended(*, n: int, w, dilation: Sequence[int], causal: bool = False,
              global_idx: Sequence[int] = (), pad_len: Optional[Sequence[int]] = None,
              b: int = 0, h: int = 0, i: int = 0, B: int = 1):
     """(sorted list of attended keys, is_global_row) for one row."""
@@ -260,14 +274,15 @@ def attended(*, n: int, w: int, dilation: Sequence[int], causal: bool = False,
     pads = _i32(pad_len)
     keys = np.zeros(max(n, 1), dtype=np.int32)
     isg = np.zeros(1, dtype=np.int32)
-    cnt = lib.lf_oracle_attended(_ptr(gidx), len(global_idx), B, H, n, int(w), _ptr(dil),
+    w0, wh = _window(w, H)
+    cnt = lib.lf_oracle_attended(_ptr(gidx), len(global_idx), B, H, n, w0, _ptr(wh), _ptr(dil),
                                  int(bool(causal)), _ptr(pads), b, h, i, _ptr(keys), _ptr(isg))
     if cnt < 0:
         raise ValueError("oracle rejected the pattern")
     return sorted(int(x) for x in keys[:cnt]), bool(isg[0])
 
 
-def count_pairs(*, B: int, H: int, n: int, w: int, dilation: Sequence[int], causal: bool = False,
+def count_pairs(*, B: int, H: int, n: int, w, dilation: Sequence[int], causal: bool = False,
                 global_idx: Sequence[int] = (), pad_len: Optional[Sequence[int]] = None):
     """(attended pairs over every row, pairs on the global tokens' own rows),
     by enumerating each row's attended set."""
@@ -277,7 +292,8 @@ def count_pairs(*, B: int, H: int, n: int, w: int, dilation: Sequence[int], caus
     pads = _i32(pad_len)
     pairs = np.zeros(1, dtype=np.int64)
     gpairs = np.zeros(1, dtype=np.int64)
-    rc = lib.lf_oracle_count_pairs(_ptr(gidx), len(global_idx), B, H, n, int(w), _ptr(dil),
+    w0, wh = _window(w, H)
+    rc = lib.lf_oracle_count_pairs(_ptr(gidx), len(global_idx), B, H, n, w0, _ptr(wh), _ptr(dil),
                                    int(bool(causal)), _ptr(pads), _ptr(pairs), _ptr(gpairs))
     if rc != 0:
         raise ValueError("oracle rejected the pattern")

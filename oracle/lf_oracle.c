@@ -61,7 +61,14 @@ typedef struct {
   int32_t G, B, H, n, d, w, causal;
   const int32_t* dilation;
   const int32_t* pad_len;
+  const int32_t* w_heads; /* window of each head, or NULL: w for every head */
 } problem;
+
+/* The window of head h (section 4.1 "Attention Pattern": window sizes differ
+ * between layers, and heads within a layer differ in their pattern). */
+static int64_t window_of(const problem* p, int32_t h) {
+  return p->w_heads ? p->w_heads[h] : p->w;
+}
 
 /* rank of position i in the sorted global list, or -1 if i is not global */
 static int global_rank(const problem* p, int32_t i) {
@@ -73,7 +80,7 @@ static int global_rank(const problem* p, int32_t i) {
 /* Is key j inside row i's (dilated, possibly causal) window? */
 static int in_window(const problem* p, int32_t h, int32_t i, int32_t j) {
   int64_t delta = p->dilation[h];
-  int64_t half = p->w / 2;
+  int64_t half = window_of(p, h) / 2;
   int64_t off = (int64_t)j - (int64_t)i;           /* key offset from the row */
   if (off % delta != 0) return 0;                  /* dilation gaps */
   int64_t steps = off / delta;
@@ -103,7 +110,7 @@ static int32_t attended_set(const problem* p, int32_t b, int32_t h, int32_t i,
   }
   /* the window: offsets delta*t for t in [-half, +half] (t <= 0 if causal) */
   int64_t delta = p->dilation[h];
-  int64_t half = p->w / 2;
+  int64_t half = window_of(p, h) / 2;
   if (half > p->n) half = p->n;                  /* wider reaches nothing new */
   int64_t right = p->causal ? 0 : half;
   for (int64_t t = -half; t <= right; ++t) {
@@ -161,7 +168,11 @@ static void one_row(const problem* p, int32_t b, int32_t h, int32_t i,
 }
 
 static int check_problem(const problem* p) {
-  if (p->B < 0 || p->H < 0 || p->n < 0 || p->d <= 0 || p->w < 0 || (p->w & 1)) return 1;
+  if (p->B < 0 || p->H < 0 || p->n < 0 || p->d <= 0) return 1;
+  for (int32_t h = 0; h < (p->w_heads ? p->H : 1); ++h) {
+    int64_t w = p->w_heads ? p->w_heads[h] : p->w;
+    if (w < 0 || (w & 1)) return 1;
+  }
   if (p->G < 0 || (p->G > 0 && !p->global_idx)) return 1;
   for (int32_t h = 0; h < p->H; ++h)
     if (p->dilation[h] < 1) return 1;
@@ -183,10 +194,10 @@ static int check_problem(const problem* p) {
 int lf_oracle_fwd(int dtype, const void* q, const void* k, const void* v,
                   const void* qg, const void* kg, const void* vg,
                   const int32_t* global_idx, int32_t G,
-                  int32_t B, int32_t H, int32_t n, int32_t d, int32_t w,
+                  int32_t B, int32_t H, int32_t n, int32_t d, int32_t w, const int32_t* w_heads,
                   const int32_t* dilation, int32_t causal, const int32_t* pad_len,
                   const int64_t* rows, int64_t nrows, double* out, int32_t nthreads) {
-  problem p = {dtype, q, k, v, qg, kg, vg, global_idx, G, B, H, n, d, w, causal, dilation, pad_len};
+  problem p = {dtype, q, k, v, qg, kg, vg, global_idx, G, B, H, n, d, w, causal, dilation, pad_len, w_heads};
   if (check_problem(&p)) return 1;
   int64_t total = rows ? nrows : (int64_t)B * H * n;
   if (total == 0) return 0;
@@ -299,11 +310,11 @@ static void one_row_bwd(const problem* p, const void* dout, int32_t b, int32_t h
 int lf_oracle_bwd(int dtype, const void* q, const void* k, const void* v,
                   const void* qg, const void* kg, const void* vg, const void* dout,
                   const int32_t* global_idx, int32_t G,
-                  int32_t B, int32_t H, int32_t n, int32_t d, int32_t w,
+                  int32_t B, int32_t H, int32_t n, int32_t d, int32_t w, const int32_t* w_heads,
                   const int32_t* dilation, int32_t causal, const int32_t* pad_len,
                   double* dq, double* dk, double* dv, double* dqg, double* dkg, double* dvg,
                   int32_t nthreads) {
-  problem p = {dtype, q, k, v, qg, kg, vg, global_idx, G, B, H, n, d, w, causal, dilation, pad_len};
+  problem p = {dtype, q, k, v, qg, kg, vg, global_idx, G, B, H, n, d, w, causal, dilation, pad_len, w_heads};
   if (check_problem(&p)) return 1;
   if (!dq || !dk || !dv || (G > 0 && (!dqg || !dkg || !dvg))) return 1;
   const size_t full = (size_t)B * H * n * d;
@@ -440,10 +451,10 @@ int lf_oracle_mem_combine(int dtype, const void* q, const void* local, const voi
 
 /* The attended key set of one row (for pattern tests).  keys must hold n ints. */
 int32_t lf_oracle_attended(const int32_t* global_idx, int32_t G, int32_t B, int32_t H,
-                           int32_t n, int32_t w, const int32_t* dilation, int32_t causal,
-                           const int32_t* pad_len, int32_t b, int32_t h, int32_t i,
+                           int32_t n, int32_t w, const int32_t* w_heads, const int32_t* dilation,
+                           int32_t causal, const int32_t* pad_len, int32_t b, int32_t h, int32_t i,
                            int32_t* keys, int32_t* is_global_row) {
-  problem p = {ORC_F64, 0, 0, 0, 0, 0, 0, global_idx, G, B, H, n, 1, w, causal, dilation, pad_len};
+  problem p = {ORC_F64, 0, 0, 0, 0, 0, 0, global_idx, G, B, H, n, 1, w, causal, dilation, pad_len, w_heads};
   if (check_problem(&p)) return -1;
   int g = 0;
   int32_t cnt = attended_set(&p, b, h, i, keys, &g);
@@ -457,9 +468,10 @@ int32_t lf_oracle_attended(const int32_t* global_idx, int32_t G, int32_t B, int3
  * own rows.  Returns 0, or -1 for a rejected pattern.
  */
 int32_t lf_oracle_count_pairs(const int32_t* global_idx, int32_t G, int32_t B, int32_t H,
-                              int32_t n, int32_t w, const int32_t* dilation, int32_t causal,
-                              const int32_t* pad_len, int64_t* pairs, int64_t* global_pairs) {
-  problem p = {ORC_F64, 0, 0, 0, 0, 0, 0, global_idx, G, B, H, n, 1, w, causal, dilation, pad_len};
+                              int32_t n, int32_t w, const int32_t* w_heads, const int32_t* dilation,
+                              int32_t causal, const int32_t* pad_len, int64_t* pairs,
+                              int64_t* global_pairs) {
+  problem p = {ORC_F64, 0, 0, 0, 0, 0, 0, global_idx, G, B, H, n, 1, w, causal, dilation, pad_len, w_heads};
   if (check_problem(&p)) return -1;
   int64_t tot = 0, gtot = 0;
   int err = 0;

@@ -6,6 +6,7 @@ ordinary dense softmax attention, where the oracle walks each row's window.
 Pattern (velog.io/@lainshower/Longformer, section 3-1): band |j - i| <= w/2
 with dilation gaps, look-back only when causal (section 4.1), global tokens
 as full rows (scored with qg, kg, vg) and full columns, padding masked.
+w is one window for every head or a sequence with one per head (section 4.1).
 """
 import numpy as np
 
@@ -36,7 +37,7 @@ def attention(q, k, v, w, dilation, causal=False, pad_len=None, qg=None, kg=None
     for b in range(B):
         L = n - (pad_len[b] if pad_len is not None else 0)
         for h in range(H):
-            local, glob = masks(n, w, dilation[h], causal, global_idx, L)
+            local, glob = masks(n, w[h] if np.ndim(w) else w, dilation[h], causal, global_idx, L)
             qq = q[b, h].copy()
             kk = np.repeat(k[b, h][None], n, axis=0)  # per-row key matrix [n, n, d]
             vv = np.repeat(v[b, h][None], n, axis=0)

@@ -259,3 +259,28 @@ def test_varglobal_refuses_bad_offsets_on_host(lib):
         st = lib.lf_attn_fwd_varglobal(f[0], f[1], f[2], f[3], f[4], f[5], _i32p(offs), _i32p(gidx), f[6],
                                        2, 2, 64, 64, 8, _i32p([1, 1]), 0, None, None)
         assert st == 1, (offs, gidx)
+
+
+@pytest.mark.parametrize("fn", ["lf_attn_fwd_hw", "lf_attn_fwd_hw_f32"])
+def test_per_head_windows_refused_on_host(lib, fn):
+    """A window per head: the list is required, and each entry must be even
+    and >= 0 (the bad entry is named in the message)."""
+    f = _FAKE
+    call = lambda wh, H=2: getattr(lib, fn)(f[0], f[1], f[2], None, None, None, None, 0, f[6], 1, H, 64, 64,
+                                           _i32p(wh) if wh is not None else None, _i32p([1] * H), 0, None,
+                                           None)
+    assert call(None) == 1
+    assert "w_heads" in lib.lf_last_error_message().decode()
+    assert call([8, 7]) == 1
+    assert "w_heads[1]" in lib.lf_last_error_message().decode()
+    assert call([8, -2]) == 1
+    assert call(None, H=0) == 0  # no heads: nothing to do
+
+
+def test_per_head_window_backward_refused_on_host(lib):
+    args = _bwd_args(lib)
+    args[19] = _i32p([4, 3])  # odd window of head 1
+    assert lib.lf_attn_bwd_hw(*args) == 1
+    assert "w_heads[1]" in lib.lf_last_error_message().decode()
+    args[19] = None
+    assert lib.lf_attn_bwd_hw(*args) == 1

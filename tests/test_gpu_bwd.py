@@ -60,6 +60,10 @@ CASES = [
     ("f32_d40_causal", "f32", 2, 2, 333, 40, 30, (1, 4), True, (11,), (7, 0)),
     ("f32_d128_g", "f32", 1, 1, 300, 128, 100, (3,), False, (0, 1, 2), None),
     ("f32_d7", "f32", 1, 3, 97, 7, 10, (1, 2, 3), True, (), None),
+    # a window per head (section 4.1 "Attention Pattern")
+    ("bf16_d64_heads_w", "bf16", 2, 3, 400, 64, [16, 128, 0], (1, 2, 1), False, (0, 150), (0, 60)),
+    ("bf16_d128_heads_w", "bf16", 1, 2, 500, 128, [64, 256], (1, 1), True, (3,), None),
+    ("f32_d48_heads_w", "f32", 1, 3, 300, 48, [64, 8, 200], (2, 1, 1), True, (7,), None),
 ]
 
 

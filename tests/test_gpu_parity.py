@@ -191,6 +191,29 @@ def test_bf16_few_globals_on_ring(G, w, causal):
     check(wl, out, oracle.wl_fwd(wl, inp))
 
 
+@pytest.mark.parametrize("d,G,causal", [(64, 0, False), (64, 1, True), (64, 20, False), (128, 1, False),
+                                         (128, 0, True)])
+def test_bf16_per_head_windows(d, G, causal):
+    """A window per head (section 4.1 "Attention Pattern"): one launch per
+    distinct window, each holding only its heads' tiles; heads that share a
+    window share a launch although they are not adjacent.  G = 20 at d = 64
+    takes the duo kernel, d = 128 the pair kernel."""
+    wh = [512, 64, 0, 64, 2000, 512]
+    dil = [1, 1, 2, 3, 1, 2]
+    gidx = tuple(range(0, 900, 45))[:G]
+    wl = workloads.custom("hw", "bf16", 2, 6, 900, d, wh, dil, causal, gidx, (0, 250), seed=50 + d + G)
+    inp = workloads.make_inputs(wl, "cuda")
+    check(wl, run(wl, inp), oracle.wl_fwd(wl, inp))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_f32_per_head_windows(causal):
+    wl = workloads.custom("hw32", "f32", 2, 4, 500, 40, [6, 100, 0, 1200], (1, 2, 1, 3), causal, (0, 250),
+                          (0, 90), seed=60)
+    inp = workloads.make_inputs(wl, "cuda")
+    check(wl, run(wl, inp), oracle.wl_fwd(wl, inp))
+
+
 def test_bf16_many_globals():
     wl = workloads.custom("glob", "bf16", 1, 2, 1500, 64, 32, (1, 2), False, tuple(range(0, 1500, 5)),
                           (0,), seed=4)

@@ -42,6 +42,9 @@ PATTERNS = [
     dict(w=8, dilation=[1, 1], causal=False, pad_len=None, global_idx=[]),
     dict(w=0, dilation=[2, 1], causal=True, pad_len=[0, 11], global_idx=[1]),
     dict(w=40, dilation=[1, 4], causal=False, pad_len=[3, 0], global_idx=[0, 5, 19]),
+    # a window per head (section 4.1 "Attention Pattern")
+    dict(w=[2, 10], dilation=[1, 2], causal=False, pad_len=[0, 4], global_idx=[3, 20]),
+    dict(w=[8, 0], dilation=[2, 1], causal=True, pad_len=None, global_idx=[6]),
 ]
 
 
@@ -80,7 +83,8 @@ def _dense_torch(x, pat):
         L = n - (pat["pad_len"][b] if pat["pad_len"] else 0)
         heads = []
         for h in range(H):
-            local, glob = dense_masks(n, pat["w"], pat["dilation"][h], pat["causal"], gidx, L)
+            wh = pat["w"][h] if np.ndim(pat["w"]) else pat["w"]
+            local, glob = dense_masks(n, wh, pat["dilation"][h], pat["causal"], gidx, L)
             outs = []
             for i in range(n):
                 if i in rank:

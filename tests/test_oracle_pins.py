@@ -144,6 +144,27 @@ def test_oracle_matches_dense_mask(n, d, w, dl, causal, gsel, pad):
 
 
 @pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("wh,dil", [([0, 6, 64], [1, 1, 1]), ([10, 2, 30], [1, 3, 2]), ([4, 4, 600], [2, 1, 1])])
+def test_per_head_windows_match_dense_mask(wh, dil, causal):
+    """A window per head (section 4.1 "Attention Pattern") against the dense
+    mask built head by head; one head's window reaches past the sequence."""
+    n, d, B = 130, 8, 2
+    gidx = [0, 64, 129]
+    pads = [0, 40]
+    rng = np.random.default_rng(sum(wh) + 7 * causal)
+    q, k, v, qg, kg, vg = _rand_problem(rng, B, len(wh), n, d, len(gidx))
+    got = oracle.fwd(q, k, v, w=wh, dilation=dil, causal=causal, pad_len=pads, qg=qg, kg=kg, vg=vg,
+                     global_idx=gidx)
+    want = dense_attention(q, k, v, wh, dil, causal, pads, qg, kg, vg, gidx)
+    np.testing.assert_allclose(got, want, atol=1e-12, rtol=0)
+    # and a head's rows do not depend on the other heads' windows
+    for h, w in enumerate(wh):
+        one = oracle.fwd(q, k, v, w=w, dilation=dil, causal=causal, pad_len=pads, qg=qg, kg=kg, vg=vg,
+                         global_idx=gidx)
+        np.testing.assert_array_equal(got[:, h], one[:, h])
+
+
+@pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("n,d", [(5, 3), (64, 16), (200, 64)])
 def test_full_attention_limit_matches_sdpa(n, d, causal):
     """w >= 2n, dilation 1, no globals, no padding is ordinary (causal) attention."""
@@ -289,6 +310,10 @@ def test_rejects_invalid_patterns():
     z = np.zeros((1, 1, 4, 2))
     with pytest.raises(ValueError):
         oracle.fwd(z, z, z, w=3, dilation=[1])  # odd window
+    with pytest.raises(ValueError):
+        oracle.fwd(z, z, z, w=[5], dilation=[1])  # odd window of a head
+    with pytest.raises(ValueError):
+        oracle.fwd(z, z, z, w=[2, 2], dilation=[1])  # one window per head
     with pytest.raises(ValueError):
         oracle.fwd(z, z, z, w=2, dilation=[0])
     with pytest.raises(ValueError):

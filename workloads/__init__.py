@@ -19,7 +19,7 @@ seeded 1 (``torch.randint(2048, 4097, (B,))``).
 from __future__ import annotations
 
 import dataclasses
-from typing import Dict, List, Optional, Tuple
+from typing import Dict, List, Optional, Tuple, Union
 
 import torch
 
@@ -34,7 +34,7 @@ class Workload:
     H: int
     n: int
     d: int
-    w: int  # total window; w/2 keys on each side (look-back only if causal)
+    w: Union[int, Tuple[int, ...]]  # total window, or one per head; w/2 keys on each side (look-back only if causal)
     dilation: Tuple[int, ...]  # one entry per head
     causal: bool = False
     global_idx: Tuple[int, ...] = ()
@@ -169,7 +169,8 @@ def make_inputs(wl: Workload, device: str = "cpu", seed: Optional[int] = None) -
 def custom(name: str = "custom", dtype: str = "bf16", B: int = 1, H: int = 1, n: int = 128,
            d: int = 64, w: int = 8, dilation=None, causal: bool = False, global_idx=(),
            pad_len=None, seed: int = 0) -> Workload:
-    """A small pattern for tests and sweeps."""
+    """A small pattern for tests and sweeps (w: one window, or one per head)."""
     dil = tuple(dilation) if dilation is not None else (1,) * H
+    w = tuple(int(x) for x in w) if isinstance(w, (list, tuple)) else w
     return Workload(name, dtype, B, H, n, d, w, dil, causal, tuple(global_idx),
                     tuple(pad_len) if pad_len is not None else None, seed)
