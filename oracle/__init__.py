@@ -44,12 +44,12 @@ def _load():
         P = ctypes.c_void_p
         i32 = ctypes.c_int32
         lib.lf_oracle_fwd.argtypes = [ctypes.c_int, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P,
-                                      P, i32, P, P, ctypes.c_int64, P, i32]
+                                      P, i32, P, P, P, ctypes.c_int64, P, i32]
         lib.lf_oracle_fwd.restype = ctypes.c_int
         lib.lf_oracle_attended.argtypes = [P, i32, i32, i32, i32, i32, P, P, i32, P, i32, i32, i32, P, P]
         lib.lf_oracle_attended.restype = i32
         lib.lf_oracle_bwd.argtypes = [ctypes.c_int, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P,
-                                      P, i32, P, P, P, P, P, P, P, i32]
+                                      P, i32, P, P, P, P, P, P, P, P, P, i32]
         lib.lf_oracle_bwd.restype = ctypes.c_int
         lib.lf_oracle_proj.argtypes = [ctypes.c_int, P, P, P, i32, i32, i32, i32, i32, i32, P, i32]
         lib.lf_oracle_proj.restype = ctypes.c_int
@@ -96,6 +96,25 @@ def _ptr(a) -> Optional[int]:
     return None if a is None else a.ctypes.data
 
 
+def _bias_table(rel_bias, H: int, w0: int, wh) -> Optional[np.ndarray]:
+    """The relative bias table as contiguous float32 [H, w + 1], or None."""
+    if rel_bias is None:
+        return None
+    if wh is not None:
+        raise ValueError("a relative bias takes one window for every head")
+    try:
+        import torch
+
+        if isinstance(rel_bias, torch.Tensor):
+            rel_bias = rel_bias.detach().cpu().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    rb = np.ascontiguousarray(np.asarray(rel_bias, dtype=np.float32))
+    if rb.shape != (H, w0 + 1):
+        raise ValueError("rel_bias must be [H, w + 1] = [%d, %d], got %s" % (H, w0 + 1, rb.shape))
+    return rb
+
+
 def _window(w, H: int):
     """w: one window for every head, or one per head -> (scalar, per-head
     int32 array or None)."""
@@ -114,14 +133,16 @@ def max_threads() -> int:
 def fwd(q, k, v, *, w, dilation: Optional[Sequence[int]] = None, causal: bool = False,
         pad_len: Optional[Sequence[int]] = None, qg=None, kg=None, vg=None,
         global_idx: Sequence[int] = (), rows: Optional[Sequence[int]] = None,
-        threads: int = 0) -> np.ndarray:
+        rel_bias=None, threads: int = 0) -> np.ndarray:
     """Attention output in float64.
 
     q, k, v, kg, vg: [B, H, n, d]; qg: [B, H, G, d] (row r belongs to
     global_idx[r]).  All inputs share one dtype (float64, float32 or bf16).
     rows: optional flat row ids ((b*H + h)*n + i); then the result is
     [len(rows), d] instead of [B, H, n, d].  w: the window of every head, or
-    a sequence with the window of each head.
+    a sequence with the window of each head.  rel_bias: optional [H, w + 1]
+    float32 table added to the band keys' scores (entry t + w/2 for window
+    step t).
     """
     lib = _load()
     qa, code = _as_array(q)
@@ -148,6 +169,7 @@ def fwd(q, k, v, *, w, dilation: Optional[Sequence[int]] = None, causal: bool = 
         raise ValueError("dilation needs one entry per head")
     gidx = _i32(global_idx) if G else None
     pads = _i32(pad_len)
+    rb = _bias_table(rel_bias, H, w0, wh)
     rws = None
     if rows is not None:
         rws = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
@@ -156,7 +178,7 @@ def fwd(q, k, v, *, w, dilation: Optional[Sequence[int]] = None, causal: bool = 
         out = np.zeros((B, H, n, d), dtype=np.float64)
     rc = lib.lf_oracle_fwd(code, _ptr(qa), _ptr(ka), _ptr(va), _ptr(qga), _ptr(kga), _ptr(vga),
                            _ptr(gidx), G, B, H, n, d, w0, _ptr(wh), _ptr(dil), int(bool(causal)),
-                           _ptr(pads), _ptr(rws), 0 if rws is None else len(rws), _ptr(out),
+                           _ptr(pads), _ptr(rb), _ptr(rws), 0 if rws is None else len(rws), _ptr(out),
                            int(threads))
     if rc != 0:
         raise ValueError("oracle rejected the problem (code %d)" % rc)
@@ -165,10 +187,11 @@ def fwd(q, k, v, *, w, dilation: Optional[Sequence[int]] = None, causal: bool = 
 
 def bwd(q, k, v, dout, *, w, dilation: Optional[Sequence[int]] = None, causal: bool = False,
         pad_len: Optional[Sequence[int]] = None, qg=None, kg=None, vg=None,
-        global_idx: Sequence[int] = (), threads: int = 0) -> dict:
+        global_idx: Sequence[int] = (), rel_bias=None, threads: int = 0) -> dict:
     """Gradients of sum(dout * out) in float64: a dict with dq, dk, dv and,
-    when there are global tokens, dqg, dkg, dvg (each the shape of its input).
-    dout has out's shape and the inputs' dtype."""
+    when there are global tokens, dqg, dkg, dvg (each the shape of its input),
+    and with rel_bias its gradient drel_bias [H, w + 1].  dout has out's shape
+    and the inputs' dtype."""
     lib = _load()
     qa, code = _as_array(q)
     ka, kc = _as_array(k)
@@ -200,10 +223,13 @@ def bwd(q, k, v, dout, *, w, dilation: Optional[Sequence[int]] = None, causal: b
         g["dqg"] = np.zeros((B, H, G, d), dtype=np.float64)
         g["dkg"] = np.zeros((B, H, n, d), dtype=np.float64)
         g["dvg"] = np.zeros((B, H, n, d), dtype=np.float64)
+    rb = _bias_table(rel_bias, H, w0, wh)
+    if rb is not None:
+        g["drel_bias"] = np.zeros(rb.shape, dtype=np.float64)
     rc = lib.lf_oracle_bwd(code, _ptr(qa), _ptr(ka), _ptr(va), _ptr(qga), _ptr(kga), _ptr(vga), _ptr(da),
                            _ptr(gidx), G, B, H, n, d, w0, _ptr(wh), _ptr(dil), int(bool(causal)), _ptr(pads),
-                           _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g.get("dqg")),
-                           _ptr(g.get("dkg")), _ptr(g.get("dvg")), int(threads))
+                           _ptr(rb), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g.get("dqg")),
+                           _ptr(g.get("dkg")), _ptr(g.get("dvg")), _ptr(g.get("drel_bias")), int(threads))
     if rc != 0:
         raise ValueError("oracle rejected the problem (code %d)" % rc)
     return g
@@ -306,15 +332,15 @@ def wl_count_pairs(wl):
                        global_idx=wl.global_idx, pad_len=wl.pad_len)
 
 
-def wl_bwd(wl, inputs, dout, threads: int = 0) -> dict:
+def wl_bwd(wl, inputs, dout, threads: int = 0, rel_bias=None) -> dict:
     """bwd() for a workloads.Workload, its Inputs and an upstream gradient."""
     return bwd(inputs.q, inputs.k, inputs.v, dout, w=wl.w, dilation=wl.dilation, causal=wl.causal,
                pad_len=wl.pad_len, qg=inputs.qg, kg=inputs.kg, vg=inputs.vg,
-               global_idx=wl.global_idx, threads=threads)
+               global_idx=wl.global_idx, rel_bias=rel_bias, threads=threads)
 
 
-def wl_fwd(wl, inputs, rows=None, threads: int = 0) -> np.ndarray:
+def wl_fwd(wl, inputs, rows=None, threads: int = 0, rel_bias=None) -> np.ndarray:
     """fwd() for a workloads.Workload and its Inputs."""
     return fwd(inputs.q, inputs.k, inputs.v, w=wl.w, dilation=wl.dilation, causal=wl.causal,
                pad_len=wl.pad_len, qg=inputs.qg, kg=inputs.kg, vg=inputs.vg,
-               global_idx=wl.global_idx, rows=rows, threads=threads)
+               global_idx=wl.global_idx, rows=rows, rel_bias=rel_bias, threads=threads)

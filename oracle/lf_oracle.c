@@ -26,7 +26,8 @@
  * restricts global rows (keys j <= g) and global columns (g <= i).
  * Padding: pad_len[b] trailing tokens of batch row b are padding; they are
  * never attended and their output rows are exact zeros.
- * Scale 1/sqrt(d); no dropout or bias.
+ * Scale 1/sqrt(d); no dropout.  An optional relative position bias is added
+ * to the band keys' scores (band_bias below).
  *
  * Everything is evaluated in double: for each row the attended set is
  * enumerated, scores are computed with a plain dot product, the row maximum
@@ -62,6 +63,7 @@ typedef struct {
   const int32_t* dilation;
   const int32_t* pad_len;
   const int32_t* w_heads; /* window of each head, or NULL: w for every head */
+  const float* rel_bias;  /* [H, w + 1] relative position bias of the band keys, or NULL */
 } problem;
 
 /* The window of head h (section 4.1 "Attention Pattern": window sizes differ
@@ -87,6 +89,21 @@ static int in_window(const problem* p, int32_t h, int32_t i, int32_t j) {
   int64_t left = half;                             /* look-back reach in steps */
   int64_t right = p->causal ? 0 : half;            /* look-ahead reach in steps */
   return steps >= -left && steps <= right;
+}
+
+/*
+ * The relative position bias of key j in row i's band (Memorizing
+ * Transformer notes, "Position bias": a T5-style bias added to the attention
+ * scores, a learned scalar per head and relative position).  Read here as
+ * rel_bias[h][t + w/2] added to the scaled score of the band key at window
+ * step t = (j - i) / delta, t in [-w/2, w/2]; the caller expands any bucketing
+ * of relative positions into that table.  Global columns outside the band
+ * and the global tokens' own rows get no bias.
+ */
+static double band_bias(const problem* p, int32_t h, int32_t i, int32_t j) {
+  if (!p->rel_bias || !in_window(p, h, i, j)) return 0.0;
+  int64_t t = ((int64_t)j - (int64_t)i) / p->dilation[h];
+  return (double)p->rel_bias[(int64_t)h * (p->w + 1) + t + p->w / 2];
 }
 
 /*
@@ -127,7 +144,7 @@ static int32_t attended_set(const problem* p, int32_t b, int32_t h, int32_t i,
   return cnt;
 }
 
-/* one output row: softmax(scale * <q_row, k_j>) weighted sum of v_j over keys */
+/* one output row: softmax(scale * <q_row, k_j> + bias) weighted sum of v_j over keys */
 static void one_row(const problem* p, int32_t b, int32_t h, int32_t i,
                     int32_t* keys, double* scores, double* out_row) {
   const int32_t n = p->n, d = p->d;
@@ -154,6 +171,7 @@ static void one_row(const problem* p, int32_t b, int32_t h, int32_t i,
     for (int32_t c = 0; c < d; ++c)
       s += load_elem(p->dtype, qs, qrow * d + c) * load_elem(p->dtype, ks, krow * d + c);
     s *= scale;
+    if (!is_g) s += band_bias(p, h, i, keys[t]);
     scores[t] = s;
     if (s > mx) mx = s;
   }
@@ -169,6 +187,7 @@ static void one_row(const problem* p, int32_t b, int32_t h, int32_t i,
 
 static int check_problem(const problem* p) {
   if (p->B < 0 || p->H < 0 || p->n < 0 || p->d <= 0) return 1;
+  if (p->rel_bias && p->w_heads) return 1; /* the bias table is sized by the one w */
   for (int32_t h = 0; h < (p->w_heads ? p->H : 1); ++h) {
     int64_t w = p->w_heads ? p->w_heads[h] : p->w;
     if (w < 0 || (w & 1)) return 1;
@@ -196,8 +215,10 @@ int lf_oracle_fwd(int dtype, const void* q, const void* k, const void* v,
                   const int32_t* global_idx, int32_t G,
                   int32_t B, int32_t H, int32_t n, int32_t d, int32_t w, const int32_t* w_heads,
                   const int32_t* dilation, int32_t causal, const int32_t* pad_len,
+                  const float* rel_bias,
                   const int64_t* rows, int64_t nrows, double* out, int32_t nthreads) {
-  problem p = {dtype, q, k, v, qg, kg, vg, global_idx, G, B, H, n, d, w, causal, dilation, pad_len, w_heads};
+  problem p = {dtype, q, k, v, qg, kg, vg, global_idx, G, B, H, n, d, w, causal, dilation, pad_len, w_heads,
+               rel_bias};
   if (check_problem(&p)) return 1;
   int64_t total = rows ? nrows : (int64_t)B * H * n;
   if (total == 0) return 0;
@@ -240,10 +261,11 @@ int lf_oracle_fwd(int dtype, const void* q, const void* k, const void* v,
  *   ds_t    = p_t * (dp_t - sum_u p_u dp_u)
  *   dq_row += scale * sum_t ds_t k_t
  *   dk_t   += scale * ds_t q_row
+ *   drb[t]  += ds_t for a band key at window step t (relative bias)
  */
 static void one_row_bwd(const problem* p, const void* dout, int32_t b, int32_t h, int32_t i,
                         int32_t* keys, double* scores, double* dp, double* dq, double* dk,
-                        double* dv, double* dqg, double* dkg, double* dvg) {
+                        double* dv, double* dqg, double* dkg, double* dvg, double* drb) {
   const int32_t n = p->n, d = p->d;
   const int64_t bh = (int64_t)b * p->H + h;
   int is_g = 0;
@@ -270,7 +292,7 @@ static void one_row_bwd(const problem* p, const void* dout, int32_t b, int32_t h
     double s = 0.0;
     for (int32_t c = 0; c < d; ++c)
       s += load_elem(p->dtype, qs, qrow * d + c) * load_elem(p->dtype, ks, krow * d + c);
-    scores[t] = s * scale;
+    scores[t] = s * scale + (is_g ? 0.0 : band_bias(p, h, i, keys[t]));
     if (scores[t] > mx) mx = scores[t];
   }
   double total = 0.0;
@@ -292,6 +314,9 @@ static void one_row_bwd(const problem* p, const void* dout, int32_t b, int32_t h
   for (int32_t t = 0; t < cnt; ++t) {
     int64_t kvrow = bh * n + keys[t];
     double ds = scores[t] * (dp[t] - dsum);
+    /* the bias enters the score with weight 1: its gradient is ds */
+    if (drb && !is_g && in_window(p, h, i, keys[t]))
+      drb[((int64_t)keys[t] - i) / p->dilation[h] + p->w / 2] += ds;
     for (int32_t c = 0; c < d; ++c) {
       dvs[kvrow * d + c] += scores[t] * load_elem(p->dtype, dout, orow * d + c);
       dq_row[c] += scale * ds * load_elem(p->dtype, ks, kvrow * d + c);
@@ -312,10 +337,20 @@ int lf_oracle_bwd(int dtype, const void* q, const void* k, const void* v,
                   const int32_t* global_idx, int32_t G,
                   int32_t B, int32_t H, int32_t n, int32_t d, int32_t w, const int32_t* w_heads,
                   const int32_t* dilation, int32_t causal, const int32_t* pad_len,
+                  const float* rel_bias,
                   double* dq, double* dk, double* dv, double* dqg, double* dkg, double* dvg,
-                  int32_t nthreads) {
-  problem p = {dtype, q, k, v, qg, kg, vg, global_idx, G, B, H, n, d, w, causal, dilation, pad_len, w_heads};
+                  double* d_rel_bias, int32_t nthreads) {
+  problem p = {dtype, q, k, v, qg, kg, vg, global_idx, G, B, H, n, d, w, causal, dilation, pad_len, w_heads,
+               rel_bias};
   if (check_problem(&p)) return 1;
+  if (d_rel_bias && !rel_bias) return 1;
+  /* the bias gradient: one [w + 1] row per (b, h) (each (b, h) runs on one
+   * thread), summed over b in order at the end */
+  double* drb_bh = NULL;
+  if (d_rel_bias) {
+    drb_bh = (double*)calloc((size_t)B * H * (w + 1) + 1, sizeof(double));
+    if (!drb_bh) return 2;
+  }
   if (!dq || !dk || !dv || (G > 0 && (!dqg || !dkg || !dvg))) return 1;
   const size_t full = (size_t)B * H * n * d;
   memset(dq, 0, full * sizeof(double));
@@ -345,11 +380,19 @@ int lf_oracle_bwd(int dtype, const void* q, const void* k, const void* v,
       for (int64_t bh = 0; bh < (int64_t)B * H; ++bh)
         for (int32_t i = 0; i < n; ++i)
           one_row_bwd(&p, dout, (int32_t)(bh / H), (int32_t)(bh % H), i, keys, scores, dp, dq, dk,
-                      dv, dqg, dkg, dvg);
+                      dv, dqg, dkg, dvg, drb_bh ? drb_bh + bh * (w + 1) : NULL);
     }
     free(keys);
     free(scores);
     free(dp);
+  }
+  if (drb_bh) {
+    memset(d_rel_bias, 0, (size_t)H * (w + 1) * sizeof(double));
+    for (int32_t b = 0; b < B; ++b)
+      for (int32_t h = 0; h < H; ++h)
+        for (int32_t t = 0; t <= w; ++t)
+          d_rel_bias[(int64_t)h * (w + 1) + t] += drb_bh[((int64_t)b * H + h) * (w + 1) + t];
+    free(drb_bh);
   }
   return err;
 }
@@ -454,7 +497,7 @@ int32_t lf_oracle_attended(const int32_t* global_idx, int32_t G, int32_t B, int3
                            int32_t n, int32_t w, const int32_t* w_heads, const int32_t* dilation,
                            int32_t causal, const int32_t* pad_len, int32_t b, int32_t h, int32_t i,
                            int32_t* keys, int32_t* is_global_row) {
-  problem p = {ORC_F64, 0, 0, 0, 0, 0, 0, global_idx, G, B, H, n, 1, w, causal, dilation, pad_len, w_heads};
+  problem p = {ORC_F64, 0, 0, 0, 0, 0, 0, global_idx, G, B, H, n, 1, w, causal, dilation, pad_len, w_heads, NULL};
   if (check_problem(&p)) return -1;
   int g = 0;
   int32_t cnt = attended_set(&p, b, h, i, keys, &g);
@@ -471,7 +514,7 @@ int32_t lf_oracle_count_pairs(const int32_t* global_idx, int32_t G, int32_t B, i
                               int32_t n, int32_t w, const int32_t* w_heads, const int32_t* dilation,
                               int32_t causal, const int32_t* pad_len, int64_t* pairs,
                               int64_t* global_pairs) {
-  problem p = {ORC_F64, 0, 0, 0, 0, 0, 0, global_idx, G, B, H, n, 1, w, causal, dilation, pad_len, w_heads};
+  problem p = {ORC_F64, 0, 0, 0, 0, 0, 0, global_idx, G, B, H, n, 1, w, causal, dilation, pad_len, w_heads, NULL};
   if (check_problem(&p)) return -1;
   int64_t tot = 0, gtot = 0;
   int err = 0;

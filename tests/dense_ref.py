@@ -7,6 +7,9 @@ Pattern (velog.io/@lainshower/Longformer, section 3-1): band |j - i| <= w/2
 with dilation gaps, look-back only when causal (section 4.1), global tokens
 as full rows (scored with qg, kg, vg) and full columns, padding masked.
 w is one window for every head or a sequence with one per head (section 4.1).
+rel_bias: optional [H, w + 1] table added to the band keys' scores of
+ordinary rows at window step t (entry t + w/2), the T5-style position bias of
+the Memorizing Transformer notes.
 """
 import numpy as np
 
@@ -28,8 +31,19 @@ def masks(n, w, delta, causal, global_idx, L):
     return local, glob
 
 
+def bias_matrix(n, w, delta, causal, table):
+    """[n, n] additive bias: table[t + w/2] on the band at window step t, 0 elsewhere."""
+    i = np.arange(n)[:, None]
+    j = np.arange(n)[None, :]
+    off = j - i
+    half = w // 2
+    band = (off % delta == 0) & (off >= -delta * half) & (off <= (0 if causal else delta * half))
+    t = np.clip(off // delta + half, 0, w)
+    return np.where(band, np.asarray(table, dtype=np.float64)[t], 0.0)
+
+
 def attention(q, k, v, w, dilation, causal=False, pad_len=None, qg=None, kg=None, vg=None,
-              global_idx=()):
+              global_idx=(), rel_bias=None):
     q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
     B, H, n, d = q.shape
     out = np.zeros_like(q)
@@ -48,6 +62,10 @@ def attention(q, k, v, w, dilation, causal=False, pad_len=None, qg=None, kg=None
                 vv[g] = np.asarray(vg, dtype=np.float64)[b, h]
                 m[g] = glob[g]
             s = np.einsum("id,ijd->ij", qq, kk) / np.sqrt(d)
+            if rel_bias is not None:  # band keys of ordinary rows only
+                bm = bias_matrix(n, w, dilation[h], causal, rel_bias[h])
+                bm[list(global_idx)] = 0.0
+                s = s + bm
             s = np.where(m, s, -np.inf)
             rowmax = np.max(s, axis=1, keepdims=True)
             rowmax = np.where(np.isfinite(rowmax), rowmax, 0.0)

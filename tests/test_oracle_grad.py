@@ -9,7 +9,9 @@ other than the backward itself:
 - the full-attention limit against autograd through torch's
   scaled_dot_product_attention;
 - closed forms and invariants: w = 0 (out = v), constant values (no score
-  gradient), sum over keys of dk = 0 and of dv = sum of dout over the rows.
+  gradient), sum over keys of dk = 0 and of dv = sum of dout over the rows;
+- the relative position bias's gradient against central differences on
+  exactly representable float32 tables and against dense autograd.
 """
 import itertools
 import zlib
@@ -20,6 +22,7 @@ import torch
 
 import oracle
 from dense_ref import masks as dense_masks
+from dense_ref import bias_matrix
 
 
 def _problem(rng, B, H, n, d, G):
@@ -187,3 +190,86 @@ def test_bf16_inputs_decode_exactly():
     b = oracle.bwd(*(t[n].double() for n in ("q", "k", "v", "dout")), **pat)
     for name in a:
         np.testing.assert_array_equal(a[name], b[name])
+
+
+# ---------------------------------------------------------------- relative position bias
+BIAS_PATTERNS = [
+    dict(w=6, dilation=[1, 2], causal=False, pad_len=[0, 5], global_idx=[0, 9]),
+    dict(w=4, dilation=[3, 1], causal=True, pad_len=None, global_idx=[]),
+    dict(w=40, dilation=[1, 2], causal=False, pad_len=[2, 0], global_idx=[11]),
+]
+
+
+def _table(rng, H, w):
+    """A bias table on a 2^-10 grid, so that +- 2^-12 steps stay exact in float32."""
+    return np.round(rng.standard_normal((H, w + 1)) * 1024) / 1024
+
+
+@pytest.mark.parametrize("pi", range(len(BIAS_PATTERNS)))
+def test_bias_gradient_matches_central_differences(pi):
+    pat = BIAS_PATTERNS[pi]
+    rng = np.random.default_rng(300 + pi)
+    B, H, n, d = 2, 2, 23, 4
+    x = _problem(rng, B, H, n, d, len(pat["global_idx"]))
+    rb = _table(rng, H, pat["w"])
+    grads = oracle.bwd(x["q"], x["k"], x["v"], x["dout"], qg=x["qg"], kg=x["kg"], vg=x["vg"],
+                       rel_bias=rb.astype(np.float32), **pat)
+    u = rng.choice([-1.0, 1.0], size=rb.shape)
+    eps = 2.0 ** -12
+
+    def loss(sign):
+        t = (rb + sign * eps * u).astype(np.float32)
+        assert np.array_equal(t.astype(np.float64), rb + sign * eps * u)
+        out = oracle.fwd(x["q"], x["k"], x["v"], qg=x["qg"], kg=x["kg"], vg=x["vg"], rel_bias=t, **pat)
+        return float(np.sum(x["dout"] * out))
+
+    fd = (loss(1) - loss(-1)) / (2 * eps)
+    an = float(np.sum(grads["drel_bias"] * u))
+    assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (fd, an)
+
+
+@pytest.mark.parametrize("pi", range(len(BIAS_PATTERNS)))
+def test_bias_gradient_matches_dense_autograd(pi):
+    """Every gradient, the bias's included, against autograd through dense
+    masked attention with the bias matrix gathered from a leaf table."""
+    pat = BIAS_PATTERNS[pi]
+    gidx = pat["global_idx"]
+    rng = np.random.default_rng(400 + pi)
+    B, H, n, d = 2, 2, 23, 4
+    x = _problem(rng, B, H, n, d, len(gidx))
+    rb = _table(rng, H, pat["w"]).astype(np.float32)
+    grads = oracle.bwd(x["q"], x["k"], x["v"], x["dout"], qg=x["qg"], kg=x["kg"], vg=x["vg"], rel_bias=rb, **pat)
+    tx = {t: torch.tensor(a, requires_grad=(t != "dout")) for t, a in x.items()}
+    table = torch.tensor(rb.astype(np.float64), requires_grad=True)
+    rank = {g: r for r, g in enumerate(gidx)}
+    w, causal = pat["w"], pat["causal"]
+    rows = []
+    for b in range(B):
+        L = n - (pat["pad_len"][b] if pat["pad_len"] else 0)
+        heads = []
+        for h in range(H):
+            dl = pat["dilation"][h]
+            local, glob = dense_masks(n, w, dl, causal, gidx, L)
+            # the bias matrix as a gather from the leaf table (indices from the grids)
+            onehot = np.stack([bias_matrix(n, w, dl, causal, np.eye(w + 1)[t]) for t in range(w + 1)], -1)
+            bm = torch.tensor(onehot) @ table[h]
+            outs = []
+            for i in range(n):
+                if i in rank:
+                    qi, kk, vv, m, bi = tx["qg"][b, h, rank[i]], tx["kg"][b, h], tx["vg"][b, h], glob[i], 0.0
+                else:
+                    qi, kk, vv, m, bi = tx["q"][b, h, i], tx["k"][b, h], tx["v"][b, h], local[i], bm[i]
+                m = torch.as_tensor(m)
+                if not bool(m.any()):
+                    outs.append(torch.zeros(d, dtype=torch.float64))
+                    continue
+                s = (kk @ qi) / np.sqrt(d) + bi
+                s = torch.where(m, s, torch.tensor(float("-inf"), dtype=torch.float64))
+                outs.append(torch.softmax(s, dim=0) @ vv)
+            heads.append(torch.stack(outs))
+        rows.append(torch.stack(heads))
+    out = torch.stack(rows)
+    (out * tx["dout"]).sum().backward()
+    np.testing.assert_allclose(grads["drel_bias"], table.grad.numpy(), atol=1e-12, rtol=0)
+    for t in ("q", "k", "v") + (("qg", "kg", "vg") if gidx else ()):
+        np.testing.assert_allclose(grads["d" + t], tx[t].grad.numpy(), atol=1e-12, rtol=0, err_msg=t)

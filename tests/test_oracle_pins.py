@@ -318,3 +318,86 @@ def test_rejects_invalid_patterns():
         oracle.fwd(z, z, z, w=2, dilation=[0])
     with pytest.raises(ValueError):
         oracle.fwd(z, z, z, w=2, dilation=[1], qg=np.zeros((1, 1, 2, 2)), kg=z, vg=z, global_idx=[2, 1])
+
+
+# ---------------------------------------------------------------- relative position bias
+BIAS_CASES = [  # n, d, w, dilation, causal, global_idx, pad_len
+    (40, 8, 6, [1, 2], False, [], None),
+    (64, 4, 10, [1, 3], True, [0, 33], [0, 9]),
+    (50, 8, 8, [2, 1], False, [5, 6, 49], [7, 0]),
+    (30, 2, 100, [1, 1], False, [0], None),      # the window reaches past both ends
+    (33, 5, 0, [1, 2], True, [2], [0, 3]),
+]
+
+
+@pytest.mark.parametrize("case", BIAS_CASES, ids=str)
+def test_relative_bias_matches_dense_mask(case):
+    """The T5-style bias (Memorizing Transformer notes, "Position bias"),
+    read as one scalar per head and window step added to the band keys'
+    scores, against the dense mask with the bias matrix built from index
+    grids; global columns outside the band and global rows get none."""
+    n, d, w, dil, causal, gidx, pads = case
+    rng = np.random.default_rng(n + 10 * w + causal)
+    B, H = 2, len(dil)
+    q, k, v, qg, kg, vg = _rand_problem(rng, B, H, n, d, len(gidx))
+    rb = rng.standard_normal((H, w + 1)).astype(np.float32) * 2
+    got = oracle.fwd(q, k, v, w=w, dilation=dil, causal=causal, pad_len=pads, qg=qg, kg=kg, vg=vg,
+                     global_idx=gidx, rel_bias=rb)
+    want = dense_attention(q, k, v, w, dil, causal, pads, qg, kg, vg, gidx, rel_bias=rb)
+    np.testing.assert_allclose(got, want, atol=1e-12, rtol=0)
+
+
+def test_relative_bias_zero_table_is_no_bias():
+    rng = np.random.default_rng(3)
+    q, k, v, qg, kg, vg = _rand_problem(rng, 1, 2, 70, 8, 2)
+    kw = dict(w=12, dilation=[1, 2], causal=False, qg=qg, kg=kg, vg=vg, global_idx=[0, 40])
+    np.testing.assert_array_equal(oracle.fwd(q, k, v, **kw),
+                                  oracle.fwd(q, k, v, rel_bias=np.zeros((2, 13), np.float32), **kw))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_relative_bias_constant_shift_cancels_without_globals(causal):
+    """Softmax is invariant to a constant added to every score of a row: a
+    table holding one value changes nothing when every key is a band key."""
+    rng = np.random.default_rng(4 + causal)
+    q, k, v = (rng.standard_normal((2, 3, 80, 8)) for _ in range(3))
+    kw = dict(w=16, dilation=[1, 2, 5], causal=causal, pad_len=[0, 13])
+    base = oracle.fwd(q, k, v, **kw)
+    shifted = oracle.fwd(q, k, v, rel_bias=np.full((3, 17), 3.25, np.float32), **kw)
+    np.testing.assert_allclose(shifted, base, atol=1e-12, rtol=0)
+
+
+def test_relative_bias_peaked_at_the_token_returns_its_value():
+    """A bias of +80 at step 0 and 0 elsewhere: each row's weight on itself is
+    1 - O(w e^-80), so the output is the row's own value."""
+    rng = np.random.default_rng(5)
+    q, k, v = (rng.standard_normal((1, 2, 60, 8)) * 0.1 for _ in range(3))
+    rb = np.zeros((2, 9), np.float32)
+    rb[:, 4] = 80.0
+    out = oracle.fwd(q, k, v, w=8, dilation=[1, 3], rel_bias=rb)
+    np.testing.assert_allclose(out, v, atol=1e-30 + 1e-12, rtol=0)
+
+
+def test_relative_bias_steps_index_the_table():
+    """One row by hand: with q = 0 every score is its bias, so the weights are
+    softmax(bias over the row's window steps) and the output their average of
+    v.  Row 10 of a dilation-2 head with w = 4 reads keys 6, 8, 10, 12, 14 at
+    steps -2..2, i.e. table entries 0..4."""
+    n, d = 20, 3
+    q = np.zeros((1, 1, n, d))
+    k = np.ones((1, 1, n, d))
+    v = np.arange(n * d, dtype=np.float64).reshape(1, 1, n, d)
+    table = np.array([[0.5, -1.0, 2.0, 0.25, 1.5]], np.float32)
+    out = oracle.fwd(q, k, v, w=4, dilation=[2], rel_bias=table)
+    wts = np.exp(table[0].astype(np.float64))
+    wts /= wts.sum()
+    want = sum(wt * v[0, 0, j] for wt, j in zip(wts, [6, 8, 10, 12, 14]))
+    np.testing.assert_allclose(out[0, 0, 10], want, rtol=1e-14, atol=0)
+
+
+def test_relative_bias_rejected_shapes():
+    z = np.zeros((1, 2, 8, 2))
+    with pytest.raises(ValueError):
+        oracle.fwd(z, z, z, w=4, dilation=[1, 1], rel_bias=np.zeros((2, 4), np.float32))
+    with pytest.raises(ValueError):
+        oracle.fwd(z, z, z, w=[4, 4], dilation=[1, 1], rel_bias=np.zeros((2, 5), np.float32))
