@@ -173,6 +173,61 @@ lf_status lf_attn_bwd_f32(const void* q, const void* k, const void* v,
                           const int32_t* pad_len, cudaStream_t stream);
 
 /*
+ * Relative position bias (Memorizing Transformer notes, "Position bias": a
+ * T5-style bias added to the attention scores, one learned scalar per head
+ * and relative position): as lf_attn_fwd / lf_attn_fwd_f32, with
+ *   score(i, j) = <q_i, k_j> / sqrt(d) + rel_bias[h * (w + 1) + t + w/2]
+ * for every key j in row i's band, t = (j - i) / dilation[h] in [-w/2, w/2]
+ * its window step (causal rows read t <= 0 only).  Global columns outside
+ * the band and the global tokens' own rows carry no bias.  A bucketed bias
+ * (T5's log-spaced buckets of the token distance |j - i|) is passed expanded
+ * into this table.  rel_bias: fp32 DEVICE memory [H, w + 1], 4-byte
+ * aligned, not overlapping `out`; NULL only for an empty problem.
+ * bf16 d = 64 runs the ring kernel whatever the number of global tokens;
+ * d = 128 the pair kernel; fp32 the CUDA-core kernel.  Errors as in the
+ * calls they extend.
+ */
+lf_status lf_attn_fwd_bias(const void* q, const void* k, const void* v,
+                           const void* qg, const void* kg, const void* vg,
+                           const int32_t* global_idx, int32_t n_global, void* out,
+                           int32_t B, int32_t H, int32_t n, int32_t d, int32_t w,
+                           const int32_t* dilation, int32_t causal, const int32_t* pad_len,
+                           const float* rel_bias, cudaStream_t stream);
+lf_status lf_attn_fwd_bias_f32(const void* q, const void* k, const void* v,
+                               const void* qg, const void* kg, const void* vg,
+                               const int32_t* global_idx, int32_t n_global, void* out,
+                               int32_t B, int32_t H, int32_t n, int32_t d, int32_t w,
+                               const int32_t* dilation, int32_t causal, const int32_t* pad_len,
+                               const float* rel_bias, cudaStream_t stream);
+
+/*
+ * Backward with the relative position bias: as lf_attn_bwd / lf_attn_bwd_f32
+ * for the scores of lf_attn_fwd_bias, plus the bias's own gradient
+ *   d_rel_bias[h * (w + 1) + t + w/2] = sum over the batch rows and the band
+ *   entries (i, j) of head h at window step t of dL/dscore(i, j)
+ * (entries no band entry reaches are 0).  d_rel_bias: fp32 DEVICE memory
+ * [H, w + 1], 4-byte aligned, overlapping nothing else, or NULL to skip it;
+ * it is written in full (summed in a fixed order: bitwise reproducible).
+ * With d_rel_bias, w <= 4096 (LF_ERR_UNSUPPORTED otherwise); its partial
+ * sums take B*H*ceil(n/64)*(w + 1)*4 bytes of stream-ordered scratch per
+ * block of 256 batch rows and 256 heads.
+ */
+lf_status lf_attn_bwd_bias(const void* q, const void* k, const void* v,
+                           const void* qg, const void* kg, const void* vg,
+                           const int32_t* global_idx, int32_t n_global, const void* dout,
+                           float* dq, float* dk, float* dv, float* dqg, float* dkg, float* dvg,
+                           int32_t B, int32_t H, int32_t n, int32_t d, int32_t w,
+                           const int32_t* dilation, int32_t causal, const int32_t* pad_len,
+                           const float* rel_bias, float* d_rel_bias, cudaStream_t stream);
+lf_status lf_attn_bwd_bias_f32(const void* q, const void* k, const void* v,
+                               const void* qg, const void* kg, const void* vg,
+                               const int32_t* global_idx, int32_t n_global, const void* dout,
+                               float* dq, float* dk, float* dv, float* dqg, float* dkg, float* dvg,
+                               int32_t B, int32_t H, int32_t n, int32_t d, int32_t w,
+                               const int32_t* dilation, int32_t causal, const int32_t* pad_len,
+                               const float* rel_bias, float* d_rel_bias, cudaStream_t stream);
+
+/*
  * Per-head windows (velog.io/@lainshower/Longformer, section 4.1: the window
  * size is chosen per layer, and within a layer heads differ, some dilated and
  * some not): as lf_attn_fwd / lf_attn_fwd_f32 / lf_attn_bwd / lf_attn_bwd_f32,

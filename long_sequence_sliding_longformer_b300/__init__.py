@@ -55,6 +55,14 @@ def load():
         fn = getattr(lib, name)
         fn.argtypes = bwd_args
         fn.restype = ctypes.c_int
+    for name in ("lf_attn_fwd_bias", "lf_attn_fwd_bias_f32"):
+        fn = getattr(lib, name)
+        fn.argtypes = fwd_args[:-1] + [P, P]
+        fn.restype = ctypes.c_int
+    for name in ("lf_attn_bwd_bias", "lf_attn_bwd_bias_f32"):
+        fn = getattr(lib, name)
+        fn.argtypes = bwd_args[:-1] + [P, P, P]
+        fn.restype = ctypes.c_int
     # per-head windows: the w argument becomes a host array
     for name, args, at in (("lf_attn_fwd_hw", fwd_args, 13), ("lf_attn_fwd_hw_f32", fwd_args, 13),
                            ("lf_attn_bwd_hw", bwd_args, 19), ("lf_attn_bwd_hw_f32", bwd_args, 19)):
@@ -103,6 +111,11 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
+def _check_table(t: torch.Tensor, H: int, w: int, name: str):
+    if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous() or tuple(t.shape) != (H, w + 1):
+        raise ValueError("%s must be a contiguous fp32 CUDA tensor of shape (%d, %d)" % (name, H, w + 1))
+
+
 def _window(w, H: int):
     """w as one int (every head) or one int per head: (the call's w
     argument, whether it is the per-head array)."""
@@ -119,9 +132,12 @@ def attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, w,
          pad_len: Optional[Sequence[int]] = None, qg: Optional[torch.Tensor] = None,
          kg: Optional[torch.Tensor] = None, vg: Optional[torch.Tensor] = None,
          global_idx: Sequence[int] = (), out: Optional[torch.Tensor] = None,
+         rel_bias: Optional[torch.Tensor] = None,
          stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """Sliding / dilated / causal window attention with global tokens.  w is
-    the window of every head, or a sequence of one window per head."""
+    the window of every head, or a sequence of one window per head.
+    rel_bias: optional fp32 CUDA tensor [H, w + 1], added to the band keys'
+    scores at window step t (entry t + w/2); needs one w for every head."""
     lib = load()
     if q.dim() != 4:
         raise ValueError("q must be [B, H, n, d]")
@@ -154,12 +170,21 @@ def attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, w,
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
     warg, per_head = _window(w, H)
     bf = q.dtype == torch.bfloat16
-    fn = (lib.lf_attn_fwd_hw if bf else lib.lf_attn_fwd_hw_f32) if per_head else \
-        (lib.lf_attn_fwd if bf else lib.lf_attn_fwd_f32)
+    extra = []
+    if rel_bias is not None:
+        if per_head:
+            raise ValueError("a relative bias takes one window for every head")
+        _check_table(rel_bias, H, warg, "rel_bias")
+        fn = lib.lf_attn_fwd_bias if bf else lib.lf_attn_fwd_bias_f32
+        extra = [rel_bias.data_ptr()]
+    elif per_head:
+        fn = lib.lf_attn_fwd_hw if bf else lib.lf_attn_fwd_hw_f32
+    else:
+        fn = lib.lf_attn_fwd if bf else lib.lf_attn_fwd_f32
     with torch.cuda.device(q.device):
         _check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr(qg) if G else None,
                   _ptr(kg) if G else None, _ptr(vg) if G else None, gidx, G, out.data_ptr(),
-                  B, H, n, d, warg, dil, int(bool(causal)), pads, s.cuda_stream))
+                  B, H, n, d, warg, dil, int(bool(causal)), pads, *extra, s.cuda_stream))
     return out
 
 
@@ -181,10 +206,11 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dout: torch.Tens
              pad_len: Optional[Sequence[int]] = None, qg: Optional[torch.Tensor] = None,
              kg: Optional[torch.Tensor] = None, vg: Optional[torch.Tensor] = None,
              global_idx: Sequence[int] = (), grads: Optional[dict] = None,
+             rel_bias: Optional[torch.Tensor] = None,
              stream: Optional[torch.cuda.Stream] = None) -> dict:
     """Gradients of sum(dout * attn(...)): a dict of fp32 tensors dq, dk, dv
-    and, with global tokens, dqg, dkg, dvg (preallocated ones may be passed in
-    `grads`)."""
+    and, with global tokens, dqg, dkg, dvg, and with rel_bias its gradient
+    drel_bias [H, w + 1] (preallocated ones may be passed in `grads`)."""
     lib = load()
     if q.dim() != 4:
         raise ValueError("q must be [B, H, n, d]")
@@ -204,9 +230,11 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dout: torch.Tens
         if tuple(t.shape) != want:
             raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), want))
     names = ["dq", "dk", "dv"] + (["dqg", "dkg", "dvg"] if G else [])
+    if rel_bias is not None:
+        names.append("drel_bias")
     g = dict(grads) if grads else {}
     for name in names:
-        want = (B, H, G, d) if name == "dqg" else (B, H, n, d)
+        want = (B, H, G, d) if name == "dqg" else (H, int(w) + 1) if name == "drel_bias" else (B, H, n, d)
         if name not in g:
             g[name] = torch.empty(want, dtype=torch.float32, device=q.device)
         t = g[name]
@@ -222,14 +250,23 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dout: torch.Tens
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
     warg, per_head = _window(w, H)
     bf = q.dtype == torch.bfloat16
-    fn = (lib.lf_attn_bwd_hw if bf else lib.lf_attn_bwd_hw_f32) if per_head else \
-        (lib.lf_attn_bwd if bf else lib.lf_attn_bwd_f32)
     gp = lambda name: _ptr(g[name]) if name in g else None
+    extra = []
+    if rel_bias is not None:
+        if per_head:
+            raise ValueError("a relative bias takes one window for every head")
+        _check_table(rel_bias, H, warg, "rel_bias")
+        fn = lib.lf_attn_bwd_bias if bf else lib.lf_attn_bwd_bias_f32
+        extra = [rel_bias.data_ptr(), gp("drel_bias")]
+    elif per_head:
+        fn = lib.lf_attn_bwd_hw if bf else lib.lf_attn_bwd_hw_f32
+    else:
+        fn = lib.lf_attn_bwd if bf else lib.lf_attn_bwd_f32
     with torch.cuda.device(q.device):
         _check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr(qg) if G else None,
                   _ptr(kg) if G else None, _ptr(vg) if G else None, gidx, G, dout.data_ptr(),
                   gp("dq"), gp("dk"), gp("dv"), gp("dqg"), gp("dkg"), gp("dvg"),
-                  B, H, n, d, warg, dil, int(bool(causal)), pads, s.cuda_stream))
+                  B, H, n, d, warg, dil, int(bool(causal)), pads, *extra, s.cuda_stream))
     return {name: g[name] for name in names}
 
 

@@ -52,7 +52,17 @@ struct BwdParams {
   int32_t gidx[kMaxGlobal];
   int32_t dil[kMaxHeadsSimt];
   int32_t half_h[kMaxHeadsSimt];  // window reach per head in class steps: back half_h, ahead causal ? 0 : half_h
+  // Relative position bias: rel_bias[(h0 + h) * rb_stride + rb_half + t] is
+  // added to the scaled score of a band key at window step t (nullptr: none).
+  // drb_part (nullptr: no bias gradient): per tile of the keys pass, the
+  // rb_stride sums of ds by window step.
+  const float* rel_bias;
+  int32_t rb_stride, rb_half;
+  float* drb_part;
 };
+
+// Largest window whose bias gradient the keys pass accumulates in shared memory.
+constexpr int kMaxBiasW = 4096;
 
 __device__ __forceinline__ float ldf(const float* p) { return __ldg(p); }
 __device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
@@ -238,6 +248,8 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 1 : 2) bwd_rows_tiled(Bwd
   const int nband = khi >= klo ? (khi - klo + 1 + kKC - 1) / kKC : 0;
   const int nglob = (p.G + kKC - 1) / kKC;
   const int nchunks = nband + nglob;
+  // the bias of this head, indexed by window step
+  const float* brow = p.rel_bias ? p.rel_bias + (int64_t)(p.h0 + t.h) * p.rb_stride + p.rb_half : nullptr;
 
   // the key (position) of chunk column kk, or -1 (also for a global token in
   // the padding: it is staged as zeros, so that whatever it holds cannot reach
@@ -291,12 +303,21 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 1 : 2) bwd_rows_tiled(Bwd
 #pragma unroll
       for (int i = 0; i < 4; ++i) att[i][j] = attends(4 * ty + i, c, key);
     }
+    // scores in the exp2 domain, with the bias on the band keys
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        s[i][j] *= p.sl2;
+        if (p.rel_bias && c < nband && att[i][j])
+          s[i][j] += __ldg(brow + (klo + c * kKC + tx + 16 * j) - (t.m0 + 4 * ty + i)) * kLog2e;
+      }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       float cm = -INFINITY;
 #pragma unroll
       for (int j = 0; j < 2; ++j)
-        if (att[i][j]) cm = fmaxf(cm, s[i][j] * p.sl2);
+        if (att[i][j]) cm = fmaxf(cm, s[i][j]);
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
       if (cm > mx[i]) {
@@ -314,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 1 : 2) bwd_rows_tiled(Bwd
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         float e = 0.f;
-        if (att[i][j]) e = exp2f(s[i][j] * p.sl2 - mx[i]);
+        if (att[i][j]) e = exp2f(s[i][j] - mx[i]);
         ls[i] += e;
         as[i] = fmaf(e, dp[i][j], as[i]);
         Es[row * (kKC + 1) + tx + 16 * j] = e;
@@ -419,6 +440,7 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 1 : 2) bwd_keys_tiled(Bwd
   float* cD = cl + kKC;               // per chunk row: D
   int* crow = reinterpret_cast<int*>(cD + kKC);  // per chunk row: position or -1
   int* kpos = crow + kKC;                       // per key: position if valid (< L), else -1
+  float* bacc = reinterpret_cast<float*>(kpos + kTR);  // bias gradient by window step (drb_part only)
 
   const Tile t = tile_of(p, blockIdx.x);
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
@@ -432,6 +454,9 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 1 : 2) bwd_keys_tiled(Bwd
     const int m = t.m0 + a;
     kpos[a] = (m <= t.mlast) ? t.r + t.delta * m : -1;
   }
+  if (p.drb_part)
+    for (int u = tid; u < p.rb_stride; u += kThreads) bacc[u] = 0.f;
+  const float* brow = p.rel_bias ? p.rel_bias + (int64_t)(p.h0 + t.h) * p.rb_stride + p.rb_half : nullptr;
   __syncthreads();
   stage_rows<T, D, kTR>(Ks, kb, d, [&](int a) { return kpos[a]; });
   stage_rows<T, D, kTR>(Vs, vb, d, [&](int a) { return kpos[a]; });
@@ -477,7 +502,9 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 1 : 2) bwd_keys_tiled(Bwd
         const int off = (t.m0 + a) - mr;  // key offset from the row, in class steps
         float pv = 0.f, ds = 0.f;
         if (i >= 0 && kpos[a] >= 0 && off >= -t.half && off <= t.right) {
-          pv = exp2f(s[a4][j] * p.sl2 - cl[rr]);
+          float s2 = s[a4][j] * p.sl2;
+          if (brow) s2 += __ldg(brow + off) * kLog2e;
+          pv = exp2f(s2 - cl[rr]);
           ds = pv * (dp[a4][j] - cD[rr]);
         }
         Ps[a * (kKC + 1) + rr] = pv;
@@ -485,6 +512,20 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 1 : 2) bwd_keys_tiled(Bwd
       }
     }
     __syncthreads();
+    if (p.drb_part) {
+      // the bias gradient: ds summed along the chunk's diagonals, on which
+      // the window step (key - row) is constant; one thread per diagonal,
+      // rows in order
+      const int o0 = t.m0 - (rlo + c * kKC);  // the step at key 0, chunk row 0
+      for (int u = tid; u < kTR + kKC - 1; u += kThreads) {
+        const int dl = u - (kKC - 1);  // key - chunk row
+        const int o = o0 + dl;
+        if (o < -t.half || o > t.right) continue;
+        float sum = 0.f;
+        for (int rr = max(0, -dl); rr < kKC && rr + dl < kTR; ++rr) sum += dSs[(rr + dl) * (kKC + 1) + rr];
+        bacc[o + p.rb_half] += sum;
+      }
+    }
 #pragma unroll 4
     for (int rr = 0; rr < kKC; ++rr) {
       float dov[CPT], qv[CPT];
@@ -505,6 +546,10 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 1 : 2) bwd_keys_tiled(Bwd
       }
     }
   }
+  if (p.drb_part) {
+    __syncthreads();
+    for (int u = tid; u < p.rb_stride; u += kThreads) p.drb_part[(int64_t)blockIdx.x * p.rb_stride + u] = bacc[u];
+  }
   // write dk, dv for every class position of the tile (zeros past the valid length)
 #pragma unroll
   for (int a4 = 0; a4 < 4; ++a4) {
@@ -523,6 +568,20 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 1 : 2) bwd_keys_tiled(Bwd
       }
     }
   }
+}
+
+// ---------------------------------------------------------------- bias_reduce
+// drb[h0 + h][o] += the keys pass's partial sums of head h at step entry o,
+// over the launch's batch rows and the head's tiles, in order (block y = h).
+__global__ void bwd_bias_reduce(BwdParams p, float* __restrict__ drb) {
+  const int h = blockIdx.y;
+  const int o = blockIdx.x * blockDim.x + threadIdx.x;
+  if (o >= p.rb_stride) return;
+  float sum = 0.f;
+  for (int b = 0; b < p.B; ++b)
+    for (int tl = p.head_tile_off[h]; tl < p.head_tile_off[h + 1]; ++tl)
+      sum += p.drb_part[((int64_t)b * p.tiles_b + tl) * p.rb_stride + o];
+  drb[(int64_t)(p.h0 + h) * p.rb_stride + o] += sum;
 }
 
 // ---------------------------------------------------------------- grows

@@ -581,6 +581,18 @@ __device__ __forceinline__ float chunk_max(const uint32_t (&x)[32], uint32_t kee
   return fmaxf(max3f(a, b, v[28]), max3f(c, d, max3f(v[29], v[30], v[31])));
 }
 
+// Relative position bias of a 32-column chunk, in place: x <- x * sl2 +
+// bias(t0 + t) * log2(e) for t = 0..31 (the scores' exp2 domain).  The step
+// is clamped to the table [tlo, thi]; a clamped column is masked anyway.
+__device__ __forceinline__ void chunk_bias(uint32_t (&x)[32], float sl2, const float* brow, int t0, int tlo,
+                                           int thi) {
+#pragma unroll
+  for (int t = 0; t < 32; ++t) {
+    const int st = min(max(t0 + t, tlo), thi);
+    x[t] = __float_as_uint(fmaf(__uint_as_float(x[t]), sl2, __ldg(brow + st) * kLog2e));
+  }
+}
+
 // P for a 32-column chunk: p = exp2(s * sl2 - m) on the kept columns, 0
 // elsewhere, packed to bf16 pairs; returns the two partial row sums.
 __device__ __forceinline__ float2 chunk_exp(const uint32_t (&x)[32], uint32_t keep, uint32_t whole,
@@ -605,7 +617,8 @@ __device__ __forceinline__ float2 chunk_exp(const uint32_t (&x)[32], uint32_t ke
 }
 
 // Softmax of tile X (one query row per thread; warp quarter wq of TMEM lanes).
-template <int D>
+// kB: the band entries' scores carry the relative position bias.
+template <int D, bool kB>
 __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_t tmem, int X,
                              int wq, int lane) {
   using C = BandCfg<D>;
@@ -674,9 +687,13 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
       if (!ok || !iss.issue_s(it, kv, qb, entry(0), len == 1)) { ok = false; break; }
     }
     float m_run = NEG_INF, l_run = 0.f;
+    // the bias of this row's head, indexed by window step
+    const float* brow = kB ? p.rel_bias + (size_t)it.h * p.rb_stride + p.rb_half : nullptr;
 
     for (int j = 0; j < len; ++j) {
       const bool is_band = j < nb;
+      // with the bias, pass 1 writes the band scores back scaled and biased
+      const bool scaled = kB && is_band;
       const int e = entry(j);
       // ---- keep c: bit t set where this row attends column 32c + t
       uint32_t keep0, keep1, keep2, keep3;
@@ -724,9 +741,15 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
         tmem_wait_ld();
         reg_fence32(x);
         const uint32_t kc = c == 0 ? keep0 : c == 1 ? keep1 : c == 2 ? keep2 : keep3;
+        if (scaled) {
+          chunk_bias(x, sl2, brow, it.U0 + 128 * e + 32 * c - m_q, -p.rb_half, p.rb_stride - 1 - p.rb_half);
+          tmem_st16_nw(tS + 32 * c, x);
+          tmem_st16_nw(tS + 32 * c + 16, x + 16);
+        }
         mx = fmaxf(mx, chunk_max(x, kc, (fullm >> c) & 1u));
       }
-      const float mt = mx * sl2;
+      if (scaled) tmem_wait_st();  // pass 2 reads the biased scores back
+      const float mt = scaled ? mx : mx * sl2;
       tr.ev(3);
       float alpha = 1.f;
       bool resc = false;
@@ -764,7 +787,7 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
           tmem_wait_ld();
           reg_fence32(x);
           const uint32_t kc = c == 0 ? keep0 : c == 1 ? keep1 : c == 2 ? keep2 : keep3;
-          sum2 = __fadd2_rn(sum2, chunk_exp(x, kc, (fullm >> c) & 1u, sl2, mneg, pk));
+          sum2 = __fadd2_rn(sum2, chunk_exp(x, kc, (fullm >> c) & 1u, scaled ? 1.f : sl2, mneg, pk));
         } else {
 #pragma unroll
           for (int t = 0; t < 16; ++t) pk[t] = 0u;
@@ -853,7 +876,7 @@ constexpr int kRegsSoftmax = 200;
 constexpr int kRegsOther = 96;
 constexpr int kRegsAtLaunchMin = (256 * kRegsSoftmax + 128 * kRegsOther + kBandThreads - 1) / kBandThreads;
 
-template <int D>
+template <int D, bool kB>
 __global__ void __launch_bounds__(kBandThreads, 1) band_tc_kernel(const __grid_constant__ BandParams p) {
   using C = BandCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -904,7 +927,7 @@ __global__ void __launch_bounds__(kBandThreads, 1) band_tc_kernel(const __grid_c
 
   if (warp >= 4) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-    band_softmax<D>(p, sm, tmem, (warp >> 2) - 1, warp & 3, lane);
+    band_softmax<D, kB>(p, sm, tmem, (warp >> 2) - 1, warp & 3, lane);
   } else {
     // the issuing warps are the oldest of the CTA: the schedulers favour them
     // over the busy softmax warps that share their sub-partitions
@@ -924,12 +947,12 @@ __global__ void __launch_bounds__(kBandThreads, 1) band_tc_kernel(const __grid_c
   }
 }
 
-template <int D>
+template <int D, bool kB>
 static lf_status launch_band_tc_d(const BandParams& p, int grid, cudaStream_t s) {
   using C = BandCfg<D>;
   static std::atomic<uint64_t> attr_done{0};
   static std::atomic<bool> regs_checked{false};
-  lf_status st = smem_attr_once((const void*)band_tc_kernel<D>, C::kSmem, attr_done, "band kernel");
+  lf_status st = smem_attr_once((const void*)band_tc_kernel<D, kB>, C::kSmem, attr_done, "band kernel");
   if (st != LF_OK) return st;
   if (!regs_checked.load(std::memory_order_acquire)) {
     cudaError_t e;
@@ -937,7 +960,7 @@ static lf_status launch_band_tc_d(const BandParams& p, int grid, cudaStream_t s)
     // it was planned for; with fewer registers setmaxnreg.inc could never be
     // satisfied, so refuse to launch rather than wait.
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, band_tc_kernel<D>);
+    e = cudaFuncGetAttributes(&fa, band_tc_kernel<D, kB>);
     if (e != cudaSuccess) {
       set_error("cudaFuncGetAttributes(band kernel): %s", cudaGetErrorString(e));
       return LF_ERR_CUDA;
@@ -949,7 +972,7 @@ static lf_status launch_band_tc_d(const BandParams& p, int grid, cudaStream_t s)
     }
     regs_checked.store(true, std::memory_order_release);
   }
-  band_tc_kernel<D><<<grid, kBandThreads, C::kSmem, s>>>(p);
+  band_tc_kernel<D, kB><<<grid, kBandThreads, C::kSmem, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("band kernel launch: %s", cudaGetErrorString(e));
@@ -960,7 +983,9 @@ static lf_status launch_band_tc_d(const BandParams& p, int grid, cudaStream_t s)
 }
 
 // D = 128 only (D = 64 runs the ring kernel of band_ring.cuh).
-inline lf_status launch(const BandParams& p, int grid, cudaStream_t s) { return launch_band_tc_d<128>(p, grid, s); }
+inline lf_status launch(const BandParams& p, int grid, cudaStream_t s) {
+  return p.rel_bias ? launch_band_tc_d<128, true>(p, grid, s) : launch_band_tc_d<128, false>(p, grid, s);
+}
 
 }  // namespace pairk
 }  // namespace lf

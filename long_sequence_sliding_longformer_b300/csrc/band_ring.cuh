@@ -692,7 +692,8 @@ __device__ __forceinline__ float exp32(const uint32_t* x, float sl2, float mneg,
 }
 
 // Softmax and epilogue (one query row per thread; warp quarter wq of TMEM lanes).
-template <int D, bool kG>
+// kB: the band entries' scores carry the relative position bias.
+template <int D, bool kG, bool kB>
 __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_t tmem, int wq, int lane) {
   using C = BandCfg<D>;
   static_assert(C::kE == 64 || C::kE == 128, "the softmax holds one entry in registers");
@@ -737,6 +738,8 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
       continue;
     }
     float m_run = NEG_INF, l_run = 0.f;
+    // the bias of this row's head, indexed by window step
+    const float* brow = kB ? p.rel_bias + (size_t)it.h * p.rb_stride + p.rb_half : nullptr;
     // Band entries e in [e_all0, e_all1] are attended whole by every row of
     // this warp, those outside [e_any0, e_any1] by none of them (the rows'
     // windows together span keys [mw - half, min(mw_last + right, Lm - 1)]).
@@ -830,11 +833,24 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
 #pragma unroll
           for (int c = 0; c < NC; ++c) mask32(x + 32 * c, keep[c]);
         }
+        if (kB && e < it.nU) {
+          // scores -> s * scale * log2(e) + bias * log2(e); masked columns stay
+          // -inf (their clamped table index is never used)
+          const int t0 = it.U0 + C::kE * e - m_q;  // window step of column 0
+          const int tmax = p.rb_stride - 1 - p.rb_half;
+#pragma unroll
+          for (int c = 0; c < C::kE; ++c) {
+            const int t = min(max(t0 + c, -p.rb_half), tmax);
+            x[c] = __float_as_uint(fmaf(__uint_as_float(x[c]), sl2, __ldg(brow + t) * kLog2e));
+          }
+        }
         mx = max64(x);  // row maximum of the raw scores (the scale is positive)
         if (NC == 4) mx = fmaxf(mx, max64(x + 64));
       }
       pf.lap(4);
-      const float mt = mx * sl2;
+      // with the bias the band entries' scores are already scaled
+      const bool scaled = kB && e < it.nU;
+      const float mt = scaled ? mx : mx * sl2;
       float alpha = 1.f;
       bool resc = false;
       if (mt > m_run + kLazy) {
@@ -853,7 +869,7 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
         float l = 0.f;
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
-          l += exp32(x + 32 * c, sl2, mneg, pk);
+          l += exp32(x + 32 * c, scaled ? 1.f : sl2, mneg, pk);
           tmem_st16_nw(tS + 16 * c, pk);  // P chunk c over columns [16c, 16c + 16) (already read)
         }
         l_run = l_run * alpha + l;
@@ -934,7 +950,7 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
 
 constexpr int kBandThreads = 256;
 
-template <int D, bool kG>
+template <int D, bool kG, bool kB>
 __global__ void __launch_bounds__(kBandThreads, BandCfg<D>::kCtaPerSm)
     band_tc_kernel(const __grid_constant__ BandParams p) {
   using C = BandCfg<D>;
@@ -983,7 +999,7 @@ __global__ void __launch_bounds__(kBandThreads, BandCfg<D>::kCtaPerSm)
   const uint32_t tmem = *sm.tmem_holder();
 
   if (warp >= 4) {
-    band_softmax<D, kG>(p, sm, tmem, warp & 3, lane);
+    band_softmax<D, kG, kB>(p, sm, tmem, warp & 3, lane);
   } else if (warp == 0) {
     band_mma<D, kG>(p, sm, tmem);
   } else if (warp == 1) {
@@ -1000,13 +1016,13 @@ __global__ void __launch_bounds__(kBandThreads, BandCfg<D>::kCtaPerSm)
   }
 }
 
-template <int D, bool kG>
+template <int D, bool kG, bool kB>
 static lf_status launch_band_tc_d(const BandParams& p, int grid, cudaStream_t s) {
   using C = BandCfg<D>;
   static std::atomic<uint64_t> attr_done{0};
-  lf_status st = smem_attr_once((const void*)band_tc_kernel<D, kG>, C::kSmem, attr_done, "band kernel");
+  lf_status st = smem_attr_once((const void*)band_tc_kernel<D, kG, kB>, C::kSmem, attr_done, "band kernel");
   if (st != LF_OK) return st;
-  band_tc_kernel<D, kG><<<grid, kBandThreads, C::kSmem, s>>>(p);
+  band_tc_kernel<D, kG, kB><<<grid, kBandThreads, C::kSmem, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("band kernel launch: %s", cudaGetErrorString(e));
@@ -1020,7 +1036,8 @@ static lf_status launch_band_tc_d(const BandParams& p, int grid, cudaStream_t s)
 // Global-row mode (p.gmode) is a separate instantiation, so that the band
 // path carries none of its code.
 inline lf_status launch(const BandParams& p, int grid, cudaStream_t s) {
-  return p.gmode ? launch_band_tc_d<64, true>(p, grid, s) : launch_band_tc_d<64, false>(p, grid, s);
+  if (p.gmode) return launch_band_tc_d<64, true, false>(p, grid, s);
+  return p.rel_bias ? launch_band_tc_d<64, false, true>(p, grid, s) : launch_band_tc_d<64, false, false>(p, grid, s);
 }
 
 }  // namespace ringk

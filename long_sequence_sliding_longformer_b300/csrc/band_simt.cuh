@@ -108,6 +108,7 @@ band_simt_f32_kernel(const __grid_constant__ SimtParams sp, const float* __restr
       float a = 0.f;
       for (int c = 0; c < D; ++c) a = fmaf(qs[warp][c], kr[c], a);
       s = a * p.scale;
+      if (sp.rel_bias) s += __ldg(sp.rel_bias + (int64_t)h * sp.rb_stride + sp.rb_half + t);
     }
     update(s, j, valid);
   }

@@ -138,6 +138,7 @@ struct Problem {
   cudaStream_t stream;
   int elem;  // bytes per element
   const int32_t* wh = nullptr;  // window per head (host), or nullptr: w for every head
+  const float* rb = nullptr;    // relative position bias [H, w + 1] (device), or nullptr
 };
 
 // the window of head h
@@ -255,6 +256,16 @@ static lf_status validate(const Problem& P, bool bf16) {
     if (t == 3) continue;
     if (overlaps(P.out, bytes, ptrs[t], t == 4 ? gbytes : bytes)) {
       set_error("out overlaps %s", names[t]);
+      return LF_ERR_INVALID_ARG;
+    }
+  }
+  if (P.rb) {
+    if (((uintptr_t)P.rb) & 3) {
+      set_error("rel_bias must be 4-byte aligned");
+      return LF_ERR_INVALID_ARG;
+    }
+    if (P.out && overlaps(P.out, bytes, P.rb, (size_t)P.H * (P.w + 1) * sizeof(float))) {
+      set_error("out overlaps rel_bias");
       return LF_ERR_INVALID_ARG;
     }
   }
@@ -434,7 +445,8 @@ static lf_status run_global_band_bf16(const Problem& P, int b0, int nbat, BandPa
 // with a one-sided (causal) window the ring kernel is 21-28% faster.
 static BandKernel band_kernel_for(const Problem& P) {
   if (P.d == 128) return BandKernel::pair;
-  return (P.G >= 16 && !P.causal) ? BandKernel::duo : BandKernel::ring;
+  // the relative position bias is built into the ring kernel only (d = 64)
+  return (P.G >= 16 && !P.causal && !P.rb) ? BandKernel::duo : BandKernel::ring;
 }
 
 // The launches of the heads whose window is wv (every head when there is one
@@ -516,6 +528,9 @@ static lf_status run_band_bf16_window(const Problem& P, int b0, int nbat, int32_
     p.G = P.G;
     p.pair = pair;
     p.pair_kernel = kind != BandKernel::ring;
+    p.rel_bias = P.rb;
+    p.rb_stride = P.w + 1;
+    p.rb_half = P.w / 2;
     p.nseg = nseg;
     p.items_per_b = items_per_b;
     const int64_t total = (int64_t)items_per_b * nbat;
@@ -561,6 +576,9 @@ static lf_status run_band_f32(const Problem& P, int b0, int nbat) {
     sp->dil[h] = P.dil[h];
     sp->half_h[h] = (int32_t)std::min<int64_t>(win_of(P, h) / 2, P.n);
   }
+  sp->rel_bias = P.rb;
+  sp->rb_stride = P.w + 1;
+  sp->rb_half = P.w / 2;
   if (injected_fault("launch")) {
     set_error("band kernel launch: injected failure (LF_FAULT=launch)");
     return LF_ERR_CUDA;
@@ -691,6 +709,16 @@ static lf_status forward_t(const Problem& P, bool bf16) {
   return st;
 }
 
+// The bias entries need the table whenever there is work.
+static lf_status check_bias_table(const float* rel_bias, int32_t B, int32_t H, int32_t n) {
+  if ((int64_t)B * H * n > 0 && !rel_bias) {
+    t_msg[0] = 0;
+    set_error("rel_bias must not be NULL");
+    return LF_ERR_INVALID_ARG;
+  }
+  return LF_OK;
+}
+
 // The per-head window entries need the window list whenever there are heads.
 static lf_status check_heads_window(const int32_t* w_heads, int32_t H) {
   if (H > 0 && !w_heads) {
@@ -736,6 +764,30 @@ lf_status lf_attn_fwd_f32(const void* q, const void* k, const void* v, const voi
                           const int32_t* pad_len, cudaStream_t stream) {
   lf::Problem P{q, k, v, qg, kg, vg, global_idx, n_global, out, B, H, n, d, w, dilation, causal,
                 pad_len, stream, 4};
+  return lf::forward(P, false);
+}
+
+lf_status lf_attn_fwd_bias(const void* q, const void* k, const void* v, const void* qg, const void* kg,
+                           const void* vg, const int32_t* global_idx, int32_t n_global, void* out,
+                           int32_t B, int32_t H, int32_t n, int32_t d, int32_t w,
+                           const int32_t* dilation, int32_t causal, const int32_t* pad_len,
+                           const float* rel_bias, cudaStream_t stream) {
+  lf_status st = lf::check_bias_table(rel_bias, B, H, n);
+  if (st != LF_OK) return st;
+  lf::Problem P{q, k, v, qg, kg, vg, global_idx, n_global, out, B, H, n, d, w, dilation, causal,
+                pad_len, stream, 2, nullptr, rel_bias};
+  return lf::forward(P, true);
+}
+
+lf_status lf_attn_fwd_bias_f32(const void* q, const void* k, const void* v, const void* qg,
+                               const void* kg, const void* vg, const int32_t* global_idx,
+                               int32_t n_global, void* out, int32_t B, int32_t H, int32_t n, int32_t d,
+                               int32_t w, const int32_t* dilation, int32_t causal,
+                               const int32_t* pad_len, const float* rel_bias, cudaStream_t stream) {
+  lf_status st = lf::check_bias_table(rel_bias, B, H, n);
+  if (st != LF_OK) return st;
+  lf::Problem P{q, k, v, qg, kg, vg, global_idx, n_global, out, B, H, n, d, w, dilation, causal,
+                pad_len, stream, 4, nullptr, rel_bias};
   return lf::forward(P, false);
 }
 

@@ -11,6 +11,7 @@ namespace lf {
 
 struct BwdOut {
   float *dq, *dk, *dv, *dqg, *dkg, *dvg;
+  float* drb = nullptr;  // gradient of the relative position bias [H, w + 1], or nullptr
 };
 
 static lf_status validate_bwd(const Problem& P, const void* dout, const BwdOut& g, bool bf16) {
@@ -59,6 +60,35 @@ static lf_status validate_bwd(const Problem& P, const void* dout, const BwdOut& 
   // no gradient may overlap an input or another gradient
   const size_t ib = (size_t)elems * P.elem, igb = (size_t)P.B * P.H * P.G * P.d * P.elem;
   const size_t ob = (size_t)elems * sizeof(float), ogb = (size_t)P.B * P.H * P.G * P.d * sizeof(float);
+  if (P.rb || g.drb) {
+    const size_t tb = (size_t)P.H * (P.w + 1) * sizeof(float);
+    if (!P.rb) {
+      set_error("d_rel_bias needs rel_bias");
+      return LF_ERR_INVALID_ARG;
+    }
+    if ((((uintptr_t)P.rb) & 3) || (((uintptr_t)g.drb) & 3)) {
+      set_error("rel_bias and d_rel_bias must be 4-byte aligned");
+      return LF_ERR_INVALID_ARG;
+    }
+    if (g.drb && P.w > bwdk::kMaxBiasW) {
+      set_error("the bias gradient supports w <= %d (got %d)", bwdk::kMaxBiasW, P.w);
+      return LF_ERR_UNSUPPORTED;
+    }
+    for (int a = 0; a < nout; ++a)
+      if (overlaps(out[a], a == 3 ? ogb : ob, P.rb, tb) || overlaps(out[a], a == 3 ? ogb : ob, g.drb, tb)) {
+        set_error("%s overlaps rel_bias or d_rel_bias", out_names[a]);
+        return LF_ERR_INVALID_ARG;
+      }
+    for (int t = 0; t < nin; ++t)
+      if (overlaps(g.drb, tb, in[t], t == 4 ? igb : ib)) {
+        set_error("d_rel_bias overlaps %s", in_names[t]);
+        return LF_ERR_INVALID_ARG;
+      }
+    if (overlaps(g.drb, tb, P.rb, tb)) {
+      set_error("d_rel_bias overlaps rel_bias");
+      return LF_ERR_INVALID_ARG;
+    }
+  }
   for (int a = 0; a < nout; ++a) {
     const size_t na = a == 3 ? ogb : ob;
     for (int t = 0; t < nin; ++t)
@@ -85,9 +115,12 @@ static lf_status launch_bwd(const bwdk::BwdParams& bp, const void* q, const void
   }
   static std::atomic<uint64_t> rows_attr{0}, keys_attr{0};
   constexpr int rows_smem = bwdk::rows_smem_bytes<D>(), keys_smem = bwdk::keys_smem_bytes<D>();
+  // the keys pass holds the bias gradient's per-step sums after its own arrays
+  constexpr int keys_smem_max = keys_smem + (bwdk::kMaxBiasW + 1) * 4;
+  const int keys_dyn = keys_smem + (bp.drb_part ? bp.rb_stride * 4 : 0);
   lf_status st = smem_attr_once((const void*)bwdk::bwd_rows_tiled<T, D>, rows_smem, rows_attr, "backward rows");
   if (st == LF_OK)
-    st = smem_attr_once((const void*)bwdk::bwd_keys_tiled<T, D>, keys_smem, keys_attr, "backward keys");
+    st = smem_attr_once((const void*)bwdk::bwd_keys_tiled<T, D>, keys_smem_max, keys_attr, "backward keys");
   if (st != LF_OK) return st;
   const T *tq = (const T*)q, *tk = (const T*)k, *tv = (const T*)v;
   const T *tqg = (const T*)qg, *tkg = (const T*)kg, *tvg = (const T*)vg, *tdo = (const T*)dout;
@@ -102,8 +135,13 @@ static lf_status launch_bwd(const bwdk::BwdParams& bp, const void* q, const void
     bwdk::bwd_grows<T, D><<<gblocks, bwdk::kWarps * 32, 0, s>>>(bp, tqg, tkg, tvg, tdo, g.dqg, stats);
     ++launched;
   }
-  bwdk::bwd_keys_tiled<T, D><<<tiles, bwdk::kThreads, keys_smem, s>>>(bp, tq, tk, tv, tdo, g.dk, g.dv, stats);
+  bwdk::bwd_keys_tiled<T, D><<<tiles, bwdk::kThreads, keys_dyn, s>>>(bp, tq, tk, tv, tdo, g.dk, g.dv, stats);
   ++launched;
+  if (bp.drb_part) {
+    const dim3 rgrid((unsigned)((bp.rb_stride + 255) / 256), (unsigned)bp.H);
+    bwdk::bwd_bias_reduce<<<rgrid, 256, 0, s>>>(bp, g.drb);
+    ++launched;
+  }
   if (bp.G > 0) {
     bwdk::bwd_gkeys<T, D><<<gblocks, bwdk::kWarps * 32, 0, s>>>(bp, tq, tk, tv, tdo, g.dk, g.dv, stats);
     bwdk::bwd_kgvg<T, D><<<kwarps, bwdk::kWarps * 32, 0, s>>>(bp, tqg, tkg, tvg, tdo, g.dkg, g.dvg, stats);
@@ -141,6 +179,14 @@ static lf_status backward_t(const Problem& P, const void* dout, const BwdOut& g)
   }
   bwdk::BwdParams* holder = bwd_params();
   lf_status st = holder ? LF_OK : LF_ERR_NO_MEMORY;
+  if (st == LF_OK && g.drb) {
+    // the bias gradient is summed into, launch block by launch block
+    e = cudaMemsetAsync(g.drb, 0, (size_t)P.H * (P.w + 1) * sizeof(float), P.stream);
+    if (e != cudaSuccess) {
+      set_error("clearing d_rel_bias: %s", cudaGetErrorString(e));
+      st = LF_ERR_CUDA;
+    }
+  }
   for (int b0 = 0; st == LF_OK && b0 < P.B; b0 += kMaxBatch) {
     for (int h0 = 0; st == LF_OK && h0 < P.H; h0 += kMaxHeadsSimt) {
       bwdk::BwdParams& bp = *holder;
@@ -154,6 +200,9 @@ static lf_status backward_t(const Problem& P, const void* dout, const BwdOut& g)
       bp.h0 = h0;
       bp.causal = P.causal;
       bp.G = P.G;
+      bp.rel_bias = P.rb;
+      bp.rb_stride = P.w + 1;
+      bp.rb_half = P.w / 2;
       bp.scale = (float)(1.0 / std::sqrt((double)P.d));
       bp.sl2 = (float)(1.4426950408889634 / std::sqrt((double)P.d));
       for (int b = 0; b < bp.B; ++b) bp.pad[b] = P.pad ? P.pad[b0 + b] : 0;
@@ -176,6 +225,18 @@ static lf_status backward_t(const Problem& P, const void* dout, const BwdOut& g)
         break;
       }
       bp.tiles_b = (int32_t)off;
+      float* part = nullptr;  // the keys pass's per-tile sums of the bias gradient
+      if (g.drb) {
+        const size_t pb = (size_t)bp.B * bp.tiles_b * bp.rb_stride * sizeof(float);
+        e = injected_fault("alloc") ? cudaErrorMemoryAllocation : cudaMallocAsync((void**)&part, pb, P.stream);
+        if (e != cudaSuccess) {
+          cudaGetLastError();
+          set_error("scratch allocation of %zu bytes failed: %s", pb, cudaGetErrorString(e));
+          st = LF_ERR_NO_MEMORY;
+          break;
+        }
+        bp.drb_part = part;
+      }
       if (P.elem == 2) {
         st = P.d == 64 ? launch_bwd<__nv_bfloat16, 64>(bp, P.q, P.k, P.v, P.qg, P.kg, P.vg, dout, g, stats, P.stream)
                        : launch_bwd<__nv_bfloat16, 128>(bp, P.q, P.k, P.v, P.qg, P.kg, P.vg, dout, g, stats, P.stream);
@@ -185,6 +246,13 @@ static lf_status backward_t(const Problem& P, const void* dout, const BwdOut& g)
         st = launch_bwd<float, 64>(bp, P.q, P.k, P.v, P.qg, P.kg, P.vg, dout, g, stats, P.stream);
       } else {
         st = launch_bwd<float, 128>(bp, P.q, P.k, P.v, P.qg, P.kg, P.vg, dout, g, stats, P.stream);
+      }
+      if (part) {
+        cudaError_t pe = cudaFreeAsync(part, P.stream);
+        if (st == LF_OK && pe != cudaSuccess) {
+          set_error("scratch free: %s", cudaGetErrorString(pe));
+          st = LF_ERR_CUDA;
+        }
       }
     }
   }
@@ -227,6 +295,32 @@ lf_status lf_attn_bwd_f32(const void* q, const void* k, const void* v, const voi
   lf::Problem P{q, k, v, qg, kg, vg, global_idx, n_global, nullptr, B, H, n, d, w, dilation, causal,
                 pad_len, stream, 4};
   return lf::backward(P, dout, lf::BwdOut{dq, dk, dv, dqg, dkg, dvg}, false);
+}
+
+lf_status lf_attn_bwd_bias(const void* q, const void* k, const void* v, const void* qg, const void* kg,
+                           const void* vg, const int32_t* global_idx, int32_t n_global, const void* dout,
+                           float* dq, float* dk, float* dv, float* dqg, float* dkg, float* dvg, int32_t B,
+                           int32_t H, int32_t n, int32_t d, int32_t w, const int32_t* dilation, int32_t causal,
+                           const int32_t* pad_len, const float* rel_bias, float* d_rel_bias,
+                           cudaStream_t stream) {
+  lf_status st = lf::check_bias_table(rel_bias, B, H, n);
+  if (st != LF_OK) return st;
+  lf::Problem P{q, k, v, qg, kg, vg, global_idx, n_global, nullptr, B, H, n, d, w, dilation, causal,
+                pad_len, stream, 2, nullptr, rel_bias};
+  return lf::backward(P, dout, lf::BwdOut{dq, dk, dv, dqg, dkg, dvg, d_rel_bias}, true);
+}
+
+lf_status lf_attn_bwd_bias_f32(const void* q, const void* k, const void* v, const void* qg, const void* kg,
+                               const void* vg, const int32_t* global_idx, int32_t n_global, const void* dout,
+                               float* dq, float* dk, float* dv, float* dqg, float* dkg, float* dvg,
+                               int32_t B, int32_t H, int32_t n, int32_t d, int32_t w,
+                               const int32_t* dilation, int32_t causal, const int32_t* pad_len,
+                               const float* rel_bias, float* d_rel_bias, cudaStream_t stream) {
+  lf_status st = lf::check_bias_table(rel_bias, B, H, n);
+  if (st != LF_OK) return st;
+  lf::Problem P{q, k, v, qg, kg, vg, global_idx, n_global, nullptr, B, H, n, d, w, dilation, causal,
+                pad_len, stream, 4, nullptr, rel_bias};
+  return lf::backward(P, dout, lf::BwdOut{dq, dk, dv, dqg, dkg, dvg, d_rel_bias}, false);
 }
 
 lf_status lf_attn_bwd_hw(const void* q, const void* k, const void* v, const void* qg, const void* kg,

@@ -83,6 +83,11 @@ struct BandParams {
   // The launch runs a kernel that takes items of two tiles (duo, pair: 1) or
   // the ring kernel (0).
   int32_t pair_kernel;
+  // Relative position bias of the band keys (ring and pair kernels):
+  // rel_bias[h * rb_stride + rb_half + t] is added to the scaled score of the
+  // key at window step t; nullptr: none.
+  const float* rel_bias;
+  int32_t rb_stride, rb_half;
   int32_t pad[kMaxBatch];
   BandSeg seg[kMaxSeg];
   int32_t gidx[kMaxGlobal];
@@ -103,6 +108,10 @@ struct SimtParams {
   PatternParams pat;
   int32_t dil[kMaxHeadsSimt];
   int32_t half_h[kMaxHeadsSimt];  // reach in steps: back half_h, ahead causal ? 0 : half_h
+  // relative position bias of the band keys: rel_bias[h * rb_stride + rb_half + t]
+  // is added to the scaled score at window step t (nullptr: none)
+  const float* rel_bias;
+  int32_t rb_stride, rb_half;
 };
 
 // ----------------------------------------------------------------- host-side launchers
@@ -573,6 +582,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
+
+constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;

@@ -284,3 +284,20 @@ def test_per_head_window_backward_refused_on_host(lib):
     assert "w_heads[1]" in lib.lf_last_error_message().decode()
     args[19] = None
     assert lib.lf_attn_bwd_hw(*args) == 1
+
+
+def test_bias_entries_refused_on_host(lib):
+    """The bias table is required; its gradient needs w <= 4096 and must not
+    overlap the other gradients."""
+    f = _FAKE
+    fwd = lambda rb: lib.lf_attn_fwd_bias(f[0], f[1], f[2], None, None, None, None, 0, f[6], 1, 2, 64, 64, 8,
+                                          _i32p([1, 1]), 0, None, rb, None)
+    assert fwd(None) == 1
+    assert "rel_bias" in lib.lf_last_error_message().decode()
+    assert fwd(f[13] + 2) == 1  # misaligned table
+    args = _bwd_args(lib)
+    bwd = lambda rb, drb, w=8: lib.lf_attn_bwd_bias(*(args[:19] + [w] + args[20:-1] + [rb, drb, None]))
+    assert bwd(None, None) == 1
+    assert bwd(f[13], f[14], w=4098) == 2  # the bias gradient's window limit
+    assert bwd(f[13], f[7]) == 1  # d_rel_bias overlaps dq
+    assert "overlaps" in lib.lf_last_error_message().decode()
