@@ -419,6 +419,32 @@ def run_gpu(args, wl):
     bwd_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evb) / Kb, ws, dev)
     del grads, dout
 
+    # ---- the same forward with a relative position bias table [H, w + 1] on
+    # the band scores (its own kernel instantiation); L2 flushed before each
+    genb = torch.Generator(device="cpu").manual_seed(wl.seed + 4000 + rank)
+    table = torch.randn(wl.H, wl.w + 1, generator=genb).to(dev)
+    bout = torch.empty_like(out)
+
+    def bias_call():
+        lf.attn(inp.q, inp.k, inp.v, w=wl.w, dilation=wl.dilation, causal=wl.causal, pad_len=wl.pad_len,
+                qg=inp.qg, kg=inp.kg, vg=inp.vg, global_idx=wl.global_idx, out=bout, rel_bias=table)
+
+    for _ in range(3):
+        bias_call()
+    bias_kernel = lf.last_band_kernel()
+    Kr = max(3, min(K, 100))
+    evr = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Kr)]
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    for i in range(Kr):
+        flush.zero_()
+        evr[i][0].record(stream)
+        bias_call()
+        evr[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    bias_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evr) / Kr, ws, dev)
+    del table, bout
+
     # ---- the projections that produce this workload's inputs from hidden
     # states [B, n, H*d] (q, k, v, and kg, vg with global tokens: one call),
     # bf16 workloads only; L2 flushed before each call
@@ -531,12 +557,17 @@ def run_gpu(args, wl):
                 "value": ws * 2.0 * flops / (bwd_ms * 1e-3) / 1e12,
                 "flops_per_step": 2.0 * flops,
                 "flops_counted": "8*d per attended pair (dP, dV, dQ, dK; the recomputed scores not counted)",
-                "kernels": "bwd_row_kernel + bwd_key_kernel (CUDA cores, fp32)",
+                "kernels": "bwd_rows_tiled + bwd_keys_tiled (+ bwd_grows, bwd_gkeys, bwd_kgvg with global "
+                           "tokens; CUDA cores, fp32)",
                 "roofline": {"bound": "alu", "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
                              "achieved": 2.0 * flops / (bwd_ms * 1e-3) / 1e12,
                              "frac": 2.0 * flops / (bwd_ms * 1e-3) / 1e12 / FP32_PEAK_TFLOPS,
                              "peak_source": "148 SMs x 128 fp32 lanes x 2 flops x 2.032 GHz"},
                 "l2": "flushed before every step"},
+            "relative_bias": {"ms_per_call": bias_ms, "steps": Kr, "unit": "TFLOP/s",
+                              "value": ws * flops / (bias_ms * 1e-3) / 1e12, "band_kernel": bias_kernel,
+                              "vs_plain_step": bias_ms / statistics.mean(step_ms),
+                              "l2": "flushed before every call"},
             "projection": proj,
             "memory_combine": memc,
             "gpu_launches": launches,
