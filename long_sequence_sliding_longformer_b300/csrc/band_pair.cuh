@@ -581,15 +581,16 @@ __device__ __forceinline__ float chunk_max(const uint32_t (&x)[32], uint32_t kee
   return fmaxf(max3f(a, b, v[28]), max3f(c, d, max3f(v[29], v[30], v[31])));
 }
 
-// Relative position bias of a 32-column chunk, in place: x <- x * sl2 +
-// bias(t0 + t) * log2(e) for t = 0..31 (the scores' exp2 domain).  The step
-// is clamped to the table [tlo, thi]; a clamped column is masked anyway.
-__device__ __forceinline__ void chunk_bias(uint32_t (&x)[32], float sl2, const float* brow, int t0, int tlo,
+// Relative position bias of a 32-column chunk, in place: x <- x * scale +
+// bias(t0 + t) for t = 0..31 (scale = 1/sqrt(d); the exp2 scaling by log2(e)
+// is applied with the maximum).  The step is clamped to the table [tlo, thi];
+// a clamped column is masked anyway.
+__device__ __forceinline__ void chunk_bias(uint32_t (&x)[32], float scale, const float* brow, int t0, int tlo,
                                            int thi) {
 #pragma unroll
   for (int t = 0; t < 32; ++t) {
     const int st = min(max(t0 + t, tlo), thi);
-    x[t] = __float_as_uint(fmaf(__uint_as_float(x[t]), sl2, __ldg(brow + st) * kLog2e));
+    x[t] = __float_as_uint(fmaf(__uint_as_float(x[t]), scale, __ldg(brow + st)));
   }
 }
 
@@ -742,14 +743,15 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
         reg_fence32(x);
         const uint32_t kc = c == 0 ? keep0 : c == 1 ? keep1 : c == 2 ? keep2 : keep3;
         if (scaled) {
-          chunk_bias(x, sl2, brow, it.U0 + 128 * e + 32 * c - m_q, -p.rb_half, p.rb_stride - 1 - p.rb_half);
+          chunk_bias(x, sl2 * (1.f / kLog2e), brow, it.U0 + 128 * e + 32 * c - m_q, -p.rb_half,
+                     p.rb_stride - 1 - p.rb_half);
           tmem_st16_nw(tS + 32 * c, x);
           tmem_st16_nw(tS + 32 * c + 16, x + 16);
         }
         mx = fmaxf(mx, chunk_max(x, kc, (fullm >> c) & 1u));
       }
       if (scaled) tmem_wait_st();  // pass 2 reads the biased scores back
-      const float mt = scaled ? mx : mx * sl2;
+      const float mt = mx * (scaled ? kLog2e : sl2);
       tr.ev(3);
       float alpha = 1.f;
       bool resc = false;
@@ -787,7 +789,7 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
           tmem_wait_ld();
           reg_fence32(x);
           const uint32_t kc = c == 0 ? keep0 : c == 1 ? keep1 : c == 2 ? keep2 : keep3;
-          sum2 = __fadd2_rn(sum2, chunk_exp(x, kc, (fullm >> c) & 1u, scaled ? 1.f : sl2, mneg, pk));
+          sum2 = __fadd2_rn(sum2, chunk_exp(x, kc, (fullm >> c) & 1u, scaled ? kLog2e : sl2, mneg, pk));
         } else {
 #pragma unroll
           for (int t = 0; t < 16; ++t) pk[t] = 0u;

@@ -834,23 +834,25 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
           for (int c = 0; c < NC; ++c) mask32(x + 32 * c, keep[c]);
         }
         if (kB && e < it.nU) {
-          // scores -> s * scale * log2(e) + bias * log2(e); masked columns stay
-          // -inf (their clamped table index is never used)
+          // scores -> s / sqrt(d) + bias (the exp2 scaling by log2(e) is
+          // applied with the maximum); masked columns stay -inf (their
+          // clamped table index is never used)
           const int t0 = it.U0 + C::kE * e - m_q;  // window step of column 0
           const int tmax = p.rb_stride - 1 - p.rb_half;
+          const float scale = sl2 * (1.f / kLog2e);
 #pragma unroll
           for (int c = 0; c < C::kE; ++c) {
             const int t = min(max(t0 + c, -p.rb_half), tmax);
-            x[c] = __float_as_uint(fmaf(__uint_as_float(x[c]), sl2, __ldg(brow + t) * kLog2e));
+            x[c] = __float_as_uint(fmaf(__uint_as_float(x[c]), scale, __ldg(brow + t)));
           }
         }
         mx = max64(x);  // row maximum of the raw scores (the scale is positive)
         if (NC == 4) mx = fmaxf(mx, max64(x + 64));
       }
       pf.lap(4);
-      // with the bias the band entries' scores are already scaled
+      // with the bias the band entries' scores are already scaled by 1/sqrt(d)
       const bool scaled = kB && e < it.nU;
-      const float mt = scaled ? mx : mx * sl2;
+      const float mt = mx * (scaled ? kLog2e : sl2);
       float alpha = 1.f;
       bool resc = false;
       if (mt > m_run + kLazy) {
@@ -869,7 +871,7 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
         float l = 0.f;
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
-          l += exp32(x + 32 * c, scaled ? 1.f : sl2, mneg, pk);
+          l += exp32(x + 32 * c, scaled ? kLog2e : sl2, mneg, pk);
           tmem_st16_nw(tS + 16 * c, pk);  // P chunk c over columns [16c, 16c + 16) (already read)
         }
         l_run = l_run * alpha + l;
