@@ -116,3 +116,38 @@ def test_zero_table_equals_the_plain_call():
                 qg=inp.qg, kg=inp.kg, vg=inp.vg, global_idx=wl.global_idx).float()
     torch.cuda.synchronize()
     assert (a - b).abs().max().item() <= 8e-3
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("f32", 32)])
+def test_bias_across_the_batch_launch_split(dtype, d):
+    """260 batch rows: the forward and backward run in blocks of 256 batch
+    rows, and the bias gradient is summed over the blocks' launches."""
+    B, H, n, w = 260, 2, 80, 16
+    wl = workloads.custom("bias_b260", dtype, B, H, n, d, w, (1, 2), False, (3,), None, seed=12)
+    inp = workloads.make_inputs(wl, "cuda")
+    table = (torch.randn(H, w + 1, generator=torch.Generator().manual_seed(13)) * 2).cuda()
+    out = fwd(wl, inp, table)
+    want = oracle.wl_fwd(wl, inp, rel_bias=table.cpu().numpy())
+    err = np.abs(out.float().cpu().numpy().astype(np.float64) - want)
+    assert err.max() <= (1e-4 if dtype == "f32" else 2e-2), err.max()
+    dout = torch.randn(B, H, n, d, generator=torch.Generator().manual_seed(14)).to(wl.torch_dtype).cuda()
+    got = lf.attn_bwd(inp.q, inp.k, inp.v, dout, w=w, dilation=wl.dilation, qg=inp.qg, kg=inp.kg, vg=inp.vg,
+                      global_idx=wl.global_idx, rel_bias=table)
+    torch.cuda.synchronize()
+    wg = oracle.wl_bwd(wl, inp, dout, rel_bias=table.cpu().numpy())
+    for name, wv in wg.items():
+        e = np.abs(got[name].cpu().numpy().astype(np.float64) - wv).max()
+        assert e <= REL * max(1.0, np.abs(wv).max()), (name, e)
+
+
+def test_many_distinct_head_windows():
+    """Twelve heads, nine distinct windows (one launch each), dilations mixed."""
+    wh = [0, 2, 6, 64, 130, 64, 512, 2, 1000, 6, 40, 512]
+    dil = [1, 2, 1, 3, 1, 1, 2, 1, 1, 4, 1, 1]
+    wl = workloads.custom("hw12", "bf16", 2, 12, 600, 64, wh, dil, False, (0, 300), (0, 70), seed=15)
+    inp = workloads.make_inputs(wl, "cuda")
+    out = lf.attn(inp.q, inp.k, inp.v, w=wl.w, dilation=wl.dilation, pad_len=wl.pad_len, qg=inp.qg, kg=inp.kg,
+                  vg=inp.vg, global_idx=wl.global_idx)
+    torch.cuda.synchronize()
+    err = np.abs(out.float().cpu().numpy().astype(np.float64) - oracle.wl_fwd(wl, inp))
+    assert err.max() <= 2e-2 and err.mean() <= 2e-3, (err.max(), err.mean())
