@@ -233,8 +233,8 @@ lf_status lf_attn_bwd_bias_f32(const void* q, const void* k, const void* v,
  * some not): as lf_attn_fwd / lf_attn_fwd_f32 / lf_attn_bwd / lf_attn_bwd_f32,
  * with head h using the window w_heads[h] (even, >= 0) in place of the one w.
  * w_heads: host array of H values, read during the call, NULL only if H == 0.
- * Heads sharing a window run in one set of launches (bf16: one launch per
- * distinct window, each holding the tiles of its heads only).  Errors as in
+ * bf16: one band launch holds every head's tiles, each carrying its head's
+ * reach (d = 64 with windows that differ runs the ring kernel).  Errors as in
  * the calls they extend; a bad w_heads entry is LF_ERR_INVALID_ARG.
  */
 lf_status lf_attn_fwd_hw(const void* q, const void* k, const void* v,

@@ -78,6 +78,7 @@ struct BandCfg {
 // way by every role from the item number alone.
 struct PairItem {
   int b, h, r, delta, n_r, set, m0, Lb, Lm, bh;
+  int half, right;  // the head's window reach in steps: back, ahead
   bool zero;        // no valid row in the pair: output zeros only
   int act[2];       // tile X has at least one valid row
   int U0, nU, nE;   // first key (m coordinate) of the band entries, their count, all entries
@@ -116,6 +117,8 @@ __device__ __forceinline__ PairItem decode_pair(const BandParams& p, const BandS
   it.h = sg.h;
   it.r = sg.r;
   it.delta = sg.delta;
+  it.half = sg.half;
+  it.right = p.causal ? 0 : sg.half;
   it.n_r = sg.n_r;
   it.set = sg.set;
   it.m0 = (rem - sg.begin) * 256;
@@ -128,8 +131,8 @@ __device__ __forceinline__ PairItem decode_pair(const BandParams& p, const BandS
     const int q0 = it.m0 + 128 * X;
     it.act[X] = q0 < it.Lm;
     const int qlast = min(q0 + 127, it.Lm - 1);
-    it.klo[X] = max(0, q0 - p.half);
-    it.kend[X] = min(it.Lm - 1, qlast + p.right);
+    it.klo[X] = max(0, q0 - it.half);
+    it.kend[X] = min(it.Lm - 1, qlast + it.right);
     int glim = it.Lb - 1;
     if (p.causal) glim = min(glim, it.r + it.delta * qlast);
     it.gcnt[X] = (it.act[X] && p.G > 0) ? upper_bound_gidx(p, glim) : 0;
@@ -542,7 +545,7 @@ __device__ __forceinline__ uint32_t bit_range(int lo, int hi) {
 // Global entry e, chunk c: bit t set where this row attends global column
 // 32c + t (a global key already in the row's band is counted there, once).
 __device__ __forceinline__ uint32_t global_keep(const BandParams& p, const PairItem& it, int e, int c,
-                                                int m_q, bool row_valid) {
+                                                int m_q, bool row_valid, int half, int right) {
   int gx, gt;
   global_entry(it, e, gx, gt);
   const int tend = max(0, min(32, global_count(it, gx, gt) - 32 * c));
@@ -552,7 +555,7 @@ __device__ __forceinline__ uint32_t global_keep(const BandParams& p, const PairI
   for (int t = 0; t < tend; ++t) {
     const int g = p.gidx[128 * gt + 32 * c + t];
     const int mg = residue_coord(g, it.r, it.delta);
-    const bool in_band = (m_q - mg <= p.half) && (mg - m_q <= p.right);
+    const bool in_band = (m_q - mg <= half) && (mg - m_q <= right);
     k |= (uint32_t)((!p.causal || g <= i_q) && !in_band) << t;
   }
   return row_valid ? k : 0u;
@@ -618,8 +621,9 @@ __device__ __forceinline__ float2 chunk_exp(const uint32_t (&x)[32], uint32_t ke
 }
 
 // Softmax of tile X (one query row per thread; warp quarter wq of TMEM lanes).
-// kB: the band entries' scores carry the relative position bias.
-template <int D, bool kB>
+// kB: the band entries' scores carry the relative position bias.  kW: heads'
+// windows differ (each item's reach comes from its segment).
+template <int D, bool kB, bool kW>
 __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_t tmem, int X,
                              int wq, int lane) {
   using C = BandCfg<D>;
@@ -688,6 +692,8 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
       if (!ok || !iss.issue_s(it, kv, qb, entry(0), len == 1)) { ok = false; break; }
     }
     float m_run = NEG_INF, l_run = 0.f;
+    // the window reach of this item's head
+    const int half = kW ? it.half : p.half, right = kW ? it.right : p.right;
     // the bias of this row's head, indexed by window step
     const float* brow = kB ? p.rel_bias + (size_t)it.h * p.rb_stride + p.rb_half : nullptr;
 
@@ -700,18 +706,18 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
       uint32_t keep0, keep1, keep2, keep3;
       if (is_band) {
         const int kb = it.U0 + 128 * e;
-        const int clo = m_q - p.half - kb;
-        int chi = min(m_q + p.right, it.Lm - 1) - kb;
+        const int clo = m_q - half - kb;
+        int chi = min(m_q + right, it.Lm - 1) - kb;
         if (!row_valid) chi = clo - 1;
         keep0 = bit_range(clo, chi);
         keep1 = bit_range(clo - 32, chi - 32);
         keep2 = bit_range(clo - 64, chi - 64);
         keep3 = bit_range(clo - 96, chi - 96);
       } else {
-        keep0 = global_keep(p, it, e, 0, m_q, row_valid);
-        keep1 = global_keep(p, it, e, 1, m_q, row_valid);
-        keep2 = global_keep(p, it, e, 2, m_q, row_valid);
-        keep3 = global_keep(p, it, e, 3, m_q, row_valid);
+        keep0 = global_keep(p, it, e, 0, m_q, row_valid, half, right);
+        keep1 = global_keep(p, it, e, 1, m_q, row_valid, half, right);
+        keep2 = global_keep(p, it, e, 2, m_q, row_valid, half, right);
+        keep3 = global_keep(p, it, e, 3, m_q, row_valid, half, right);
       }
       // chunks some lane of the warp needs, and chunks every lane needs whole
       const uint32_t onm = (__any_sync(0xffffffffu, keep0 != 0u) ? 1u : 0u) |
@@ -878,7 +884,7 @@ constexpr int kRegsSoftmax = 200;
 constexpr int kRegsOther = 96;
 constexpr int kRegsAtLaunchMin = (256 * kRegsSoftmax + 128 * kRegsOther + kBandThreads - 1) / kBandThreads;
 
-template <int D, bool kB>
+template <int D, bool kB, bool kW>
 __global__ void __launch_bounds__(kBandThreads, 1) band_tc_kernel(const __grid_constant__ BandParams p) {
   using C = BandCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -929,7 +935,7 @@ __global__ void __launch_bounds__(kBandThreads, 1) band_tc_kernel(const __grid_c
 
   if (warp >= 4) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-    band_softmax<D, kB>(p, sm, tmem, (warp >> 2) - 1, warp & 3, lane);
+    band_softmax<D, kB, kW>(p, sm, tmem, (warp >> 2) - 1, warp & 3, lane);
   } else {
     // the issuing warps are the oldest of the CTA: the schedulers favour them
     // over the busy softmax warps that share their sub-partitions
@@ -949,12 +955,12 @@ __global__ void __launch_bounds__(kBandThreads, 1) band_tc_kernel(const __grid_c
   }
 }
 
-template <int D, bool kB>
+template <int D, bool kB, bool kW>
 static lf_status launch_band_tc_d(const BandParams& p, int grid, cudaStream_t s) {
   using C = BandCfg<D>;
   static std::atomic<uint64_t> attr_done{0};
   static std::atomic<bool> regs_checked{false};
-  lf_status st = smem_attr_once((const void*)band_tc_kernel<D, kB>, C::kSmem, attr_done, "band kernel");
+  lf_status st = smem_attr_once((const void*)band_tc_kernel<D, kB, kW>, C::kSmem, attr_done, "band kernel");
   if (st != LF_OK) return st;
   if (!regs_checked.load(std::memory_order_acquire)) {
     cudaError_t e;
@@ -962,7 +968,7 @@ static lf_status launch_band_tc_d(const BandParams& p, int grid, cudaStream_t s)
     // it was planned for; with fewer registers setmaxnreg.inc could never be
     // satisfied, so refuse to launch rather than wait.
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, band_tc_kernel<D, kB>);
+    e = cudaFuncGetAttributes(&fa, band_tc_kernel<D, kB, kW>);
     if (e != cudaSuccess) {
       set_error("cudaFuncGetAttributes(band kernel): %s", cudaGetErrorString(e));
       return LF_ERR_CUDA;
@@ -974,7 +980,7 @@ static lf_status launch_band_tc_d(const BandParams& p, int grid, cudaStream_t s)
     }
     regs_checked.store(true, std::memory_order_release);
   }
-  band_tc_kernel<D, kB><<<grid, kBandThreads, C::kSmem, s>>>(p);
+  band_tc_kernel<D, kB, kW><<<grid, kBandThreads, C::kSmem, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("band kernel launch: %s", cudaGetErrorString(e));
@@ -986,7 +992,8 @@ static lf_status launch_band_tc_d(const BandParams& p, int grid, cudaStream_t s)
 
 // D = 128 only (D = 64 runs the ring kernel of band_ring.cuh).
 inline lf_status launch(const BandParams& p, int grid, cudaStream_t s) {
-  return p.rel_bias ? launch_band_tc_d<128, true>(p, grid, s) : launch_band_tc_d<128, false>(p, grid, s);
+  if (p.rel_bias) return launch_band_tc_d<128, true, false>(p, grid, s);
+  return p.varwin ? launch_band_tc_d<128, false, true>(p, grid, s) : launch_band_tc_d<128, false, false>(p, grid, s);
 }
 
 }  // namespace pairk

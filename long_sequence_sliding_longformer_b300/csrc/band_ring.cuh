@@ -114,6 +114,7 @@ __device__ __forceinline__ int gidx_at(const BandParams& p, const Tables& tb, in
 
 struct TileItem {
   int b, h, r, delta, n_r, set, m0, Lb, Lm, bh;
+  int half, right;  // the head's window reach in steps: back, ahead
   bool act;     // the tile has at least one valid row
   int U0, nU;   // band entries: keys (m coordinate) [U0 + kE*e, U0 + kE*e + kE), e < nU
   int klo, khi; // first and last key any row of the tile attends in the band
@@ -148,6 +149,8 @@ __device__ __noinline__ TileItem decode_tile(const BandParams& p, const Tables& 
   it.h = sg.h;
   it.r = sg.r;
   it.delta = sg.delta;
+  it.half = sg.half;
+  it.right = p.causal ? 0 : sg.half;
   it.n_r = sg.n_r;
   it.set = sg.set;
   it.m0 = (rem - sg.begin) * 128;
@@ -180,8 +183,8 @@ __device__ __noinline__ TileItem decode_tile(const BandParams& p, const Tables& 
     return it;
   }
   const int qlast = min(it.m0 + 127, it.Lm - 1);
-  it.klo = max(0, it.m0 - p.half);
-  it.khi = min(it.Lm - 1, qlast + p.right);
+  it.klo = max(0, it.m0 - it.half);
+  it.khi = min(it.Lm - 1, qlast + it.right);
   it.U0 = it.klo;
   it.nU = (it.khi - it.klo) / kE + 1;
   int glim = it.Lb - 1;
@@ -633,7 +636,7 @@ __device__ __forceinline__ uint32_t bit_range(int lo, int hi) {
 // 32c + t (a global key already in the row's band is counted there, once).
 template <int kE>
 __device__ __forceinline__ uint32_t global_keep(const BandParams& p, const Tables& tb, const TileItem& it,
-                                                int e, int c, int m_q, bool row_valid) {
+                                                int e, int c, int m_q, bool row_valid, int half, int right) {
   const int gt = e - it.nU;
   const int tend = max(0, min(32, global_count<kE>(it, e) - 32 * c));
   const int i_q = it.r + it.delta * m_q;
@@ -642,7 +645,7 @@ __device__ __forceinline__ uint32_t global_keep(const BandParams& p, const Table
   for (int t = 0; t < tend; ++t) {
     const int g = gidx_at(p, tb, kE * gt + 32 * c + t);
     const int mg = residue_coord(g, it.r, it.delta);
-    const bool in_band = (m_q - mg <= p.half) && (mg - m_q <= p.right);
+    const bool in_band = (m_q - mg <= half) && (mg - m_q <= right);
     k |= (uint32_t)((!p.causal || g <= i_q) && !in_band) << t;
   }
   return row_valid ? k : 0u;
@@ -692,8 +695,9 @@ __device__ __forceinline__ float exp32(const uint32_t* x, float sl2, float mneg,
 }
 
 // Softmax and epilogue (one query row per thread; warp quarter wq of TMEM lanes).
-// kB: the band entries' scores carry the relative position bias.
-template <int D, bool kG, bool kB>
+// kB: the band entries' scores carry the relative position bias.  kW: heads'
+// windows differ (each item's reach comes from its segment).
+template <int D, bool kG, bool kB, bool kW>
 __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_t tmem, int wq, int lane) {
   using C = BandCfg<D>;
   static_assert(C::kE == 64 || C::kE == 128, "the softmax holds one entry in registers");
@@ -738,6 +742,8 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
       continue;
     }
     float m_run = NEG_INF, l_run = 0.f;
+    // the window reach of this item's head
+    const int half = kW ? it.half : p.half, right = kW ? it.right : p.right;
     // the bias of this row's head, indexed by window step
     const float* brow = kB ? p.rel_bias + (size_t)it.h * p.rb_stride + p.rb_half : nullptr;
     // Band entries e in [e_all0, e_all1] are attended whole by every row of
@@ -747,17 +753,17 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
     {
       const int mw = it.m0 + 32 * wq;  // first row of this warp
       const int mw_last = min(mw + 31, it.Lm - 1);
-      const int hi_w = min(mw + p.right, it.Lm - 1);  // last key the warp's first row attends
+      const int hi_w = min(mw + right, it.Lm - 1);  // last key the warp's first row attends
       if (mw + 31 < it.Lm) {
-        e_all0 = ceil_div_i(mw + 31 - p.half - it.U0, C::kE);
+        e_all0 = ceil_div_i(mw + 31 - half - it.U0, C::kE);
         e_all1 = floor_div_i(hi_w - (C::kE - 1) - it.U0, C::kE);
       } else {
         e_all0 = 1;
         e_all1 = 0;
       }
       if (mw < it.Lm) {
-        e_any0 = ceil_div_i(mw - p.half - (C::kE - 1) - it.U0, C::kE);
-        e_any1 = floor_div_i(min(mw_last + p.right, it.Lm - 1) - it.U0, C::kE);
+        e_any0 = ceil_div_i(mw - half - (C::kE - 1) - it.U0, C::kE);
+        e_any1 = floor_div_i(min(mw_last + right, it.Lm - 1) - it.U0, C::kE);
       } else {
         e_any0 = 1;
         e_any1 = 0;
@@ -791,8 +797,8 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
         mode = (e >= e_all0 && e <= e_all1) ? 1 : (e >= e_any0 && e <= e_any1) ? 2 : 0;
         if (mode == 2) {
           const int kb = it.U0 + C::kE * e;
-          const int clo = m_q - p.half - kb;
-          int chi = min(min(m_q + p.right, it.Lm - 1) - kb, C::kE - 1);
+          const int clo = m_q - half - kb;
+          int chi = min(min(m_q + right, it.Lm - 1) - kb, C::kE - 1);
           if (!row_valid) chi = clo - 1;
 #pragma unroll
           for (int c = 0; c < NC; ++c) keep[c] = bit_range(clo - 32 * c, chi - 32 * c);
@@ -801,7 +807,7 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
         uint32_t any_bits = 0u, all_bits = ~0u;
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
-          keep[c] = global_keep<C::kE>(p, tb, it, e, c, m_q, row_valid);
+          keep[c] = global_keep<C::kE>(p, tb, it, e, c, m_q, row_valid, half, right);
           any_bits |= keep[c];
           all_bits &= keep[c];
         }
@@ -952,7 +958,7 @@ __device__ void band_softmax(const BandParams& p, const BandSmem<D>& sm, uint32_
 
 constexpr int kBandThreads = 256;
 
-template <int D, bool kG, bool kB>
+template <int D, bool kG, bool kB, bool kW>
 __global__ void __launch_bounds__(kBandThreads, BandCfg<D>::kCtaPerSm)
     band_tc_kernel(const __grid_constant__ BandParams p) {
   using C = BandCfg<D>;
@@ -1001,7 +1007,7 @@ __global__ void __launch_bounds__(kBandThreads, BandCfg<D>::kCtaPerSm)
   const uint32_t tmem = *sm.tmem_holder();
 
   if (warp >= 4) {
-    band_softmax<D, kG, kB>(p, sm, tmem, warp & 3, lane);
+    band_softmax<D, kG, kB, kW>(p, sm, tmem, warp & 3, lane);
   } else if (warp == 0) {
     band_mma<D, kG>(p, sm, tmem);
   } else if (warp == 1) {
@@ -1018,13 +1024,13 @@ __global__ void __launch_bounds__(kBandThreads, BandCfg<D>::kCtaPerSm)
   }
 }
 
-template <int D, bool kG, bool kB>
+template <int D, bool kG, bool kB, bool kW>
 static lf_status launch_band_tc_d(const BandParams& p, int grid, cudaStream_t s) {
   using C = BandCfg<D>;
   static std::atomic<uint64_t> attr_done{0};
-  lf_status st = smem_attr_once((const void*)band_tc_kernel<D, kG, kB>, C::kSmem, attr_done, "band kernel");
+  lf_status st = smem_attr_once((const void*)band_tc_kernel<D, kG, kB, kW>, C::kSmem, attr_done, "band kernel");
   if (st != LF_OK) return st;
-  band_tc_kernel<D, kG, kB><<<grid, kBandThreads, C::kSmem, s>>>(p);
+  band_tc_kernel<D, kG, kB, kW><<<grid, kBandThreads, C::kSmem, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("band kernel launch: %s", cudaGetErrorString(e));
@@ -1038,8 +1044,10 @@ static lf_status launch_band_tc_d(const BandParams& p, int grid, cudaStream_t s)
 // Global-row mode (p.gmode) is a separate instantiation, so that the band
 // path carries none of its code.
 inline lf_status launch(const BandParams& p, int grid, cudaStream_t s) {
-  if (p.gmode) return launch_band_tc_d<64, true, false>(p, grid, s);
-  return p.rel_bias ? launch_band_tc_d<64, false, true>(p, grid, s) : launch_band_tc_d<64, false, false>(p, grid, s);
+  if (p.gmode) return launch_band_tc_d<64, true, false, false>(p, grid, s);
+  if (p.rel_bias) return launch_band_tc_d<64, false, true, false>(p, grid, s);
+  return p.varwin ? launch_band_tc_d<64, false, false, true>(p, grid, s)
+                  : launch_band_tc_d<64, false, false, false>(p, grid, s);
 }
 
 }  // namespace ringk

@@ -397,6 +397,7 @@ static lf_status run_global_band_bf16(const Problem& P, int b0, int nbat, BandPa
       bs.items = qtiles;
       bs.set = 0;
       bs.begin = j * qtiles;
+      bs.half = P.n;  // every key is in reach
     }
     lf_status st;
     const int ek = ringk::BandCfg<64>::kE;
@@ -445,23 +446,30 @@ static lf_status run_global_band_bf16(const Problem& P, int b0, int nbat, BandPa
 // with a one-sided (causal) window the ring kernel is 21-28% faster.
 static BandKernel band_kernel_for(const Problem& P) {
   if (P.d == 128) return BandKernel::pair;
-  // the relative position bias is built into the ring kernel only (d = 64)
-  return (P.G >= 16 && !P.causal && !P.rb) ? BandKernel::duo : BandKernel::ring;
+  // the relative position bias is built into the ring kernel only (d = 64),
+  // and so are windows that differ between heads
+  bool one_window = true;
+  for (int h = 1; P.wh && h < P.H; ++h) one_window = one_window && P.wh[h] == P.wh[0];
+  return (P.G >= 16 && !P.causal && !P.rb && one_window) ? BandKernel::duo : BandKernel::ring;
 }
 
-// The launches of the heads whose window is wv (every head when there is one
-// window): the segments of those heads only, a launch per kMaxSeg segments or
-// kMaxSets (dilation, residue) tensor-map sets.
-static lf_status run_band_bf16_window(const Problem& P, int b0, int nbat, int32_t wv, BandParams& p) {
+// Every head's segments, each carrying its head's window reach (heads may
+// differ), a launch per kMaxSeg segments or kMaxSets (dilation, residue)
+// tensor-map sets.
+static lf_status run_band_bf16(const Problem& P, int b0, int nbat, BandParams& p) {
   const BandKernel kind = band_kernel_for(P);
   // persistent CTAs: two per SM for the ring kernel, one for the others
   const int grid_cap = sm_count() * (kind == BandKernel::ring ? ringk::BandCfg<64>::kCtaPerSm : 1);
-  const int64_t half0 = std::min<int64_t>(wv / 2, P.n);
-  const int64_t right0 = P.causal ? 0 : half0;
-  // The duo kernel pairs tiles when the window reach is a multiple of 16
-  // keys (the tiles' key ranges then meet on 16-key steps); the pair kernel
-  // always pairs, the ring kernel never.
-  const int pair = kind == BandKernel::pair || (kind == BandKernel::duo && half0 % 16 == 0 && right0 % 16 == 0);
+  // The duo kernel pairs tiles when every head's window reach is a multiple
+  // of 16 keys (the tiles' key ranges then meet on 16-key steps); the pair
+  // kernel always pairs, the ring kernel never.
+  bool reach16 = true, varwin = false;
+  for (int h = 0; h < P.H; ++h) {
+    varwin = varwin || win_of(P, h) != win_of(P, 0);
+    const int64_t half_h = std::min<int64_t>(win_of(P, h) / 2, P.n), right_h = P.causal ? 0 : half_h;
+    reach16 = reach16 && half_h % 16 == 0 && right_h % 16 == 0;
+  }
+  const int pair = kind == BandKernel::pair || (kind == BandKernel::duo && reach16);
   const int rows_per_item = pair ? 256 : 128;
   // keys per K/V load
   const int ek = kind == BandKernel::ring ? ringk::BandCfg<64>::kE : kind == BandKernel::duo ? duok::kLK : 128;
@@ -471,7 +479,6 @@ static lf_status run_band_bf16_window(const Problem& P, int b0, int nbat, int32_
   const __nv_bfloat16* v = reinterpret_cast<const __nv_bfloat16*>(P.v) + off;
   __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(P.out) + off;
   const int64_t planes = (int64_t)nbat * P.H;
-  const int64_t half = half0;
   int h = 0, r = 0;  // next segment to place
   while (h < P.H) {
     memset(&p, 0, sizeof p);
@@ -479,7 +486,7 @@ static lf_status run_band_bf16_window(const Problem& P, int b0, int nbat, int32_
     int set_delta[kMaxSets], set_r[kMaxSets];
     while (h < P.H && nseg < kMaxSeg) {
       const int delta = P.dil[h];
-      if (r >= delta || r >= P.n || win_of(P, h) != wv) {
+      if (r >= delta || r >= P.n) {
         ++h;
         r = 0;
         continue;
@@ -502,6 +509,7 @@ static lf_status run_band_bf16_window(const Problem& P, int b0, int nbat, int32_
       bs.items = (n_r + rows_per_item - 1) / rows_per_item;
       bs.set = set;
       bs.begin = items_per_b;
+      bs.half = (int32_t)std::min<int64_t>(win_of(P, h) / 2, P.n);
       items_per_b += bs.items;
       ++r;
     }
@@ -522,10 +530,11 @@ static lf_status run_band_bf16_window(const Problem& P, int b0, int nbat, int32_
     p.B = nbat;
     p.H = P.H;
     p.n = P.n;
-    p.half = (int32_t)half;
-    p.right = P.causal ? 0 : (int32_t)half;
     p.causal = P.causal;
     p.G = P.G;
+    p.half = P.H > 0 ? (int32_t)std::min<int64_t>(win_of(P, 0) / 2, P.n) : 0;
+    p.right = P.causal ? 0 : p.half;
+    p.varwin = varwin;
     p.pair = pair;
     p.pair_kernel = kind != BandKernel::ring;
     p.rel_bias = P.rb;
@@ -551,18 +560,6 @@ static lf_status run_band_bf16_window(const Problem& P, int b0, int nbat, int32_
   return LF_OK;
 }
 
-// Heads whose windows differ run in separate launches, one per window, each
-// holding the segments of its heads only.
-static lf_status run_band_bf16(const Problem& P, int b0, int nbat, BandParams& p) {
-  for (int hw = 0; hw < P.H; ++hw) {
-    bool first = true;  // hw is the first head with its window
-    for (int t = 0; t < hw && first; ++t) first = win_of(P, t) != win_of(P, hw);
-    if (!first) continue;
-    lf_status st = run_band_bf16_window(P, b0, nbat, win_of(P, hw), p);
-    if (st != LF_OK) return st;
-  }
-  return LF_OK;
-}
 static lf_status run_band_f32(const Problem& P, int b0, int nbat) {
   static thread_local SimtParams* sp = nullptr;  // ~18 KB: keep it off the stack
   if (!sp) sp = new (std::nothrow) SimtParams;

@@ -56,9 +56,10 @@ __device__ unsigned long long g_prof[kProfSlots][kProfPhases];
 // ----------------------------------------------------------------- band kernel params
 // A segment is one (head, residue class) of the dilated window: rows
 // i = r + delta*m for m in [0, n_r).  Its work items are its 128-row tiles
-// (D = 64) or pairs of consecutive tiles (D = 128).
+// (D = 64) or pairs of consecutive tiles (D = 128).  half: its head's window
+// reach in steps (look-back half, look-ahead causal ? 0 : half).
 struct BandSeg {
-  int32_t h, r, delta, n_r, items, set, begin, pad_;
+  int32_t h, r, delta, n_r, items, set, begin, half;
 };
 
 struct BandParams {
@@ -69,7 +70,14 @@ struct BandParams {
   const __nv_bfloat16* v;
   __nv_bfloat16* out;
   int32_t B, H, n;
-  int32_t half, right;     // window reach in steps: look-back half, look-ahead right
+  // window reach in steps shared by every head of the launch (look-back
+  // half, look-ahead right); the duo kernel is only chosen when all heads
+  // share one window
+  int32_t half, right;
+  // Heads' windows differ (varwin = 1): the ring and pair kernels then read
+  // each segment's reach (an instantiation of their own); otherwise every
+  // kernel reads half and right above.
+  int32_t varwin;
   int32_t causal, G, nseg, items_per_b, total_items;
   float sl2;               // log2(e) / sqrt(d)
   // Global-row mode (d = 64 kernel only): the query rows are the global

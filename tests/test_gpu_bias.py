@@ -141,7 +141,7 @@ def test_bias_across_the_batch_launch_split(dtype, d):
 
 
 def test_many_distinct_head_windows():
-    """Twelve heads, nine distinct windows (one launch each), dilations mixed."""
+    """Twelve heads, nine distinct windows in one launch, dilations mixed."""
     wh = [0, 2, 6, 64, 130, 64, 512, 2, 1000, 6, 40, 512]
     dil = [1, 2, 1, 3, 1, 1, 2, 1, 1, 4, 1, 1]
     wl = workloads.custom("hw12", "bf16", 2, 12, 600, 64, wh, dil, False, (0, 300), (0, 70), seed=15)

@@ -194,16 +194,18 @@ def test_bf16_few_globals_on_ring(G, w, causal):
 @pytest.mark.parametrize("d,G,causal", [(64, 0, False), (64, 1, True), (64, 20, False), (128, 1, False),
                                          (128, 0, True)])
 def test_bf16_per_head_windows(d, G, causal):
-    """A window per head (section 4.1 "Attention Pattern"): one launch per
-    distinct window, each holding only its heads' tiles; heads that share a
-    window share a launch although they are not adjacent.  G = 20 at d = 64
-    takes the duo kernel, d = 128 the pair kernel."""
+    """A window per head (section 4.1 "Attention Pattern"): one launch, each
+    tile reading its head's reach from its segment.  d = 64 runs the ring
+    kernel even with G = 20 (the duo kernel keeps one window per launch),
+    d = 128 the pair kernel."""
     wh = [512, 64, 0, 64, 2000, 512]
     dil = [1, 1, 2, 3, 1, 2]
     gidx = tuple(range(0, 900, 45))[:G]
     wl = workloads.custom("hw", "bf16", 2, 6, 900, d, wh, dil, causal, gidx, (0, 250), seed=50 + d + G)
     inp = workloads.make_inputs(wl, "cuda")
-    check(wl, run(wl, inp), oracle.wl_fwd(wl, inp))
+    out = run(wl, inp)
+    assert lf.last_band_kernel() == ("band_pair" if d == 128 else "band_ring")
+    check(wl, out, oracle.wl_fwd(wl, inp))
 
 
 @pytest.mark.parametrize("causal", [False, True])
