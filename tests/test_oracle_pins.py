@@ -401,3 +401,25 @@ def test_relative_bias_rejected_shapes():
         oracle.fwd(z, z, z, w=4, dilation=[1, 1], rel_bias=np.zeros((2, 4), np.float32))
     with pytest.raises(ValueError):
         oracle.fwd(z, z, z, w=[4, 4], dilation=[1, 1], rel_bias=np.zeros((2, 5), np.float32))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_per_head_window_pair_count_matches_dense_masks(causal):
+    """The oracle's pair count with a window per head equals the number of
+    attended entries in the dense masks built head by head."""
+    from dense_ref import masks
+    n, wh, dil, gidx, pads = 70, [0, 6, 40, 200], [1, 2, 1, 3], [0, 35], [0, 11]
+    pairs, gpairs = oracle.count_pairs(B=2, H=4, n=n, w=wh, dilation=dil, causal=causal, global_idx=gidx,
+                                       pad_len=pads)
+    want = wantg = 0
+    for b in range(2):
+        L = n - pads[b]
+        for h in range(4):
+            local, glob = masks(n, wh[h], dil[h], causal, gidx, L)
+            for i in range(n):
+                if i in gidx:
+                    want += int(glob[i].sum())
+                    wantg += int(glob[i].sum())
+                else:
+                    want += int(local[i].sum())
+    assert (pairs, gpairs) == (want, wantg)
